@@ -1,0 +1,210 @@
+"""Plain fp64 CPU oracle for the paged KV-cache hot path.
+
+TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+baseline / reference arm may import this module; the library never does, and
+it shares no code with the CUDA path.
+
+Each function is the plain definition of one step, written from the pages:
+
+* slot mapping: logical block floor(t/B), offset t mod B, physical id from the
+  block table ("PagedAttention: Virtual-Memory KV Cache Management, Continuous
+  Batching, and PyTorch Architecture", ailinkdeeptech.com, §1 Paged Virtual
+  Memory Mapping; "PagedAttention: Manage the Cache Without Moving the
+  Sequence", neelmishra.github.io, §Map a ten-token sequence into pages);
+* KV write: the new token's k, v go to slot len % b of the last block
+  ("PagedAttention: paging the KV cache", pofe.ai, §How it works and §Minimal
+  implementation);
+* block copy for copy-on-write: the whole block, K and V, every layer (pofe.ai
+  §Sharing and copy-on-write; ailinkdeeptech.com §4, step 2);
+* decode attention: gather the sequence's K and V through its block table, then
+  textbook softmax attention (pofe.ai §Minimal implementation gather; "the math
+  is unchanged; only the addresses are indirect", pofe.ai §How it works;
+  ailinkdeeptech.com §3 standard attention softmax(QK^T/sqrt(d_k))V). Query
+  head h reads KV head h // g with g = H_q / H_kv (repeat_interleave grouping,
+  ailinkdeeptech.com Step 2 and pofe.ai §Minimal implementation).
+* the blockwise online-softmax recurrence and the partition-combine rule of
+  ailinkdeeptech.com §3 (running max m, normaliser l, unnormalised o), used to
+  pin the split-K reduction.
+
+Half-precision inputs arrive as uint16 bit patterns and are widened exactly to
+fp64 before any arithmetic. Parity unpinned: none (every function is checked
+against the pages' worked values, closed forms, library routines or
+invariants by the CPU tests).
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------
+# exact widening of stored values
+
+
+def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact fp64 value of fp16 / bf16 bit patterns."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+# ----------------------------------------------------------------------------
+# slot mapping (integer)
+
+
+def slot_mapping(block_tables: np.ndarray, seq_idx: Sequence[int], positions: Sequence[int],
+                 block_size: int) -> np.ndarray:
+    """slot = table[s][t // B] * B + t % B for every (s, t) pair.
+
+    Logical block i = floor(t / B), offset j = t mod B, physical block B(i) from
+    the sequence's table; a slot numbers rows of the pool, block-major.
+    """
+    out = np.empty(len(positions), dtype=np.int64)
+    for n, (s, t) in enumerate(zip(seq_idx, positions)):
+        i, j = int(t) // block_size, int(t) % block_size
+        out[n] = int(block_tables[int(s)][i]) * block_size + j
+    return out
+
+
+# ----------------------------------------------------------------------------
+# KV write and block copy (bytes)
+
+
+def write_kv(k_cache: np.ndarray, v_cache: np.ndarray, key: np.ndarray, value: np.ndarray,
+             slots: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
+    """New caches with row ``slot`` of the pool set to each token's k and v.
+
+    Caches are ``[num_blocks, B, H_kv, D]``; slot s is block s // B, row s % B.
+    A slot of -1 marks a padding token and writes nothing.
+    """
+    k = k_cache.copy()
+    v = v_cache.copy()
+    b = k.shape[1]
+    for n, s in enumerate(slots):
+        s = int(s)
+        if s < 0:
+            continue
+        k[s // b, s % b] = key[n]
+        v[s // b, s % b] = value[n]
+    return k, v
+
+
+def copy_blocks(k_caches: Sequence[np.ndarray], v_caches: Sequence[np.ndarray],
+                pairs: Iterable[Tuple[int, int]]) -> Tuple[List[np.ndarray], List[np.ndarray]]:
+    """New caches where block dst holds a copy of block src, for every layer."""
+    ks = [k.copy() for k in k_caches]
+    vs = [v.copy() for v in v_caches]
+    for src, dst in pairs:
+        for k, v in zip(ks, vs):
+            k[int(dst)] = k[int(src)]
+            v[int(dst)] = v[int(src)]
+    return ks, vs
+
+
+# ----------------------------------------------------------------------------
+# decode attention (fp64)
+
+
+def gather_kv(cache: np.ndarray, table_row: Sequence[int], length: int, kv_head: int) -> np.ndarray:
+    """The first ``length`` rows of one KV head, in logical order.
+
+    Blocks ``table_row[:ceil(length / B)]`` are gathered, flattened to token
+    rows and cut at the sequence length, so slots past the length are never
+    read.
+    """
+    b = cache.shape[1]
+    nblk = -(-length // b)
+    idx = np.asarray(table_row[:nblk], dtype=np.int64)
+    rows = cache[idx].reshape(nblk * b, cache.shape[2], cache.shape[3])
+    return rows[:length, kv_head]
+
+
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """softmax(scale * q K^T) V for query rows q [g, D] over keys K, V [L, D]."""
+    x = scale * (q @ K.T)
+    x = x - x.max(axis=1, keepdims=True)
+    p = np.exp(x)
+    p = p / p.sum(axis=1, keepdims=True)
+    return p @ V
+
+
+def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
+           seq_lens: Sequence[int], scale: float, dtype: str,
+           pairs: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+    """Decode attention for every (sequence, query head), or for ``pairs`` only.
+
+    Returns fp64 ``[N, H_q, D]``; rows not in ``pairs`` are NaN. A sequence of
+    length 0 attends to nothing and yields zeros.
+    """
+    n, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    g = hq // hkv
+    out = np.full((n, hq, d), np.nan)
+    if pairs is None:
+        want = {(s, kvh): list(range(kvh * g, (kvh + 1) * g)) for s in range(n) for kvh in range(hkv)}
+    else:
+        want = {}
+        for s, h in pairs:
+            want.setdefault((int(s), int(h) // g), []).append(int(h))
+    for (s, kvh), heads in want.items():
+        L = int(seq_lens[s])
+        if L == 0:
+            out[s, heads] = 0.0
+            continue
+        K = bits_to_f64(gather_kv(k_cache, block_tables[s], L, kvh), dtype)
+        V = bits_to_f64(gather_kv(v_cache, block_tables[s], L, kvh), dtype)
+        Q = bits_to_f64(q[s, heads], dtype)
+        out[s, heads] = attention(Q, K, V, scale)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# blockwise online softmax and the partition combine
+
+
+def online_softmax_blocks(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
+                          block_size: int) -> np.ndarray:
+    """The per-block recurrence: running max m, normaliser l, accumulator o.
+
+    For each block of B keys: S = scale q K_b^T (masked to the sequence),
+    m_new = max(m, max S), P = exp(S - m_new), l = l exp(m - m_new) + sum P,
+    o = o exp(m - m_new) + P V_b, m = m_new; finally O = o / l.
+    """
+    L = K.shape[0]
+    m = -math.inf
+    l = 0.0
+    o = np.zeros(V.shape[1])
+    for start in range(0, L, block_size):
+        S = scale * (K[start:start + block_size] @ q)
+        m_new = max(m, float(S.max()))
+        P = np.exp(S - m_new)
+        alpha = math.exp(m - m_new) if m != -math.inf else 0.0
+        l = l * alpha + float(P.sum())
+        o = o * alpha + P @ V[start:start + block_size]
+        m = m_new
+    return o / l
+
+
+def partition_state(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float
+                    ) -> Tuple[float, float, np.ndarray]:
+    """(m, l, o) of one token range: max logit, sum of exp(S - m), unnormalised output."""
+    S = scale * (K @ q)
+    m = float(S.max())
+    P = np.exp(S - m)
+    return m, float(P.sum()), P @ V
+
+
+def combine_partitions(states: Sequence[Tuple[float, float, np.ndarray]]) -> np.ndarray:
+    """Merge per-range (m, l, o) states with the rescale identity.
+
+    M = max m_p, l = sum l_p exp(m_p - M), O = sum o_p exp(m_p - M) / l.
+    """
+    M = max(s[0] for s in states)
+    l = sum(s[1] * math.exp(s[0] - M) for s in states)
+    o = sum(s[2] * math.exp(s[0] - M) for s in states)
+    return o / l

@@ -1,0 +1,347 @@
+"""Seeded synthetic workloads shaped like the pages' decode scenarios.
+
+Every array is generated on the host with ``numpy.random.default_rng`` and a
+fixed seed, so the GPU path and the oracle see identical bytes on any machine.
+Half-precision tensors are carried as ``uint16`` bit patterns (fp16 or bf16).
+
+Recipe (shared by every config):
+
+* ``q`` and the K/V rows the scenario writes are drawn N(0,1) and rounded to
+  the storage dtype (round-to-nearest-even).
+* Pool blocks that hold a sequence's tokens are filled with N(0,1) values. Each
+  block is a window, at a seeded random offset, into one 2**24-element N(0,1)
+  sample (drawing >1e9 normals per workload on the host is too slow).
+* Every slot that no sequence owns holds a quiet-NaN pattern: unused blocks and
+  the tail rows of each sequence's last block. A kernel that lets any of them
+  into its arithmetic produces NaN, so masking is checked at every size.
+* Physical placement comes from :mod:`workloads.block_manager` with a seeded
+  shuffle of the free list; block tables are zero padded to the longest table.
+
+Five named configs follow the decode scenarios the pages discuss: a tiny case
+holding the ten-token, b=4, table [7, 2, 11] example; a 7B/13B-style MHA batch;
+the 70B GQA head shape (80 layers, 8 KV heads, head_dim 128) timed per layer;
+a 32k-token long-context batch for split-K; and a shared 1000-token prefix with
+copy-on-write.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+from .block_manager import BlockPool, SeqTable
+
+NAN_BITS = {"f16": np.uint16(0x7E00), "bf16": np.uint16(0x7FC0)}
+_BASE_LEN = 1 << 24
+
+CONFIG_NAMES = {
+    1: "tiny_b4_fp16",
+    2: "mha_7b13b_fp16_b16",
+    3: "gqa_70b_bf16_b16",
+    4: "long32k_splitk_bf16",
+    5: "prefix_cow_fp16_b16",
+}
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even) and return the bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + rounding) >> np.uint32(16)).astype(np.uint16)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f16":
+        return f32_to_f16_bits(x)
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+@dataclass
+class Workload:
+    """All host-side inputs of one scenario.
+
+    Layouts: ``k_cache``/``v_cache`` are ``[num_blocks, block_size, num_kv_heads,
+    head_dim]``; ``q`` is ``[num_seqs, num_q_heads, head_dim]``; ``key``/``value``
+    are ``[num_tokens, num_kv_heads, head_dim]``; ``block_tables`` is
+    ``int32[num_seqs, max_blocks_per_seq]``.
+
+    The scenario is: block copies ``copy_pairs`` (copy-on-write), then the write
+    of ``key``/``value`` for the tokens ``(seq_idx, positions)``, then decode of
+    every sequence at length ``seq_lens``.
+    """
+    name: str
+    dtype: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    q: np.ndarray
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    block_tables: np.ndarray
+    seq_lens: np.ndarray
+    key: np.ndarray
+    value: np.ndarray
+    seq_idx: np.ndarray
+    positions: np.ndarray
+    copy_pairs: np.ndarray
+    partition_tokens: int = 0
+    shared_blocks: List[int] = field(default_factory=list)
+    meta: Dict[str, object] = field(default_factory=dict)
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.seq_lens.size else 0
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+
+def decode_step_tokens(w: Workload) -> np.ndarray:
+    """Indices (into key/value) of each sequence's newest token, position L-1.
+
+    A decode step writes exactly these rows and then attends over L tokens.
+    """
+    last = {}
+    for i, (s, t) in enumerate(zip(w.seq_idx.tolist(), w.positions.tolist())):
+        if t == int(w.seq_lens[s]) - 1:
+            last[s] = i
+    return np.array([last[s] for s in sorted(last)], dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# helpers
+
+
+class _Filler:
+    """Fills pool blocks with windows of one N(0,1) sample."""
+
+    def __init__(self, rng: np.random.Generator, dtype: str) -> None:
+        self.rng = rng
+        self.base = to_bits(rng.standard_normal(_BASE_LEN, dtype=np.float32), dtype)
+
+    def block(self, n: int) -> np.ndarray:
+        off = int(self.rng.integers(0, _BASE_LEN - n))
+        return self.base[off:off + n]
+
+
+def _normal_bits(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
+    return to_bits(rng.standard_normal(shape, dtype=np.float32), dtype)
+
+
+def _pad_tables(tables: Sequence[Sequence[int]], pad: int) -> np.ndarray:
+    width = max(1, max((len(t) for t in tables), default=1))
+    out = np.full((len(tables), width), pad, dtype=np.int32)
+    for i, t in enumerate(tables):
+        out[i, :len(t)] = t
+    return out
+
+
+def _fill_sequences(k: np.ndarray, v: np.ndarray, tables, lens, filler_k: _Filler,
+                    filler_v: _Filler, nan: np.uint16, skip_blocks=()) -> None:
+    """Give every block a sequence owns N(0,1) rows; NaN rows past the length."""
+    b = k.shape[1]
+    per_block = int(np.prod(k.shape[1:]))
+    done = set(skip_blocks)
+    for table, L in zip(tables, lens):
+        nblk = -(-int(L) // b)
+        for j in range(nblk):
+            blk = int(table[j])
+            if blk in done:
+                continue
+            done.add(blk)
+            k[blk] = filler_k.block(per_block).reshape(k.shape[1:])
+            v[blk] = filler_v.block(per_block).reshape(v.shape[1:])
+            valid = int(L) - j * b
+            if valid < b:
+                k[blk, valid:] = nan
+                v[blk, valid:] = nan
+
+
+def _new_pool(nb: int, b: int, hkv: int, d: int, dtype: str):
+    nan = NAN_BITS[dtype]
+    k = np.full((nb, b, hkv, d), nan, dtype=np.uint16)
+    v = np.full((nb, b, hkv, d), nan, dtype=np.uint16)
+    return k, v, nan
+
+
+# ----------------------------------------------------------------------------
+# generic random case (tests)
+
+
+def make_random_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                     head_dim: int, block_size: int, seq_lens: Sequence[int],
+                     dtype: str = "f16", pool_factor: float = 1.25, pad: int = 0,
+                     scale: Optional[float] = None, partition_tokens: int = 0,
+                     name: str = "random") -> Workload:
+    """A decode batch with given lengths and a shuffled pool.
+
+    The scenario writes each sequence's newest token (position L-1) and decodes.
+    Sequences of length 0 own no block and write nothing.
+    """
+    rng = np.random.default_rng(seed)
+    b = block_size
+    lens = [int(x) for x in seq_lens]
+    assert len(lens) == num_seqs
+    need = sum(-(-L // b) for L in lens)
+    nb = max(1, int(np.ceil(pool_factor * need)))
+    pool = BlockPool(nb, b, free_order=rng.permutation(nb))
+    seqs = []
+    for L in lens:
+        s = SeqTable(pool)
+        s.admit(L)
+        seqs.append(s)
+    tables = [s.table for s in seqs]
+    k, v, nan = _new_pool(nb, b, num_kv_heads, head_dim, dtype)
+    fk, fv = _Filler(rng, dtype), _Filler(rng, dtype)
+    _fill_sequences(k, v, tables, lens, fk, fv, nan)
+    q = _normal_bits(rng, (num_seqs, num_q_heads, head_dim), dtype)
+    writers = [i for i, L in enumerate(lens) if L > 0]
+    key = _normal_bits(rng, (len(writers), num_kv_heads, head_dim), dtype)
+    value = _normal_bits(rng, (len(writers), num_kv_heads, head_dim), dtype)
+    return Workload(
+        name=name, dtype=dtype, num_seqs=num_seqs, num_q_heads=num_q_heads,
+        num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=b, num_blocks=nb,
+        scale=float(scale if scale is not None else 1.0 / np.sqrt(head_dim)),
+        q=q, k_cache=k, v_cache=v, block_tables=_pad_tables(tables, pad),
+        seq_lens=np.array(lens, dtype=np.int32), key=key, value=value,
+        seq_idx=np.array(writers, dtype=np.int32),
+        positions=np.array([lens[i] - 1 for i in writers], dtype=np.int32),
+        copy_pairs=np.zeros((0, 2), dtype=np.int64), partition_tokens=partition_tokens)
+
+
+# ----------------------------------------------------------------------------
+# the five named configs
+
+
+def _config1(rng: np.random.Generator) -> Workload:
+    """Tiny: 4 sequences {10,1,16,33}, 4/4 heads, d=64, b=4, 64 blocks, fp16.
+
+    Sequence 0 holds the ten-token example with block table [7, 2, 11]. The pool
+    starts as NaN; one write of all 60 tokens fills it, then decode runs.
+    """
+    lens = [10, 1, 16, 33]
+    n, hq, hkv, d, b, nb = 4, 4, 4, 64, 4, 64
+    pool = BlockPool(nb, b, free_order=rng.permutation(nb))
+    s0 = SeqTable(pool)
+    s0.table = [pool.take(7), pool.take(2), pool.take(11)]
+    s0.length = 10
+    seqs = [s0]
+    for L in lens[1:]:
+        s = SeqTable(pool)
+        s.admit(L)
+        seqs.append(s)
+    k, v, _ = _new_pool(nb, b, hkv, d, "f16")
+    total = sum(lens)
+    seq_idx = np.concatenate([np.full(L, i, dtype=np.int32) for i, L in enumerate(lens)])
+    positions = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    return Workload(
+        name=CONFIG_NAMES[1], dtype="f16", num_seqs=n, num_q_heads=hq, num_kv_heads=hkv,
+        head_dim=d, block_size=b, num_blocks=nb, scale=1.0 / np.sqrt(d),
+        q=_normal_bits(rng, (n, hq, d), "f16"), k_cache=k, v_cache=v,
+        block_tables=_pad_tables([s.table for s in seqs], 0),
+        seq_lens=np.array(lens, dtype=np.int32),
+        key=_normal_bits(rng, (total, hkv, d), "f16"),
+        value=_normal_bits(rng, (total, hkv, d), "f16"),
+        seq_idx=seq_idx, positions=positions,
+        copy_pairs=np.zeros((0, 2), dtype=np.int64), partition_tokens=0)
+
+
+def _decode_batch(rng, name, *, n, hq, hkv, d, b, dtype, lens, partition_tokens) -> Workload:
+    w = make_random_case(int(rng.integers(0, 2**31)), num_seqs=n, num_q_heads=hq,
+                         num_kv_heads=hkv, head_dim=d, block_size=b, seq_lens=lens,
+                         dtype=dtype, partition_tokens=partition_tokens, name=name)
+    return w
+
+
+def _config5(rng: np.random.Generator) -> Workload:
+    """256 sequences sharing one 1000-token prefix, private suffixes U[16,512].
+
+    The prefix fills 62 full blocks and 8 rows of a 63rd. Each sequence's first
+    suffix token lands in that shared partial block, so all but the last writer
+    copy it first (255 copy-on-write pairs). The scenario then writes every
+    suffix token and decodes.
+    """
+    n, hq, hkv, d, b, dtype = 256, 32, 8, 128, 16, "f16"
+    prefix = 1000
+    suffix = rng.integers(16, 512, size=n, endpoint=True)
+    need = 63 + sum(-(-(prefix + int(s)) // b) - 62 for s in suffix)
+    nb = int(np.ceil(1.25 * need))
+    pool = BlockPool(nb, b, free_order=rng.permutation(nb))
+    root = SeqTable(pool)
+    root.admit(prefix)
+    prefix_blocks = list(root.table)
+    seqs = [root.fork() for _ in range(n)]
+    root.free()
+    pairs = []
+    seq_idx, positions = [], []
+    for i, s in enumerate(seqs):
+        for _ in range(int(suffix[i])):
+            seq_idx.append(i)
+            positions.append(s.length)
+            p = s.append()
+            if p is not None:
+                pairs.append(p)
+    k, v, nan = _new_pool(nb, b, hkv, d, dtype)
+    fk, fv = _Filler(rng, dtype), _Filler(rng, dtype)
+    _fill_sequences(k, v, [prefix_blocks], [prefix], fk, fv, nan)
+    lens = [prefix + int(s) for s in suffix]
+    total = len(seq_idx)
+    return Workload(
+        name=CONFIG_NAMES[5], dtype=dtype, num_seqs=n, num_q_heads=hq, num_kv_heads=hkv,
+        head_dim=d, block_size=b, num_blocks=nb, scale=1.0 / np.sqrt(d),
+        q=_normal_bits(rng, (n, hq, d), dtype), k_cache=k, v_cache=v,
+        block_tables=_pad_tables([s.table for s in seqs], 0),
+        seq_lens=np.array(lens, dtype=np.int32),
+        key=_normal_bits(rng, (total, hkv, d), dtype),
+        value=_normal_bits(rng, (total, hkv, d), dtype),
+        seq_idx=np.array(seq_idx, dtype=np.int32), positions=np.array(positions, dtype=np.int32),
+        copy_pairs=np.array(pairs, dtype=np.int64).reshape(-1, 2), partition_tokens=512,
+        shared_blocks=prefix_blocks[:62],
+        meta={"prefix_tokens": prefix, "suffix_tokens": suffix.astype(np.int64)})
+
+
+def make_config(cid: int, *, block_size: Optional[int] = None) -> Workload:
+    """Build named config ``cid`` (1..5). ``block_size`` overrides config 4's b."""
+    rng = np.random.default_rng(1000 + cid)
+    if cid == 1:
+        return _config1(rng)
+    if cid == 2:
+        lens = rng.integers(128, 2048, size=64, endpoint=True)
+        return _decode_batch(rng, CONFIG_NAMES[2], n=64, hq=32, hkv=32, d=128, b=16,
+                             dtype="f16", lens=lens, partition_tokens=512)
+    if cid == 3:
+        lens = rng.integers(512, 8192, size=128, endpoint=True)
+        return _decode_batch(rng, CONFIG_NAMES[3], n=128, hq=64, hkv=8, d=128, b=16,
+                             dtype="bf16", lens=lens, partition_tokens=512)
+    if cid == 4:
+        b = 32 if block_size is None else int(block_size)
+        name = CONFIG_NAMES[4] + f"_b{b}"
+        return _decode_batch(rng, name, n=8, hq=32, hkv=8, d=128, b=b, dtype="bf16",
+                             lens=[32768] * 8, partition_tokens=512)
+    if cid == 5:
+        return _config5(rng)
+    raise ValueError(f"unknown config {cid}")
