@@ -1,0 +1,549 @@
+"""Benchmark of the paged decode hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one decode batch: slot mapping
+of each sequence's new token, the slot-mapped KV write, and decode attention
+through the block tables (split-K partitions plus the reduce). Inputs are
+resident in HBM when the timed region starts; the pool (about 1.4 GB for the
+default workload) is far larger than L2, so no flush is needed between steps.
+
+value  = algorithmic bytes of a step x steps x ranks / max-over-ranks time, GB/s
+e2e    = the same metric through the same calls with pinned host buffers:
+         every step copies its inputs host -> device and reads the output back.
+roofline = decode call only (partition kernel + reduce): algorithmic bytes per
+         call / mean call time from CUDA events on the launching stream.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention achieved HBM GB/s (% of peak) and decode tokens/s"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+KERNEL_SOURCES = ["pa_decode.cuh", "pa_ptx.cuh", "pa_decode_reduce.cu", "pa_decode_inst.cu",
+                  "pa_internal.h"]
+
+
+# ----------------------------------------------------------------------------- accounting
+
+
+def step_tokens(w):
+    """Indices of the rows a timed step writes: each sequence's newest token
+    (config 1 writes its whole scenario, all 60 tokens)."""
+    from workloads import decode_step_tokens
+    if w.name.startswith("tiny"):
+        return np.arange(len(w.positions))
+    return decode_step_tokens(w)
+
+
+def decode_bytes(w, out_elem=4):
+    """Algorithmic bytes of one decode call: every valid K and V row once, q,
+    the output, the table entries the lengths cover, and the lengths."""
+    L = w.seq_lens.astype(np.int64)
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    q = w.num_seqs * w.num_q_heads * w.head_dim * 2
+    out = w.num_seqs * w.num_q_heads * w.head_dim * out_elem
+    tables = int((-(-L // w.block_size)).sum()) * 4
+    return kv + q + out + tables + 4 * w.num_seqs
+
+
+def unique_decode_bytes(w):
+    """Like decode_bytes but counting shared prefix blocks once (config 5)."""
+    if not w.shared_blocks:
+        return decode_bytes(w)
+    shared_tokens = len(w.shared_blocks) * w.block_size
+    L = w.seq_lens.astype(np.int64)
+    row = w.num_kv_heads * w.head_dim * 2 * 2
+    return decode_bytes(w) - (w.num_seqs - 1) * shared_tokens * row
+
+
+def write_bytes(w, n_tokens):
+    """Slot mapping (ids, positions, table entries in; slots out) and the KV write
+    (key/value rows read once, written once)."""
+    row = w.num_kv_heads * w.head_dim * 2
+    return n_tokens * (4 + 4 + 4 + 8) + n_tokens * (8 + 2 * row + 2 * row)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_114_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, partition):
+    """DRAM bytes per decode call from the committed ncu summary, or None when
+    the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_hash") != kernel_hash():
+        return None
+    entry = rec.get("workloads", {}).get(f"{workload}/p{partition}")
+    return None if entry is None else int(entry["dram_bytes_per_call"])
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+class Run:
+    """One workload resident on the device, with the step's inputs."""
+
+    def __init__(self, w, dev, partition):
+        import torch
+
+        import paged_kv_cache_114_gb300 as pa
+        self.w, self.dev, self.pa, self.torch = w, dev, pa, torch
+        self.k = to_dev(w.k_cache, dev, w.dtype)
+        self.v = to_dev(w.v_cache, dev, w.dtype)
+        self.tables = to_dev(w.block_tables, dev)
+        self.lens = to_dev(w.seq_lens, dev)
+        self.q = to_dev(w.q, dev, w.dtype)
+        idx = step_tokens(w)
+        # scenario rows written before timing (config 5's suffixes, after its copies)
+        setup = np.setdiff1d(np.arange(len(w.positions)), idx)
+        if len(w.copy_pairs):
+            pa.copy_blocks([self.k], [self.v], to_dev(w.copy_pairs, dev))
+        if len(setup):
+            sl = pa.slot_mapping(self.tables, to_dev(w.seq_idx[setup], dev),
+                                 to_dev(w.positions[setup], dev), w.block_size, w.num_blocks)
+            pa.write_kv(to_dev(w.key[setup], dev, w.dtype), to_dev(w.value[setup], dev, w.dtype),
+                        sl, self.k, self.v)
+        self.host = {
+            "seq_idx": w.seq_idx[idx], "positions": w.positions[idx],
+            "key": w.key[idx], "value": w.value[idx],
+        }
+        self.seq_idx = to_dev(self.host["seq_idx"], dev)
+        self.positions = to_dev(self.host["positions"], dev)
+        self.key = to_dev(self.host["key"], dev, w.dtype)
+        self.value = to_dev(self.host["value"], dev, w.dtype)
+        self.n_tokens = len(idx)
+        self.slots = torch.empty(self.n_tokens, dtype=torch.int64, device=dev)
+        self.out = torch.empty(self.q.shape, dtype=torch.float32, device=dev)
+        self.partition = partition
+        ws = pa.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim, w.max_seq_len, partition)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.launches_per_step = 3 + (1 if ws else 0)
+
+    def decode(self, q=None, lens=None, tables=None, out=None):
+        return self.pa.decode(self.q if q is None else q, self.k, self.v,
+                              self.tables if tables is None else tables,
+                              self.lens if lens is None else lens, self.w.scale,
+                              max_seq_len=self.w.max_seq_len, out=self.out if out is None else out,
+                              partition_tokens=self.partition, workspace=self.ws)
+
+    def step(self, ev=None):
+        pa = self.pa
+        pa.slot_mapping(self.tables, self.seq_idx, self.positions, self.w.block_size,
+                        self.w.num_blocks, out=self.slots)
+        pa.write_kv(self.key, self.value, self.slots, self.k, self.v)
+        if ev is not None:
+            ev[0].record()
+        self.decode()
+        if ev is not None:
+            ev[1].record()
+
+
+def to_dev(a, dev, dtype=None):
+    """Host numpy array -> device tensor (fp16/bf16 bit patterns viewed as that dtype)."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if dtype is not None:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(
+            torch.float16 if dtype == "f16" else torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (identity on one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_gpu(args):
+    import torch
+
+    from workloads import CONFIG_NAMES, make_config
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import paged_kv_cache_114_gb300 as pa
+    pa.lib()
+
+    w = make_config(args.config, block_size=args.block_size) if args.config == 4 else make_config(args.config)
+    partition = args.partition if args.partition is not None else pa.default_partition(
+        w.num_seqs, w.num_kv_heads, w.max_seq_len, w.block_size)
+    run = Run(w, dev, partition)
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error during setup")
+
+    step_bytes = write_bytes(w, run.n_tokens) + decode_bytes(w)
+    dec_bytes = decode_bytes(w)
+    K, W = args.steps, args.warmup
+
+    for _ in range(W):
+        run.step()
+    torch.cuda.synchronize()
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error during warm-up")
+
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for i in range(K):
+            run.step(evs[i])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = reduce_max(e0.elapsed_time(e1), world, dev)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    err = pa.get_device_error(dev)
+    if err:
+        raise RuntimeError(f"device error word {err} after the timed region")
+
+    ms_step = ms_total / K
+    value = step_bytes * K * world / (ms_total / 1e3) / 1e9
+    tok_s = w.num_seqs * K * world / (ms_total / 1e3)
+
+    # ---- end to end: pinned host inputs in, output back to the host, every step
+    e2e = run_e2e(run, K, W, world, dev, step_bytes)
+
+    peak, peak_kind = measured_peaks()
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    workload = f"{w.name}"
+    traffic = recorded_traffic(workload, partition)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy rate)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "frac_of_8tbs_spec": round(achieved / SPEC_HBM_GBS, 4),
+                "kernel": "pa_decode: partition kernel + reduce" if run.ws.numel() > 16 else "pa_decode",
+                "algorithmic_bytes_per_call": dec_bytes, "mean_call_us": round(dec_ms * 1e3, 2)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {
+            "workload": workload,
+            "shape": f"{w.num_seqs} seqs, {w.num_q_heads} q heads / {w.num_kv_heads} kv heads, "
+                     f"head_dim {w.head_dim}, block {w.block_size}, seq_len {int(w.seq_lens.min())}.."
+                     f"{int(w.seq_lens.max())} (mean {float(w.seq_lens.mean()):.0f})",
+            "step": "pa_slot_mapping + pa_write_kv (one new token per sequence) + pa_decode",
+            "partition_tokens": partition,
+            "pool_bytes": int(w.k_cache.nbytes + w.v_cache.nbytes),
+            "l2": "inputs larger than L2: the K/V pool far exceeds the 129 MB L2; no flush",
+            "algorithmic_bytes_per_step": step_bytes,
+            "parallelism": f"{world} independent replica(s), no collective",
+        },
+        "decode_tok_s": round(tok_s, 1),
+        "decode_tok_s_note": "attention-only, one layer: sequences decoded per second",
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": run.launches_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if w.shared_blocks:
+        line["config"]["unique_decode_bytes"] = unique_decode_bytes(w)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_child(args.config, args.block_size, "cpu_baseline")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(run, K, W, world, dev, step_bytes):
+    """Same step through the public API with pinned host buffers; every step
+    copies its inputs to the device and reads the output back."""
+    import torch
+    w = run.w
+    pin = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if dt else
+                                              np.ascontiguousarray(a)).pin_memory()
+    h = {
+        "q": pin(w.q, 1), "key": pin(run.host["key"], 1), "value": pin(run.host["value"], 1),
+        "seq_idx": pin(run.host["seq_idx"]), "positions": pin(run.host["positions"]),
+        "tables": pin(w.block_tables), "lens": pin(w.seq_lens),
+    }
+    out_host = torch.empty(run.out.shape, dtype=torch.float32).pin_memory()
+    tdt = run.q.dtype
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out_host.numel() * out_host.element_size()
+    pa = run.pa
+
+    def one():
+        d = {k: t.to(dev, non_blocking=True) for k, t in h.items()}
+        q = d["q"].view(tdt)
+        key, value = d["key"].view(tdt), d["value"].view(tdt)
+        pa.slot_mapping(d["tables"], d["seq_idx"], d["positions"], w.block_size, w.num_blocks,
+                        out=run.slots)
+        pa.write_kv(key, value, run.slots, run.k, run.v)
+        run.decode(q=q, lens=d["lens"], tables=d["tables"])
+        out_host.copy_(run.out, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(W):
+        one()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    t1 = time.perf_counter()
+    barrier(world)
+    secs = reduce_max(t1 - t0, world, dev)
+    return {"value": round(step_bytes * K * world / secs / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(secs / K * 1e3, 5)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample_step(w, seqs, state):
+    """One oracle step on a sample of sequences: slot mapping and write of their
+    newest tokens, then decode of all their heads."""
+    import oracle
+    idx = step_tokens(w)
+    mine = [i for i in idx if int(w.seq_idx[i]) in set(seqs)]
+    slots = oracle.slot_mapping(w.block_tables, w.seq_idx[mine], w.positions[mine], w.block_size)
+    k, v = oracle.write_kv(state["k"], state["v"], w.key[mine], w.value[mine], slots)
+    heads = [(s, h) for s in seqs for h in range(w.num_q_heads)]
+    oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, pairs=heads)
+    return len(mine)
+
+
+def sample_bytes(w, seqs, n_tok):
+    L = w.seq_lens[list(seqs)].astype(np.int64)
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 4
+    q = len(seqs) * w.num_q_heads * w.head_dim * (2 + 4)
+    tables = int((-(-L // w.block_size)).sum()) * 4 + 4 * len(seqs)
+    return kv + q + tables + write_bytes(w, n_tok)
+
+
+def prepared_oracle_state(w):
+    """The pool as the timed steps see it (config 5: copies and suffix writes applied)."""
+    import oracle
+    k, v = w.k_cache, w.v_cache
+    idx = step_tokens(w)
+    setup = np.setdiff1d(np.arange(len(w.positions)), idx)
+    if len(w.copy_pairs):
+        ks, vs = oracle.copy_blocks([k], [v], [tuple(p) for p in w.copy_pairs.tolist()])
+        k, v = ks[0], vs[0]
+    if len(setup):
+        sl = oracle.slot_mapping(w.block_tables, w.seq_idx[setup], w.positions[setup], w.block_size)
+        k, v = oracle.write_kv(k, v, w.key[setup], w.value[setup], sl)
+    return {"k": k, "v": v}
+
+
+def cpu_baseline_child(config, block_size, mode, steps=0, warmup=0):
+    """Runs the oracle timing in a fresh single-threaded process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-child", mode, "--config", str(config),
+           "--steps", str(steps), "--warmup", str(warmup)]
+    if block_size is not None:
+        cmd += ["--block-size", str(block_size)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "error": r.stderr.strip().splitlines()[-1:] or ["failed"]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_child(args):
+    """Oracle timing: 'cpu_baseline' = one bounded sample (~10-30 s); 'reference'
+    = the reference arm's K + W steps, each a bounded sample."""
+    from workloads import make_config
+    w = make_config(args.config, block_size=args.block_size) if args.config == 4 else make_config(args.config)
+    state = prepared_oracle_state(w)
+    order = np.argsort(w.seq_lens)[::-1] if w.num_seqs > 1 else np.arange(1)
+    rng = np.random.default_rng(0)
+    if args.cpu_child == "cpu_baseline":
+        budget, done_b, t_used, seqs_done = 12.0, 0, 0.0, 0
+        perm = rng.permutation(w.num_seqs)
+        for s in perm:
+            t0 = time.perf_counter()
+            n_tok = oracle_sample_step(w, [int(s)], state)
+            t_used += time.perf_counter() - t0
+            done_b += sample_bytes(w, [int(s)], n_tok)
+            seqs_done += 1
+            if t_used >= budget:
+                break
+        res = {"value": round(done_b / t_used / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{seqs_done} of {w.num_seqs} sequences (random order), all heads, "
+                         f"their new-token writes; {t_used:.1f} s of single-thread CPU time"}
+        print(json.dumps(res))
+        return
+    # reference arm: W + K steps, each one random sequence
+    total_b, total_t = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        s = int(rng.integers(0, w.num_seqs))
+        t0 = time.perf_counter()
+        n_tok = oracle_sample_step(w, [s], state)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            total_b += sample_bytes(w, [s], n_tok)
+            total_t += dt
+    print(json.dumps({"value": round(total_b / total_t / 1e9, 4), "ms_per_step": total_t / max(args.steps, 1) * 1e3,
+                      "sample": f"each step: one random sequence of {w.num_seqs}, all heads"}))
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    from workloads import CONFIG_NAMES
+    res = cpu_baseline_child(args.config, args.block_size, "reference", args.steps, args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": res.get("value"), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res.get("ms_per_step"), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": CONFIG_NAMES[args.config],
+                   "note": "the pages publish no runnable reference; this arm times the fp64 CPU oracle"},
+        "cpu_baseline": {"value": res.get("value"), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": res.get("sample")},
+        "e2e": {"value": res.get("value"), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--block-size", type=int, default=None, help="config 4 block size (8/16/32)")
+    ap.add_argument("--partition", type=int, default=None, help="split-K partition tokens (default: library's)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-child", choices=["cpu_baseline", "reference"], default=None,
+                    help=argparse.SUPPRESS)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.cpu_child is None and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.cpu_child:
+        return cpu_child(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * pa.h - C ABI of libpagedkv: the device hot path of PagedAttention on one GB300.
+ *
+ * A sequence's KV cache lives in fixed-size blocks of a shared pool; a block
+ * table maps its logical block floor(t/b) to a physical block id and token t
+ * sits at row t mod b of that block ("PagedAttention: paging the KV cache",
+ * pofe.ai, section "How it works"; "PagedAttention: Virtual-Memory KV Cache
+ * Management, Continuous Batching, and PyTorch Architecture", ailinkdeeptech.com,
+ * section "Mathematical Foundations", 1. Paged Virtual Memory Mapping).
+ *
+ * Conventions for every call:
+ *  - All buffers are caller-owned. Pointers documented as "device" must be CUDA
+ *    device memory of the current device; "host" pointers are ordinary memory.
+ *    The library allocates no device memory and keeps only one static device
+ *    error word per device.
+ *  - Every call enqueues work on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns without synchronising, except pa_get_device_error.
+ *  - Return value: PA_OK (0) or a negative PA_ERR_* status. A negative status
+ *    means nothing was launched. Problems only the device can see (a block id
+ *    out of range, a bad length or slot) never trap: the offending row is
+ *    skipped and a PA_DEVERR_* bit is OR-ed into the device error word, which
+ *    pa_get_device_error reads and clears.
+ *
+ * Cache layout (per layer): k and v are each [num_blocks][block_size]
+ * [num_kv_heads][head_dim], row-major, fp16 or bf16; element (blk, off, h, d)
+ * is at ((blk*block_size + off)*num_kv_heads + h)*head_dim + d. A "slot" numbers
+ * pool rows: slot = blk*block_size + off. Layers are separate pools that share
+ * block ids.
+ */
+#ifndef PAGED_KV_CACHE_114_GB300_PA_H
+#define PAGED_KV_CACHE_114_GB300_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,       /* a required pointer is NULL */
+  PA_ERR_DTYPE = -2,      /* unsupported or mismatched dtype */
+  PA_ERR_SHAPE = -3,      /* unsupported head_dim, block_size, head grouping or size */
+  PA_ERR_ALIGN = -4,      /* a pointer is not aligned as documented */
+  PA_ERR_WORKSPACE = -5,  /* workspace missing or smaller than pa_decode_workspace_bytes */
+  PA_ERR_ARG = -6,        /* other invalid argument */
+  PA_ERR_CUDA = -7,       /* a CUDA runtime call failed */
+  PA_ERR_PAIRS = -8       /* copy pairs violate the distinct-destination rule */
+};
+
+/* Bits of the device error word. */
+#define PA_DEVERR_BLOCK_ID 1  /* a block id outside [0, num_blocks) in a table or pair */
+#define PA_DEVERR_SEQ_LEN 2   /* seq_len < 0 or above max_seq_len or the table's capacity */
+#define PA_DEVERR_SLOT 4      /* a slot outside [-1, num_blocks*block_size) */
+#define PA_DEVERR_POSITION 8  /* slot mapping: seq index or position outside the table */
+#define PA_DEVERR_TIMEOUT 16  /* a bounded wait for an asynchronous copy gave up */
+
+/* One layer's paged cache. k and v: device, 16-byte aligned, layout above. */
+typedef struct {
+  void* k;
+  void* v;
+  int64_t num_blocks;   /* blocks in the pool, < 2^31 */
+  int32_t block_size;   /* tokens per block b */
+  int32_t num_kv_heads; /* H_kv */
+  int32_t head_dim;     /* D */
+  pa_dtype dtype;       /* PA_F16 or PA_BF16 */
+} pa_cache;
+
+/*
+ * pa_slot_mapping - pool slot of each new token.
+ * slot[i] = block_tables[seq_idx[i]][positions[i] / block_size] * block_size
+ *           + positions[i] % block_size
+ * (ailinkdeeptech.com, 1. Paged Virtual Memory Mapping: logical block
+ * floor(t/B), offset t mod B; neelmishra.github.io "PagedAttention: Manage the
+ * Cache Without Moving the Sequence", section "Map a ten-token sequence into
+ * pages").
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]
+ *   seq_idx       device int32 [num_tokens]  sequence of each token
+ *   positions     device int32 [num_tokens]  logical position t of each token
+ *   num_blocks    pool size, used to range-check table entries
+ *   slot_mapping  device int64 [num_tokens]  output
+ * Errors: a seq index, position or table entry out of range writes slot -1 and
+ * sets PA_DEVERR_POSITION or PA_DEVERR_BLOCK_ID. num_tokens == 0 is a no-op.
+ */
+int pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                    const int32_t* seq_idx, const int32_t* positions, int64_t num_tokens,
+                    int32_t block_size, int64_t num_blocks, int64_t* slot_mapping, void* stream);
+
+/*
+ * pa_write_kv - store each new token's key and value rows at its slot.
+ * k_cache[slot / b][slot % b][h][:] = key[i][h][:], same for v (pofe.ai,
+ * sections "How it works", "write k, v of the new token into slot len(s) % b of
+ * block table[s][-1]", and "Minimal implementation", Sequence.append).
+ *   key, value    device [num_tokens][num_kv_heads][head_dim], cache dtype,
+ *                 16-byte aligned
+ *   slot_mapping  device int64 [num_tokens]; -1 marks a padding token (skipped)
+ *   cache         host pointer to one pa_cache
+ * Errors: a slot outside [-1, num_blocks*block_size) skips the token and sets
+ * PA_DEVERR_SLOT. Two tokens with the same slot race (last writer unspecified).
+ */
+int pa_write_kv(const void* key, const void* value, const int64_t* slot_mapping,
+                int64_t num_tokens, const pa_cache* cache, void* stream);
+
+/*
+ * pa_copy_blocks - copy-on-write block copies: for every (src, dst) pair and
+ * every layer, block dst of k and v becomes a copy of block src (pofe.ai,
+ * section "Sharing and copy-on-write" and Sequence.append in "Minimal
+ * implementation"; ailinkdeeptech.com section 4, Copy-on-Write step 2).
+ *   caches         host array of num_layers pa_cache (same geometry and dtype)
+ *   src_dst_pairs  device int64 [num_pairs][2]
+ * Destinations must be distinct and no destination may also be a source
+ * (copy-on-write always copies into a fresh block); pa_check_copy_pairs checks
+ * this on a host copy. Violations race. An id outside [0, num_blocks) skips the
+ * pair and sets PA_DEVERR_BLOCK_ID.
+ */
+int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* src_dst_pairs,
+                   int64_t num_pairs, void* stream);
+
+/* Host-side check of copy pairs: ids in range, distinct destinations, no
+ * destination used as a source. Returns PA_OK or PA_ERR_PAIRS / PA_ERR_NULL. */
+int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t num_blocks);
+
+/*
+ * pa_decode - single-query (decode) attention through block tables.
+ * For sequence s and query head h (KV head h / g, g = num_q_heads/num_kv_heads):
+ *   out[s][h] = sum_{t < L_s} softmax_t(scale * q[s][h] . K_s[t]) V_s[t]
+ * where K_s[t], V_s[t] are gathered at slot(s, t). The sum runs block by block
+ * with a running maximum and normaliser (ailinkdeeptech.com section 3,
+ * Non-Contiguous Online Softmax Attention Kernel; learn.pranaymahendrakar.com
+ * "PagedAttention", section "The kernel consequence"); the g query heads of a
+ * KV head share each loaded block (ailinkdeeptech.com Step 2, grouped-query
+ * ratio). Slots at t >= L_s are never part of the result.
+ *   q              device [num_seqs][num_q_heads][head_dim], cache dtype
+ *   cache          host pointer to one pa_cache; head_dim 64, 128 or 256;
+ *                  block_size a divisor of 16 or a multiple of 16
+ *   block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(L_s/b) are never read
+ *   seq_lens       device int32 [num_seqs]; 0 gives a zero output row
+ *   max_seq_len    host upper bound of seq_lens (sizes the launch)
+ *   scale          softmax scale, usually 1/sqrt(head_dim)
+ *   out            device [num_seqs][num_q_heads][head_dim] of out_dtype
+ *   partition_tokens  0: one pass per (sequence, KV head); otherwise a multiple
+ *                  of 16: split-K, each sequence cut into partitions of that
+ *                  many tokens whose (max, normaliser, unnormalised output)
+ *                  partials a second kernel merges with the rescale identity
+ *   workspace      device, >= pa_decode_workspace_bytes(...) bytes, 16-byte
+ *                  aligned; unused (may be NULL) when no sequence needs more
+ *                  than one partition
+ * Errors (device): L_s outside [0, min(max_seq_len, max_blocks_per_seq*b)]
+ * sets PA_DEVERR_SEQ_LEN and is clamped; a table entry out of range sets
+ * PA_DEVERR_BLOCK_ID and its tokens are left out.
+ */
+int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cache* cache,
+              const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+              int32_t max_seq_len, float scale, void* out, pa_dtype out_dtype,
+              int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes pa_decode needs for these sizes (0 when one partition covers
+ * max_seq_len or partition_tokens == 0). */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_seq_len, int32_t partition_tokens);
+
+/* A partition size for pa_decode chosen from the batch shape and the current
+ * device's SM count (0 = single pass). Returns a negative status on error. */
+int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                                    int32_t block_size);
+
+/* Synchronise `stream`, copy the current device's error word to *err_out and
+ * clear it. */
+int pa_get_device_error(int32_t* err_out, void* stream);
+
+/* Human-readable name of a status code. */
+const char* pa_status_string(int status);
+
+/* PA_ABI_VERSION of the loaded library. */
+int pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_CACHE_114_GB300_PA_H */

@@ -1,0 +1,22 @@
+"""GB300-native paged KV-cache hot path.
+
+The compute lives in ``libpagedkv.so`` (hand-written CUDA for sm_103a behind a
+C ABI, declared in ``include/pa.h``); this package is its Python binding.
+
+* :func:`slot_mapping` - pool slot of each new token;
+* :func:`write_kv` - slot-mapped write of new K/V rows;
+* :func:`copy_blocks` - whole-block copies for copy-on-write;
+* :func:`decode` - decode attention through block tables (single pass or
+  split-K with a reduce), GQA heads packed per KV head.
+"""
+from ._lib import (DEVERR_BLOCK_ID, DEVERR_POSITION, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT,
+                   EXPORTED, LIB_PATH, PagedKVError, lib)
+from .ops import (check_copy_pairs, copy_blocks, decode, decode_workspace_bytes, default_partition,
+                  get_device_error, make_cache, slot_mapping, write_kv)
+
+__all__ = [
+    "DEVERR_BLOCK_ID", "DEVERR_POSITION", "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
+    "EXPORTED", "LIB_PATH", "PagedKVError", "lib", "check_copy_pairs", "copy_blocks", "decode",
+    "decode_workspace_bytes", "default_partition", "get_device_error", "make_cache",
+    "slot_mapping", "write_kv",
+]

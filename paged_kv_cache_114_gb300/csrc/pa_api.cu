@@ -1,0 +1,329 @@
+// pa_api.cu - the extern "C" entry points of libpagedkv (declared in
+// include/pa.h): argument checks, TMA tensor maps, launches on the caller's
+// stream, and the per-device error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+#include <unordered_set>
+
+#include "pa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One word per device; kernels OR PA_DEVERR_* bits into it.
+__device__ int g_device_error;
+
+struct DeviceInfo {
+  int* err = nullptr;
+  int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+
+// The device address of g_device_error and the SM count of the current device.
+// The address comes from cudaGetSymbolAddress once per device: in host code
+// the symbol itself only names a host-side shadow.
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_info[dev];
+  if (di.err == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return false;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    di.err = static_cast<int*>(p);
+    di.sms = sms;
+  }
+  *out = di;
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  });
+  return fn;
+}
+
+// Tensor map over one cache [num_blocks][b][H_kv][D] viewed as 4-D
+// (D, H_kv, b, num_blocks), box = 64 x 1 x tok_per_op x 1, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* base, const pa_cache& c, int tok_per_op) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t e = 2;  // bytes per element
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.head_dim), static_cast<cuuint64_t>(c.num_kv_heads),
+                        static_cast<cuuint64_t>(c.block_size), static_cast<cuuint64_t>(c.num_blocks)};
+  cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
+  cuuint32_t box[4] = {64u, 1u, static_cast<cuuint32_t>(tok_per_op), 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapDataType dt =
+      c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cache(const pa_cache* c) {
+  if (c == nullptr || c->k == nullptr || c->v == nullptr) return PA_ERR_NULL;
+  if (c->dtype != PA_F16 && c->dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (c->num_blocks <= 0 || c->num_blocks > 0x7fffffffLL || c->block_size <= 0 ||
+      c->num_kv_heads <= 0 || c->head_dim <= 0 || c->head_dim % 8 != 0)
+    return PA_ERR_SHAPE;
+  if (!aligned(c->k, 16) || !aligned(c->v, 16)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+int64_t decode_parts(int32_t max_seq_len, int32_t partition_tokens) {
+  if (partition_tokens <= 0 || max_seq_len <= partition_tokens) return 1;
+  return (static_cast<int64_t>(max_seq_len) + partition_tokens - 1) / partition_tokens;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "null pointer";
+    case PA_ERR_DTYPE: return "unsupported or mismatched dtype";
+    case PA_ERR_SHAPE: return "unsupported shape";
+    case PA_ERR_ALIGN: return "misaligned pointer";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_ARG: return "invalid argument";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_PAIRS: return "copy pairs violate the distinct-destination rule";
+    default: return "unknown status";
+  }
+}
+
+int pa_get_device_error(int32_t* err_out, void* stream) {
+  if (err_out == nullptr) return PA_ERR_NULL;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, di.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(di.err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  *err_out = v;
+  return PA_OK;
+}
+
+int pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                    const int32_t* seq_idx, const int32_t* positions, int64_t num_tokens,
+                    int32_t block_size, int64_t num_blocks, int64_t* slot_mapping, void* stream) {
+  if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 0) return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!block_tables || !seq_idx || !positions || !slot_mapping) return PA_ERR_NULL;
+  if (block_size <= 0 || num_blocks <= 0 || num_blocks > 0x7fffffffLL) return PA_ERR_SHAPE;
+  if (num_tokens > 0x7fffffffLL * 256) return PA_ERR_SHAPE;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  cudaError_t e = pa::launch_slot_mapping(block_tables, num_seqs, max_blocks_per_seq, seq_idx,
+                                          positions, num_tokens, block_size, num_blocks,
+                                          slot_mapping, di.err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_write_kv(const void* key, const void* value, const int64_t* slot_mapping,
+                int64_t num_tokens, const pa_cache* cache, void* stream) {
+  if (num_tokens < 0) return PA_ERR_ARG;
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping) return PA_ERR_NULL;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8)) return PA_ERR_ALIGN;
+  if (num_tokens > 0x7fffffffLL) return PA_ERR_SHAPE;
+  const int64_t row_bytes = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim * 2;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  cudaError_t e = pa::launch_write_kv(key, value, slot_mapping, num_tokens, cache->k, cache->v,
+                                      cache->num_blocks, cache->block_size, row_bytes, di.err,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t num_blocks) {
+  if (num_pairs < 0) return PA_ERR_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (host_pairs == nullptr) return PA_ERR_NULL;
+  std::unordered_set<int64_t> dsts;
+  std::unordered_set<int64_t> srcs;
+  for (int64_t i = 0; i < num_pairs; ++i) {
+    const int64_t s = host_pairs[2 * i];
+    const int64_t d = host_pairs[2 * i + 1];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) return PA_ERR_PAIRS;
+    if (!dsts.insert(d).second) return PA_ERR_PAIRS;
+    srcs.insert(s);
+  }
+  for (int64_t d : dsts)
+    if (srcs.count(d)) return PA_ERR_PAIRS;
+  return PA_OK;
+}
+
+int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* src_dst_pairs,
+                   int64_t num_pairs, void* stream) {
+  if (num_layers <= 0 || num_pairs < 0) return PA_ERR_ARG;
+  if (caches == nullptr) return PA_ERR_NULL;
+  for (int32_t l = 0; l < num_layers; ++l) {
+    int rc = check_cache(&caches[l]);
+    if (rc != PA_OK) return rc;
+    const pa_cache& c0 = caches[0];
+    const pa_cache& c = caches[l];
+    if (c.dtype != c0.dtype) return PA_ERR_DTYPE;
+    if (c.num_blocks != c0.num_blocks || c.block_size != c0.block_size ||
+        c.num_kv_heads != c0.num_kv_heads || c.head_dim != c0.head_dim)
+      return PA_ERR_SHAPE;
+  }
+  if (num_pairs == 0) return PA_OK;
+  if (src_dst_pairs == nullptr) return PA_ERR_NULL;
+  if (!aligned(src_dst_pairs, 8)) return PA_ERR_ALIGN;
+  const int64_t block_bytes = static_cast<int64_t>(caches[0].block_size) * caches[0].num_kv_heads *
+                              caches[0].head_dim * 2;
+  if (num_pairs * ((block_bytes + 16383) / 16384) > 0x7fffffffLL) return PA_ERR_SHAPE;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  for (int32_t l0 = 0; l0 < num_layers; l0 += pa::kMaxCopyLayers) {
+    const int32_t n = (num_layers - l0) < pa::kMaxCopyLayers ? (num_layers - l0) : pa::kMaxCopyLayers;
+    pa::CopyLayers layers{};
+    for (int32_t i = 0; i < n; ++i) {
+      layers.k[i] = caches[l0 + i].k;
+      layers.v[i] = caches[l0 + i].v;
+    }
+    cudaError_t e = pa::launch_copy_blocks(layers, n, src_dst_pairs, num_pairs, caches[0].num_blocks,
+                                           block_bytes, di.err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_seq_len, int32_t partition_tokens) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  const int64_t parts = decode_parts(max_seq_len, partition_tokens);
+  if (parts <= 1) return 0;
+  return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
+int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                                    int32_t block_size) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || max_seq_len < 0 || block_size <= 0) return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  // Two CTAs fit per SM. Split when whole sequences would leave SMs idle or
+  // when lengths are long enough that partitions even out ragged batches.
+  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  if (max_seq_len <= 512) return 0;
+  (void)units;
+  (void)block_size;
+  return 512;
+}
+
+int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cache* cache,
+              const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+              int32_t max_seq_len, float scale, void* out, pa_dtype out_dtype,
+              int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || num_q_heads <= 0) return PA_ERR_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !block_tables || !seq_lens || !out) return PA_ERR_NULL;
+  if (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_DTYPE;
+  const int D = cache->head_dim;
+  const int b = cache->block_size;
+  const int hkv = cache->num_kv_heads;
+  if (D != 64 && D != 128 && D != 256) return PA_ERR_SHAPE;
+  if (!(b % pa::kStageRows == 0 || pa::kStageRows % b == 0)) return PA_ERR_SHAPE;
+  if (num_q_heads % hkv != 0) return PA_ERR_SHAPE;
+  const int g = num_q_heads / hkv;
+  if (g > 16) return PA_ERR_SHAPE;
+  if (max_blocks_per_seq <= 0 || max_seq_len < 0) return PA_ERR_ARG;
+  if (partition_tokens < 0 || partition_tokens % pa::kStageRows != 0) return PA_ERR_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_ARG;
+  if (!aligned(q, 4) || !aligned(out, 4) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return PA_ERR_ALIGN;
+  const int64_t parts = decode_parts(max_seq_len, partition_tokens);
+  if (parts > 65535 || num_seqs > 65535 || hkv > 65535) return PA_ERR_SHAPE;
+
+  pa::DecodeArgs a{};
+  a.q = q;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.num_blocks = cache->num_blocks;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = hkv;
+  a.group = g;
+  a.block_size = b;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.part_tokens = parts > 1 ? partition_tokens : 0;
+  a.max_parts = static_cast<int32_t>(parts);
+  a.tok_per_op = b < pa::kStageRows ? b : pa::kStageRows;
+  a.slot_rows = a.tok_per_op < 8 ? 8 : a.tok_per_op;
+  a.ops_per_stage = pa::kStageRows / a.slot_rows;
+  a.out_dtype = out_dtype;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (parts > 1) {
+    const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, D, max_seq_len,
+                                                  partition_tokens);
+    if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = a.part_o + static_cast<int64_t>(num_seqs) * num_q_heads * parts * D;
+  }
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  a.err = di.err;
+
+  CUtensorMap tk, tv;
+  if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
+      !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
+    return PA_ERR_CUDA;
+
+  const dim3 grid(static_cast<unsigned>(hkv), static_cast<unsigned>(parts),
+                  static_cast<unsigned>(num_seqs));
+  const int tiles = (g + 7) / 8;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cache->dtype == PA_F16) {
+    e = D == 64 ? pa::launch_decode_f16_64(tk, tv, a, tiles, grid, st)
+        : D == 128 ? pa::launch_decode_f16_128(tk, tv, a, tiles, grid, st)
+                   : pa::launch_decode_f16_256(tk, tv, a, tiles, grid, st);
+  } else {
+    e = D == 64 ? pa::launch_decode_bf16_64(tk, tv, a, tiles, grid, st)
+        : D == 128 ? pa::launch_decode_bf16_128(tk, tv, a, tiles, grid, st)
+                   : pa::launch_decode_bf16_256(tk, tv, a, tiles, grid, st);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (parts > 1) {
+    e = pa::launch_decode_reduce(a, D, st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,28 @@
+// pa_decode_inst.cu - one decode instantiation per (dtype, head_dim).
+// Compiled once per combination with -DPA_INST_BF16={0,1} -DPA_INST_D={64,128,256}
+// so the variants build in parallel.
+#include "pa_decode.cuh"
+
+#ifndef PA_INST_BF16
+#error "PA_INST_BF16 must be defined"
+#endif
+#ifndef PA_INST_D
+#error "PA_INST_D must be defined"
+#endif
+
+#define PA_CAT3(a, b, c) a##b##c
+#define PA_NAME(dt, d) PA_CAT3(launch_decode_, dt, d)
+#if PA_INST_BF16
+#define PA_FN PA_NAME(bf16_, PA_INST_D)
+#else
+#define PA_FN PA_NAME(f16_, PA_INST_D)
+#endif
+
+namespace pa {
+
+cudaError_t PA_FN(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int group_tiles,
+                  dim3 grid, cudaStream_t st) {
+  return launch_decode_dispatch<PA_INST_BF16 != 0, PA_INST_D>(tk, tv, a, group_tiles, grid, st);
+}
+
+}  // namespace pa

@@ -1,0 +1,76 @@
+// pa_internal.h - host-side launchers shared between the translation units of
+// libpagedkv. Not part of the public ABI (include/pa.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Kernel arguments of the decode kernels (plain data, passed by value).
+struct DecodeArgs {
+  const void* q;                 // [N][Hq][D]
+  void* out;                     // [N][Hq][D] of out_dtype
+  float* part_o;                 // [N][Hq][max_parts][D]   (split-K only)
+  float* part_ml;                // [N][Hq][max_parts][2]   (max in log2 units, normaliser)
+  const int32_t* block_tables;   // [N][max_blocks]
+  const int32_t* seq_lens;       // [N]
+  int* err;                      // device error word
+  int64_t num_blocks;
+  int32_t num_seqs, num_q_heads, num_kv_heads, group;
+  int32_t block_size, max_blocks, max_seq_len;
+  int32_t part_tokens;           // 0 = single pass
+  int32_t max_parts;             // partitions per sequence held in the workspace
+  int32_t tok_per_op;            // tokens one TMA box covers: min(block_size, 16)
+  int32_t slot_rows;             // shared-memory rows reserved per box: max(tok_per_op, 8)
+  int32_t ops_per_stage;         // boxes per 16-row stage
+  int32_t out_dtype;             // pa_dtype
+  float scale_log2;              // scale * log2(e)
+};
+
+// Rows of shared memory one pipeline stage holds (one m16 tile of tokens).
+constexpr int kStageRows = 16;
+// Warps per decode CTA; each owns a private ring of stages.
+constexpr int kDecodeWarps = 4;
+
+// Decode launchers, one per (dtype, head_dim) translation unit.
+// group_tiles = ceil(group / 8) in {1, 2}.
+cudaError_t launch_decode_f16_64(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                 int group_tiles, dim3 grid, cudaStream_t st);
+cudaError_t launch_decode_f16_128(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  int group_tiles, dim3 grid, cudaStream_t st);
+cudaError_t launch_decode_f16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  int group_tiles, dim3 grid, cudaStream_t st);
+cudaError_t launch_decode_bf16_64(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  int group_tiles, dim3 grid, cudaStream_t st);
+cudaError_t launch_decode_bf16_128(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                   int group_tiles, dim3 grid, cudaStream_t st);
+cudaError_t launch_decode_bf16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                   int group_tiles, dim3 grid, cudaStream_t st);
+
+// Merges split-K partials into out (pa_decode_reduce.cu).
+cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);
+
+// Cache operations (pa_cache_ops.cu).
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
+                                const int32_t* seq_idx, const int32_t* positions, int64_t num_tokens,
+                                int32_t block_size, int64_t num_blocks, int64_t* slots, int* err,
+                                cudaStream_t st);
+cudaError_t launch_write_kv(const void* key, const void* value, const int64_t* slots,
+                            int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                            int32_t block_size, int64_t row_bytes, int* err, cudaStream_t st);
+
+constexpr int kMaxCopyLayers = 64;
+struct CopyLayers {
+  void* k[kMaxCopyLayers];
+  void* v[kMaxCopyLayers];
+};
+cudaError_t launch_copy_blocks(const CopyLayers& layers, int32_t num_layers,
+                               const int64_t* pairs, int64_t num_pairs, int64_t num_blocks,
+                               int64_t block_bytes, int* err, cudaStream_t st);
+
+}  // namespace pa

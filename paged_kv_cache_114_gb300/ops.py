@@ -1,0 +1,164 @@
+"""Torch-facing binding of the C ABI: argument marshalling only.
+
+Each function checks that its tensors are on one CUDA device with the expected
+dtype and layout, turns them into pointers, and calls the matching ``pa_*``
+entry point on the current stream. All arithmetic runs in the library's CUDA
+kernels; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float16: _lib.PA_F16, torch.bfloat16: _lib.PA_BF16, torch.float32: _lib.PA_F32}
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda(*ts: torch.Tensor) -> torch.device:
+    dev = ts[0].device
+    for t in ts:
+        _need(t.is_cuda, "tensors must live on a CUDA device")
+        _need(t.device == dev, "tensors must live on one device")
+        _need(t.is_contiguous(), "tensors must be contiguous")
+    return dev
+
+
+def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> _lib.PaCache:
+    """pa_cache for one layer's pool, k/v shaped [num_blocks, block_size, H_kv, D]."""
+    _cuda(k_cache, v_cache)
+    _need(k_cache.dim() == 4 and k_cache.shape == v_cache.shape, "k/v caches: [NB, b, H_kv, D], same shape")
+    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in (torch.float16, torch.bfloat16),
+          "caches must both be float16 or both bfloat16")
+    nb, b, hkv, d = k_cache.shape
+    return _lib.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, b, hkv, d, _DTYPES[k_cache.dtype])
+
+
+def slot_mapping(block_tables: torch.Tensor, seq_idx: torch.Tensor, positions: torch.Tensor,
+                 block_size: int, num_blocks: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """int64 pool slot of each (sequence, position) token."""
+    dev = _cuda(block_tables, seq_idx, positions)
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2, "block_tables: int32 [N, maxB]")
+    _need(seq_idx.dtype == torch.int32 and positions.dtype == torch.int32, "seq_idx/positions: int32")
+    _need(seq_idx.shape == positions.shape and seq_idx.dim() == 1, "seq_idx/positions: [T]")
+    if out is None:
+        out = torch.empty(positions.shape[0], dtype=torch.int64, device=dev)
+    _need(out.dtype == torch.int64 and out.shape == positions.shape, "out: int64 [T]")
+    _cuda(out, block_tables)
+    st = _lib.lib().pa_slot_mapping(_ptr(block_tables), block_tables.shape[0], block_tables.shape[1],
+                                    _ptr(seq_idx), _ptr(positions), positions.shape[0], block_size,
+                                    num_blocks, _ptr(out), _stream(dev))
+    _lib.check("pa_slot_mapping", st)
+    return out
+
+
+def write_kv(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """k_cache/v_cache row at each slot <- the token's key/value rows (in place)."""
+    dev = _cuda(key, value, slot_mapping, k_cache, v_cache)
+    _need(key.shape == value.shape and key.dim() == 3, "key/value: [T, H_kv, D]")
+    _need(key.shape[1:] == k_cache.shape[2:], "key/value rows must match the cache's [H_kv, D]")
+    _need(key.dtype == k_cache.dtype == value.dtype, "key/value dtype must match the cache")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == key.shape[:1], "slot_mapping: int64 [T]")
+    cache = make_cache(k_cache, v_cache)
+    st = _lib.lib().pa_write_kv(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
+                                ctypes.byref(cache), _stream(dev))
+    _lib.check("pa_write_kv", st)
+
+
+def check_copy_pairs(pairs_host: torch.Tensor, num_blocks: int) -> None:
+    """Host-side check of copy pairs (ids in range, distinct destinations, none a source)."""
+    _need(pairs_host.device.type == "cpu" and pairs_host.dtype == torch.int64, "pairs: host int64 [P, 2]")
+    p = pairs_host.contiguous()
+    st = _lib.lib().pa_check_copy_pairs(_ptr(p), p.shape[0], num_blocks)
+    _lib.check("pa_check_copy_pairs", st)
+
+
+def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor],
+                pairs: torch.Tensor) -> None:
+    """For every (src, dst) pair and every layer, block dst <- block src (in place)."""
+    _need(len(k_caches) == len(v_caches) and len(k_caches) > 0, "one k and one v cache per layer")
+    dev = _cuda(pairs, *k_caches, *v_caches)
+    _need(pairs.dtype == torch.int64 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs: int64 [P, 2]")
+    arr = (_lib.PaCache * len(k_caches))(*[make_cache(k, v) for k, v in zip(k_caches, v_caches)])
+    st = _lib.lib().pa_copy_blocks(arr, len(k_caches), _ptr(pairs), pairs.shape[0], _stream(dev))
+    _lib.check("pa_copy_blocks", st)
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int,
+                           partition_tokens: int) -> int:
+    return int(_lib.lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len,
+                                                    partition_tokens))
+
+
+def default_partition(num_seqs: int, num_kv_heads: int, max_seq_len: int, block_size: int) -> int:
+    v = int(_lib.lib().pa_decode_default_partition(num_seqs, num_kv_heads, max_seq_len, block_size))
+    _lib.check("pa_decode_default_partition", min(v, 0))
+    return v
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           seq_lens: torch.Tensor, scale: float, *, max_seq_len: int,
+           out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+           partition_tokens: Optional[int] = None,
+           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Paged decode attention: out[s, h] over the first seq_lens[s] tokens of sequence s.
+
+    ``max_seq_len`` bounds ``seq_lens`` (it sizes the launch, so the call never
+    reads the lengths back). ``partition_tokens`` = 0 runs one pass per
+    (sequence, KV head); a multiple of 16 runs split-K with a reduce;
+    None picks the library's default for this shape. The workspace, when a
+    split needs one, comes from the caller or from torch's allocator.
+    """
+    dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [N, Hq, D] with the cache's D")
+    _need(q.dtype == k_cache.dtype, "q dtype must match the cache")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+          and block_tables.shape[0] == q.shape[0], "block_tables: int32 [N, maxB]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.shape == (q.shape[0],), "seq_lens: int32 [N]")
+    n, hq, d = q.shape
+    if out is None:
+        out = torch.empty((n, hq, d), dtype=out_dtype or q.dtype, device=dev)
+    _cuda(out, q)
+    _need(out.shape == q.shape and out.dtype in _DTYPES, "out: [N, Hq, D] of float16/bfloat16/float32")
+    nb, b, hkv, _ = k_cache.shape
+    if partition_tokens is None:
+        partition_tokens = default_partition(n, hkv, max_seq_len, b)
+    ws_bytes = decode_workspace_bytes(n, hq, d, max_seq_len, partition_tokens)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _cuda(workspace, q)
+    cache = make_cache(k_cache, v_cache)
+    st = _lib.lib().pa_decode(_ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables),
+                              block_tables.shape[1], _ptr(seq_lens), int(max_seq_len), float(scale),
+                              _ptr(out), _DTYPES[out.dtype], int(partition_tokens), _ptr(workspace),
+                              0 if workspace is None else workspace.numel() * workspace.element_size(),
+                              _stream(dev))
+    _lib.check("pa_decode", st)
+    return out
+
+
+def get_device_error(device: Optional[torch.device] = None) -> int:
+    """Synchronise the current stream, read and clear the device error word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    v = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        st = _lib.lib().pa_get_device_error(ctypes.byref(v), _stream(dev))
+    _lib.check("pa_get_device_error", st)
+    return int(v.value)

@@ -1,0 +1,119 @@
+"""The C ABI library on a host without a GPU: it builds, loads, exports every
+symbol include/pa.h declares, and its host-only entry points behave.
+
+No call here touches a device.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_114_gb300 import build
+    build.build()
+    import paged_kv_cache_114_gb300 as pa
+    return pa.lib()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    import paged_kv_cache_114_gb300 as pa
+    assert _header_functions() == sorted(pa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+    nm = os.popen(f"nm -D --defined-only {lib._name}").read()
+    for name in _header_functions():
+        assert re.search(rf"\bT {name}\b", nm), f"{name} not exported as a text symbol"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pa_abi_version() == 1
+    assert lib.pa_status_string(0) == b"ok"
+    assert lib.pa_status_string(-5).startswith(b"workspace")
+    assert lib.pa_status_string(12345) == b"unknown status"
+
+
+def test_workspace_bytes(lib):
+    # N * Hq * ceil(L / P) * (D + 2) floats; no workspace when one partition covers L
+    assert lib.pa_decode_workspace_bytes(8, 32, 128, 32768, 512) == 8 * 32 * 64 * 130 * 4
+    assert lib.pa_decode_workspace_bytes(8, 32, 128, 512, 512) == 0
+    assert lib.pa_decode_workspace_bytes(8, 32, 128, 4096, 0) == 0
+    assert lib.pa_decode_workspace_bytes(4, 4, 64, 33, 16) == 4 * 4 * 3 * 66 * 4
+
+
+def test_check_copy_pairs(lib):
+    def chk(pairs, nb=16):
+        a = np.ascontiguousarray(np.array(pairs, dtype=np.int64).reshape(-1, 2))
+        return lib.pa_check_copy_pairs(a.ctypes.data_as(ctypes.c_void_p), a.shape[0], nb)
+    assert chk([(1, 2), (1, 3), (4, 5)]) == 0
+    assert chk([(1, 2), (3, 2)]) == -8          # duplicate destination
+    assert chk([(1, 2), (2, 3)]) == -8          # a destination is also a source
+    assert chk([(1, 16)]) == -8                 # out of range
+    assert chk([(-1, 3)]) == -8
+    assert lib.pa_check_copy_pairs(None, 0, 16) == 0
+    assert lib.pa_check_copy_pairs(None, 2, 16) == -1
+
+
+def test_host_argument_errors_launch_nothing(lib):
+    import paged_kv_cache_114_gb300._lib as L
+    vp = ctypes.c_void_p
+    # a NULL cache is rejected before any CUDA call
+    assert lib.pa_decode(vp(0), 1, 1, None, vp(0), 1, vp(0), 1, 1.0, vp(0), 0, 0, vp(0), 0, vp(0)) == -1
+    assert lib.pa_write_kv(vp(0), vp(0), vp(0), 1, None, vp(0)) == -1
+    assert lib.pa_copy_blocks(None, 1, vp(0), 1, vp(0)) == -1
+    assert lib.pa_copy_blocks(None, 0, vp(0), 1, vp(0)) == -6
+    assert lib.pa_slot_mapping(vp(0), 1, 1, vp(0), vp(0), -1, 4, 8, vp(0), vp(0)) == -6
+    assert lib.pa_slot_mapping(vp(0), 1, 1, vp(0), vp(0), 0, 4, 8, vp(0), vp(0)) == 0
+    # cache checks: dtype, shape and alignment, all on the host
+    good = L.PaCache(4096, 8192, 64, 16, 8, 128, L.PA_F16)
+    bad_dtype = L.PaCache(4096, 8192, 64, 16, 8, 128, L.PA_F32)
+    bad_dim = L.PaCache(4096, 8192, 64, 16, 8, 100, L.PA_F16)
+    misaligned = L.PaCache(4100, 8192, 64, 16, 8, 128, L.PA_F16)
+    args = (vp(4096), 1, 8)
+    assert lib.pa_decode(*args[:1], 1, 8, ctypes.byref(bad_dtype), vp(4096), 1, vp(4096), 1, 1.0,
+                         vp(4096), 0, 0, vp(0), 0, vp(0)) == -2
+    assert lib.pa_decode(vp(4096), 1, 8, ctypes.byref(bad_dim), vp(4096), 1, vp(4096), 1, 1.0,
+                         vp(4096), 0, 0, vp(0), 0, vp(0)) == -3
+    assert lib.pa_decode(vp(4096), 1, 8, ctypes.byref(misaligned), vp(4096), 1, vp(4096), 1, 1.0,
+                         vp(4096), 0, 0, vp(0), 0, vp(0)) == -4
+    # head grouping: 12 query heads over 8 KV heads is not a whole group
+    assert lib.pa_decode(vp(4096), 1, 12, ctypes.byref(good), vp(4096), 1, vp(4096), 1, 1.0,
+                         vp(4096), 0, 0, vp(0), 0, vp(0)) == -3
+    # more than 16 query heads per KV head
+    assert lib.pa_decode(vp(4096), 1, 8 * 17, ctypes.byref(good), vp(4096), 1, vp(4096), 1, 1.0,
+                         vp(4096), 0, 0, vp(0), 0, vp(0)) == -3
+    # partition size must be a multiple of 16
+    assert lib.pa_decode(vp(4096), 1, 8, ctypes.byref(good), vp(4096), 1, vp(4096), 100, 1.0,
+                         vp(4096), 0, 24, vp(0), 0, vp(0)) == -6
+    # split-K without a workspace
+    assert lib.pa_decode(vp(4096), 1, 8, ctypes.byref(good), vp(4096), 64, vp(4096), 1000, 1.0,
+                         vp(4096), 0, 512, vp(0), 0, vp(0)) == -5
+    # bad block size (neither a divisor nor a multiple of 16)
+    b24 = L.PaCache(4096, 8192, 64, 24, 8, 128, L.PA_F16)
+    assert lib.pa_decode(vp(4096), 1, 8, ctypes.byref(b24), vp(4096), 1, vp(4096), 1, 1.0,
+                         vp(4096), 0, 0, vp(0), 0, vp(0)) == -3
+    # zero sequences is a no-op
+    assert lib.pa_decode(vp(0), 0, 8, ctypes.byref(good), vp(0), 1, vp(0), 1, 1.0,
+                         vp(0), 0, 0, vp(0), 0, vp(0)) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import paged_kv_cache_114_gb300._lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        L.lib()
