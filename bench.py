@@ -414,17 +414,43 @@ def run_e2e(run, K, W, world, dev, step_bytes):
 # ----------------------------------------------------------------------------- CPU oracle
 
 
-def oracle_sample_step(w, seqs, state):
-    """One oracle step on a sample of sequences: slot mapping and write of their
-    newest tokens, then decode of all their heads."""
-    import oracle
-    idx = step_tokens(w)
-    mine = [i for i in idx if int(w.seq_idx[i]) in set(seqs)]
-    slots = oracle.slot_mapping(w.block_tables, w.seq_idx[mine], w.positions[mine], w.block_size)
-    k, v = oracle.write_kv(state["k"], state["v"], w.key[mine], w.value[mine], slots)
-    heads = [(s, h) for s in seqs for h in range(w.num_q_heads)]
-    oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, pairs=heads)
-    return len(mine)
+class OracleSample:
+    """Per-sequence inputs for bounded oracle steps.
+
+    A step covers one sequence: the slot mapping and write of its newest token
+    and decode of all its query heads. The oracle's write returns a new copy of
+    the pool it is given, so each sequence gets a sub-pool holding just its own
+    blocks (table remapped to 0..n-1); building it is input preparation and is
+    not timed. The oracle functions run unchanged.
+    """
+
+    def __init__(self, w):
+        self.w = w
+        self.state = prepared_oracle_state(w)
+        self.newest = {int(w.seq_idx[i]): int(i) for i in step_tokens(w)}
+        self.cache = {}
+
+    def inputs(self, s):
+        if s not in self.cache:
+            w = self.w
+            nblk = -(-int(w.seq_lens[s]) // w.block_size)
+            blocks = w.block_tables[s, :nblk]
+            self.cache = {s: (self.state["k"][blocks], self.state["v"][blocks],
+                              np.arange(max(nblk, 1), dtype=np.int32)[None])}
+        return self.cache[s]
+
+    def step(self, s):
+        import oracle
+        w = self.w
+        k, v, table = self.inputs(s)
+        i = self.newest.get(s)
+        n_tok = 0
+        if i is not None:
+            slots = oracle.slot_mapping(table, [0], [int(w.positions[i])], w.block_size)
+            k, v = oracle.write_kv(k, v, w.key[i:i + 1], w.value[i:i + 1], slots)
+            n_tok = 1
+        oracle.decode(w.q[s:s + 1], k, v, table, w.seq_lens[s:s + 1], w.scale, w.dtype)
+        return n_tok
 
 
 def sample_bytes(w, seqs, n_tok):
@@ -465,41 +491,44 @@ def cpu_baseline_child(config, block_size, mode, steps=0, warmup=0):
 
 
 def cpu_child(args):
-    """Oracle timing: 'cpu_baseline' = one bounded sample (~10-30 s); 'reference'
-    = the reference arm's K + W steps, each a bounded sample."""
+    """Oracle timing: 'cpu_baseline' = one bounded sample (about 12 s of CPU);
+    'reference' = the reference arm's W + K steps, each one random sequence."""
     from workloads import make_config
     w = make_config(args.config, block_size=args.block_size) if args.config == 4 else make_config(args.config)
-    state = prepared_oracle_state(w)
-    order = np.argsort(w.seq_lens)[::-1] if w.num_seqs > 1 else np.arange(1)
+    sampler = OracleSample(w)
     rng = np.random.default_rng(0)
     if args.cpu_child == "cpu_baseline":
         budget, done_b, t_used, seqs_done = 12.0, 0, 0.0, 0
-        perm = rng.permutation(w.num_seqs)
-        for s in perm:
+        for s in rng.permutation(w.num_seqs):
+            sampler.inputs(int(s))
             t0 = time.perf_counter()
-            n_tok = oracle_sample_step(w, [int(s)], state)
+            n_tok = sampler.step(int(s))
             t_used += time.perf_counter() - t0
             done_b += sample_bytes(w, [int(s)], n_tok)
             seqs_done += 1
             if t_used >= budget:
                 break
         res = {"value": round(done_b / t_used / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{seqs_done} of {w.num_seqs} sequences (random order), all heads, "
-                         f"their new-token writes; {t_used:.1f} s of single-thread CPU time"}
+               "sample": f"{seqs_done} of {w.num_seqs} sequences in random order, each: its new "
+                         f"token's slot mapping and write, decode of all {w.num_q_heads} heads; "
+                         f"{t_used:.1f} s of single-thread CPU time"}
         print(json.dumps(res))
         return
-    # reference arm: W + K steps, each one random sequence
     total_b, total_t = 0, 0.0
     for i in range(args.warmup + args.steps):
         s = int(rng.integers(0, w.num_seqs))
+        sampler.inputs(s)
         t0 = time.perf_counter()
-        n_tok = oracle_sample_step(w, [s], state)
+        n_tok = sampler.step(s)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             total_b += sample_bytes(w, [s], n_tok)
             total_t += dt
-    print(json.dumps({"value": round(total_b / total_t / 1e9, 4), "ms_per_step": total_t / max(args.steps, 1) * 1e3,
-                      "sample": f"each step: one random sequence of {w.num_seqs}, all heads"}))
+    print(json.dumps({"value": round(total_b / total_t / 1e9, 4),
+                      "ms_per_step": round(total_t / max(args.steps, 1) * 1e3, 4),
+                      "sample": f"each step: one random sequence of {w.num_seqs} (its new token's "
+                                f"slot mapping and write, decode of all {w.num_q_heads} heads), "
+                                f"single thread"}))
 
 
 def run_reference(args):

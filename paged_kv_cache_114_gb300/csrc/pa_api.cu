@@ -232,13 +232,20 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
   if (num_seqs < 0 || num_kv_heads <= 0 || max_seq_len < 0 || block_size <= 0) return PA_ERR_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
-  // Two CTAs fit per SM. Split when whole sequences would leave SMs idle or
-  // when lengths are long enough that partitions even out ragged batches.
+  // Two decode CTAs are resident per SM. With at least 8 (sequence, KV head)
+  // units per SM the hardware scheduler balances whole sequences well; below
+  // that, cut sequences so the grid holds about 16 CTAs per SM. Partitions
+  // stay within [512, 2048] tokens: shorter ones pay the per-CTA prologue and
+  // the reduce too often, longer ones unbalance ragged batches.
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
-  if (max_seq_len <= 512) return 0;
-  (void)units;
+  if (units == 0 || max_seq_len <= 512 || units >= 8LL * di.sms) return 0;
+  const int64_t parts = (16LL * di.sms + units - 1) / units;
+  int64_t pt = (max_seq_len + parts - 1) / parts;
+  pt = ((pt + 255) / 256) * 256;
+  if (pt < 512) pt = 512;
+  if (pt > 2048) pt = 2048;
   (void)block_size;
-  return 512;
+  return pt >= max_seq_len ? 0 : static_cast<int32_t>(pt);
 }
 
 int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cache* cache,
