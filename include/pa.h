@@ -170,6 +170,35 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
 int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                                     int32_t block_size);
 
+/*
+ * pa_decode_static_workspace - pa_decode for callers that cannot allocate
+ * device memory. The pages have no counterpart; this call is a library
+ * convenience. Some callers cannot cudaMalloc a workspace: code inside a host
+ * application whose own pool owns all device memory, latency-critical paths
+ * where cudaMalloc/cudaFree may synchronise the device, and bindings from
+ * runtimes without a device allocator. This call takes the same arguments as
+ * pa_decode minus the workspace, and keeps the split-K partials in a
+ * fixed array of PA_STATIC_WORKSPACE_BYTES compiled into the library (held by
+ * every GPU that loads it until the process exits). The caller still passes q,
+ * the cache, the tables, the lengths and out.
+ *   - Sizes whose workspace (pa_decode_workspace_bytes) exceeds
+ *     PA_STATIC_WORKSPACE_BYTES return PA_ERR_WORKSPACE and launch nothing.
+ *   - The call allocates nothing. The first call on a device looks up the
+ *     array's device address (once per device, with that device current); make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     partials; nothing in it needs to start at zero, because each call writes
+ *     every partial it reads. Calls that overlap on the GPU (other streams,
+ *     other threads) race on the array: serialise them.
+ * Other arguments, errors and results are those of pa_decode.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+int pa_decode_static_workspace(const void* q, int32_t num_seqs, int32_t num_q_heads,
+                               const pa_cache* cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t max_seq_len, float scale, void* out, pa_dtype out_dtype,
+                               int32_t partition_tokens, void* stream);
+
 /* Synchronise `stream`, copy the current device's error word to *err_out and
  * clear it. */
 int pa_get_device_error(int32_t* err_out, void* stream);

@@ -24,8 +24,9 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_POSITION, DEVERR_TIMEOUT = 
 EXPORTED = (
     "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_check_copy_pairs", "pa_decode",
     "pa_decode_workspace_bytes", "pa_decode_default_partition", "pa_get_device_error",
-    "pa_status_string", "pa_abi_version",
+    "pa_status_string", "pa_abi_version", "pa_decode_static_workspace",
 )
+STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
 class PaCache(ctypes.Structure):
@@ -62,6 +63,8 @@ def _declare(lib):
         "pa_check_copy_pairs": (ctypes.c_int, [vp, i64, i64]),
         "pa_decode": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32, ctypes.c_float, vp,
                                      ctypes.c_int, i32, vp, sz, vp]),
+        "pa_decode_static_workspace": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32,
+                                                      ctypes.c_float, vp, ctypes.c_int, i32, vp]),
         "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
         "pa_decode_default_partition": (i32, [i32, i32, i32, i32]),
         "pa_get_device_error": (ctypes.c_int, [ctypes.POINTER(i32), vp]),

@@ -154,6 +154,39 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     return out
 
 
+def decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
+                            max_seq_len: int, partition_tokens: int,
+                            out: Optional[torch.Tensor] = None,
+                            out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
+    """Decode like :func:`decode`, with the split-K partials kept in the library's
+    fixed device array instead of a workspace from the caller.
+
+    For callers that cannot allocate device memory. The array holds
+    ``STATIC_WORKSPACE_BYTES``; larger workspaces raise. All calls share it, so
+    calls that overlap on the GPU race. Only ``out`` (when not given) is
+    allocated here, by torch, for convenience.
+    """
+    dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [N, Hq, D] with the cache's D")
+    _need(q.dtype == k_cache.dtype, "q dtype must match the cache")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+          and block_tables.shape[0] == q.shape[0], "block_tables: int32 [N, maxB]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.shape == (q.shape[0],), "seq_lens: int32 [N]")
+    n, hq, d = q.shape
+    if out is None:
+        out = torch.empty((n, hq, d), dtype=out_dtype or q.dtype, device=dev)
+    _cuda(out, q)
+    _need(out.shape == q.shape and out.dtype in _DTYPES, "out: [N, Hq, D] of float16/bfloat16/float32")
+    cache = make_cache(k_cache, v_cache)
+    st = _lib.lib().pa_decode_static_workspace(
+        _ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), int(max_seq_len), float(scale), _ptr(out), _DTYPES[out.dtype],
+        int(partition_tokens), _stream(dev))
+    _lib.check("pa_decode_static_workspace", st)
+    return out
+
+
 def get_device_error(device: Optional[torch.device] = None) -> int:
     """Synchronise the current stream, read and clear the device error word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
