@@ -207,9 +207,10 @@ class Run:
         self.slots = torch.empty(self.n_tokens, dtype=torch.int64, device=dev)
         self.out = torch.empty(self.q.shape, dtype=torch.float32, device=dev)
         self.partition = partition
-        ws = pa.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim, w.max_seq_len, partition)
-        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-        self.launches_per_step = 3 + (1 if ws else 0)
+        self.ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                   w.max_seq_len, partition, dev)
+        # slot mapping + KV write + decode (+ the reduce of fixed split-K partitions)
+        self.launches_per_step = 3 + (1 if (self.ws is not None and partition > 0) else 0)
 
     def decode(self, q=None, lens=None, tables=None, out=None):
         return self.pa.decode(self.q if q is None else q, self.k, self.v,
@@ -330,7 +331,9 @@ def run_gpu(args):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy rate)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "frac_of_8tbs_spec": round(achieved / SPEC_HBM_GBS, 4),
-                "kernel": "pa_decode: partition kernel + reduce" if run.ws.numel() > 16 else "pa_decode",
+                "kernel": {0: "decode_kernel (single pass)",
+                           -1: "decode_balanced_kernel (equal stage ranges per warp)"}.get(
+                               partition, "decode_kernel + decode_reduce_kernel (split-K)"),
                 "algorithmic_bytes_per_call": dec_bytes, "mean_call_us": round(dec_ms * 1e3, 2)}
 
     line = {

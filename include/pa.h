@@ -144,13 +144,19 @@ int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t nu
  *   max_seq_len    host upper bound of seq_lens (sizes the launch)
  *   scale          softmax scale, usually 1/sqrt(head_dim)
  *   out            device [num_seqs][num_q_heads][head_dim] of out_dtype
- *   partition_tokens  0: one pass per (sequence, KV head); otherwise a multiple
- *                  of 16: split-K, each sequence cut into partitions of that
- *                  many tokens whose (max, normaliser, unnormalised output)
- *                  partials a second kernel merges with the rescale identity
- *   workspace      device, >= pa_decode_workspace_bytes(...) bytes, 16-byte
- *                  aligned; unused (may be NULL) when no sequence needs more
- *                  than one partition
+ *   partition_tokens  0: one pass per (sequence, KV head); a multiple of 16:
+ *                  split-K, each sequence cut into partitions of that many
+ *                  tokens whose (max, normaliser, unnormalised output)
+ *                  partials a second kernel merges with the rescale identity;
+ *                  PA_PARTITION_BALANCED: a persistent grid in which every warp
+ *                  streams an equal share of all sequences' 16-token stages;
+ *                  a (sequence, KV head) cut between warps is merged by the
+ *                  last warp to finish its share (num_seqs <= 2048)
+ *   workspace      device, >= pa_decode_workspace_bytes(...) bytes; 16-byte
+ *                  aligned (256-byte in balanced mode); unused (may be NULL)
+ *                  when no sequence needs more than one partition. Its prior
+ *                  contents do not matter: balanced mode clears its arrival
+ *                  counters (a memset on `stream`) at the start of each call
  * Errors (device): L_s outside [0, min(max_seq_len, max_blocks_per_seq*b)]
  * sets PA_DEVERR_SEQ_LEN and is clamped; a table entry out of range sets
  * PA_DEVERR_BLOCK_ID and its tokens are left out.
@@ -161,12 +167,17 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
               int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes pa_decode needs for these sizes (0 when one partition covers
- * max_seq_len or partition_tokens == 0). */
-size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                                 int32_t max_seq_len, int32_t partition_tokens);
+ * max_seq_len or partition_tokens == 0). The balanced mode's size depends on
+ * the current device's SM count. */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens);
 
-/* A partition size for pa_decode chosen from the batch shape and the current
- * device's SM count (0 = single pass). Returns a negative status on error. */
+/* partition_tokens value selecting pa_decode's balanced split. */
+#define PA_PARTITION_BALANCED (-1)
+
+/* A partition_tokens value for pa_decode chosen from the batch shape and the
+ * current device's SM count: 0 (single pass), PA_PARTITION_BALANCED, or a
+ * partition size. Returns a negative status (other than -1) on error. */
 int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                                     int32_t block_size);
 
@@ -187,9 +198,10 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
  *     array's device address (once per device, with that device current); make
  *     that first call before any stream capture.
  *   - Every call shares the one array, which keeps the previous call's
- *     partials; nothing in it needs to start at zero, because each call writes
- *     every partial it reads. Calls that overlap on the GPU (other streams,
- *     other threads) race on the array: serialise them.
+ *     partials. Nothing in it needs to start at zero: each call writes every
+ *     partial before reading it, and clears the balanced mode's arrival
+ *     counters itself. Calls that overlap on the GPU (other streams, other
+ *     threads) race on the array: serialise them.
  * Other arguments, errors and results are those of pa_decode.
  */
 #define PA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)

@@ -11,14 +11,15 @@ C ABI, declared in ``include/pa.h``); this package is its Python binding.
 """
 from ._lib import (DEVERR_BLOCK_ID, DEVERR_POSITION, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT,
                    EXPORTED, LIB_PATH, PagedKVError, lib)
-from ._lib import STATIC_WORKSPACE_BYTES
+from ._lib import PA_PARTITION_BALANCED, STATIC_WORKSPACE_BYTES
 from .ops import (check_copy_pairs, copy_blocks, decode, decode_static_workspace,
                   decode_workspace_bytes, default_partition, get_device_error, make_cache,
-                  slot_mapping, write_kv)
+                  new_workspace, slot_mapping, write_kv)
 
 __all__ = [
     "DEVERR_BLOCK_ID", "DEVERR_POSITION", "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
     "EXPORTED", "LIB_PATH", "PagedKVError", "lib", "check_copy_pairs", "copy_blocks", "decode",
     "decode_workspace_bytes", "default_partition", "get_device_error", "make_cache",
     "slot_mapping", "write_kv", "decode_static_workspace", "STATIC_WORKSPACE_BYTES",
+    "PA_PARTITION_BALANCED", "new_workspace",
 ]

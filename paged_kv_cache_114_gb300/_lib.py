@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.
 
 PA_F16, PA_BF16, PA_F32 = 0, 1, 2
 PA_OK = 0
+PA_PARTITION_BALANCED = -1
 STATUS = {
     0: "ok", -1: "null pointer", -2: "unsupported or mismatched dtype", -3: "unsupported shape",
     -4: "misaligned pointer", -5: "workspace missing or too small", -6: "invalid argument",
@@ -65,7 +66,7 @@ def _declare(lib):
                                      ctypes.c_int, i32, vp, sz, vp]),
         "pa_decode_static_workspace": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32,
                                                       ctypes.c_float, vp, ctypes.c_int, i32, vp]),
-        "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
+        "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "pa_decode_default_partition": (i32, [i32, i32, i32, i32]),
         "pa_get_device_error": (ctypes.c_int, [ctypes.POINTER(i32), vp]),
         "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),

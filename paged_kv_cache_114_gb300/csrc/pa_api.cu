@@ -97,6 +97,25 @@ int64_t decode_parts(int32_t max_seq_len, int32_t partition_tokens) {
   return (static_cast<int64_t>(max_seq_len) + partition_tokens - 1) / partition_tokens;
 }
 
+// Balanced-mode workspace: arrival counters [N][H_kv] (cleared by every call),
+// then per warp two partial slots of (m, l) and o for the g heads of a group.
+struct BalancedLayout {
+  size_t ml_offset, o_offset, total;
+  int64_t warps;
+};
+
+BalancedLayout balanced_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int sms) {
+  BalancedLayout l{};
+  const int64_t g = num_q_heads / num_kv_heads;
+  l.warps = static_cast<int64_t>(pa::balanced_ctas_per_sm(head_dim)) * sms * pa::kDecodeWarps;
+  const size_t counters = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(unsigned int);
+  l.ml_offset = (counters + 255) / 256 * 256;
+  l.o_offset = l.ml_offset + static_cast<size_t>(2 * l.warps * g * 2) * sizeof(float);
+  l.total = l.o_offset + static_cast<size_t>(2 * l.warps * g * head_dim) * sizeof(float);
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
@@ -219,9 +238,15 @@ int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* sr
   return PA_OK;
 }
 
-size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                                 int32_t max_seq_len, int32_t partition_tokens) {
-  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  if (partition_tokens == PA_PARTITION_BALANCED) {
+    DeviceInfo di;
+    if (!device_info(&di)) return 0;
+    const BalancedLayout lay = balanced_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, di.sms);
+    return lay.total;
+  }
   const int64_t parts = decode_parts(max_seq_len, partition_tokens);
   if (parts <= 1) return 0;
   return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
@@ -232,19 +257,22 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
   if (num_seqs < 0 || num_kv_heads <= 0 || max_seq_len < 0 || block_size <= 0) return PA_ERR_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
-  // Two decode CTAs are resident per SM. With at least 8 (sequence, KV head)
-  // units per SM the hardware scheduler balances whole sequences well; below
-  // that, cut sequences so the grid holds about 16 CTAs per SM. Partitions
-  // stay within [512, 2048] tokens: shorter ones pay the per-CTA prologue and
-  // the reduce too often, longer ones unbalance ragged batches.
+  // Whole (sequence, KV head) units, scheduled by the hardware, balance well
+  // once there are many of them per SM; below that, ragged lengths leave SMs
+  // idle at the end and the balanced split (equal stage ranges per warp) wins.
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
-  if (units == 0 || max_seq_len <= 512 || units >= 8LL * di.sms) return 0;
+  if (units == 0 || max_seq_len <= 16) return 0;
+  const int64_t tt = block_size < pa::kStageRows ? 2LL * block_size : pa::kStageRows;
+  const bool balanced_fits = num_seqs <= pa::kMaxBalancedSeqs &&
+                             num_kv_heads <= 2LL * di.sms * pa::kDecodeWarps &&
+                             units * ((max_seq_len + tt - 1) / tt) <= 0x7fffffffLL;
+  if (balanced_fits && units < 64LL * di.sms) return PA_PARTITION_BALANCED;
+  if (units >= 8LL * di.sms || max_seq_len <= 512) return 0;
+  // few units but no balanced split: fixed partitions, ~16 CTAs per SM
   const int64_t parts = (16LL * di.sms + units - 1) / units;
   int64_t pt = (max_seq_len + parts - 1) / parts;
   pt = ((pt + 255) / 256) * 256;
-  if (pt < 512) pt = 512;
-  if (pt > 2048) pt = 2048;
-  (void)block_size;
+  pt = pt < 512 ? 512 : (pt > 2048 ? 2048 : pt);
   return pt >= max_seq_len ? 0 : static_cast<int32_t>(pt);
 }
 
@@ -267,12 +295,21 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   const int g = num_q_heads / hkv;
   if (g > 16) return PA_ERR_SHAPE;
   if (max_blocks_per_seq <= 0 || max_seq_len < 0) return PA_ERR_ARG;
-  if (partition_tokens < 0 || partition_tokens % pa::kStageRows != 0) return PA_ERR_ARG;
+  const bool balanced = partition_tokens == PA_PARTITION_BALANCED;
+  if (!balanced && (partition_tokens < 0 || partition_tokens % pa::kStageRows != 0)) return PA_ERR_ARG;
   if (!std::isfinite(scale)) return PA_ERR_ARG;
   if (!aligned(q, 4) || !aligned(out, 4) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return PA_ERR_ALIGN;
-  const int64_t parts = decode_parts(max_seq_len, partition_tokens);
+  const int64_t parts = balanced ? 1 : decode_parts(max_seq_len, partition_tokens);
   if (parts > 65535 || num_seqs > 65535 || hkv > 65535) return PA_ERR_SHAPE;
+  // partial indices (row * partitions + partition) are 32-bit in the merges
+  if (static_cast<int64_t>(num_seqs) * num_q_heads * parts > 0x7fffffffLL) return PA_ERR_SHAPE;
+  if (balanced) {
+    // every per-sequence stage offset must fit the kernel's int32 prefix sums
+    const int64_t tt = b < pa::kStageRows ? 2LL * b : pa::kStageRows;
+    const int64_t max_stages = static_cast<int64_t>(num_seqs) * hkv * ((max_seq_len + tt - 1) / tt);
+    if (num_seqs > pa::kMaxBalancedSeqs || max_stages > 0x7fffffffLL) return PA_ERR_SHAPE;
+  }
 
   pa::DecodeArgs a{};
   a.q = q;
@@ -294,8 +331,10 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   a.ops_per_stage = pa::kStageRows / a.slot_rows;
   a.out_dtype = out_dtype;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  if (parts > 1) {
-    const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, D, max_seq_len,
+  dim3 grid(static_cast<unsigned>(hkv), static_cast<unsigned>(parts),
+            static_cast<unsigned>(num_seqs));
+  if (!balanced && parts > 1) {
+    const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, hkv, D, max_seq_len,
                                                   partition_tokens);
     if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
@@ -305,28 +344,42 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   a.err = di.err;
+  if (balanced) {
+    const BalancedLayout lay = balanced_layout(num_seqs, num_q_heads, hkv, D, di.sms);
+    if (hkv > lay.warps) return PA_ERR_SHAPE;  // a range group needs one warp per KV head
+    if (workspace == nullptr || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
+    char* ws = static_cast<char*>(workspace);
+    a.counters = reinterpret_cast<unsigned int*>(ws);
+    a.part_ml = reinterpret_cast<float*>(ws + lay.ml_offset);
+    a.part_o = reinterpret_cast<float*>(ws + lay.o_offset);
+    grid = dim3(static_cast<unsigned>(lay.warps / pa::kDecodeWarps), 1, 1);
+  }
 
   CUtensorMap tk, tv;
   if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
       !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
     return PA_ERR_CUDA;
 
-  const dim3 grid(static_cast<unsigned>(hkv), static_cast<unsigned>(parts),
-                  static_cast<unsigned>(num_seqs));
   const int tiles = (g + 7) / 8;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (balanced) {
+    // arrival counters start each call at zero, whatever the workspace held
+    e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(num_seqs) * hkv * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
   if (cache->dtype == PA_F16) {
-    e = D == 64 ? pa::launch_decode_f16_64(tk, tv, a, tiles, grid, st)
-        : D == 128 ? pa::launch_decode_f16_128(tk, tv, a, tiles, grid, st)
-                   : pa::launch_decode_f16_256(tk, tv, a, tiles, grid, st);
+    e = D == 64 ? pa::launch_decode_f16_64(tk, tv, a, tiles, grid, balanced, st)
+        : D == 128 ? pa::launch_decode_f16_128(tk, tv, a, tiles, grid, balanced, st)
+                   : pa::launch_decode_f16_256(tk, tv, a, tiles, grid, balanced, st);
   } else {
-    e = D == 64 ? pa::launch_decode_bf16_64(tk, tv, a, tiles, grid, st)
-        : D == 128 ? pa::launch_decode_bf16_128(tk, tv, a, tiles, grid, st)
-                   : pa::launch_decode_bf16_256(tk, tv, a, tiles, grid, st);
+    e = D == 64 ? pa::launch_decode_bf16_64(tk, tv, a, tiles, grid, balanced, st)
+        : D == 128 ? pa::launch_decode_bf16_128(tk, tv, a, tiles, grid, balanced, st)
+                   : pa::launch_decode_bf16_256(tk, tv, a, tiles, grid, balanced, st);
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (parts > 1) {
+  if (!balanced && parts > 1) {
     e = pa::launch_decode_reduce(a, D, st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }

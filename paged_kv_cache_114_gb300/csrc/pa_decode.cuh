@@ -3,32 +3,41 @@
 // Computes, for one sequence s and one KV head, the g query heads
 //   out[s][h] = sum_t softmax_t(scale * q[s][h] . K[t]) V[t],   t < L_s,
 // reading K[t], V[t] through the block table (logical block t / b, row t % b)
-// and accumulating block by block with a running maximum m, normaliser l and
+// and accumulating stage by stage with a running maximum m, normaliser l and
 // unnormalised output o ("PagedAttention: Virtual-Memory KV Cache Management,
 // ...", 3. Non-Contiguous Online Softmax Attention Kernel).
 //
-// Design (one CTA = one (sequence, KV head, partition)):
-//  * 4 warps; each warp owns a private ring of NS shared-memory stages. A stage
-//    is 16 token rows of K and of V for this KV head, loaded by TMA tensor
-//    copies straight from the scattered pool blocks (box = 64 head-dim
+// Building blocks shared by both kernels:
+//  * A stage is 16 token rows of K and of V for one KV head, loaded by TMA
+//    tensor copies straight from the scattered pool blocks (box = 64 head-dim
 //    elements x 1 head x up to 16 tokens x 1 block, 128-byte swizzle). Lane j
-//    issues the copies of the j-th block piece of the stage, so block-table
-//    lookups and copy issue are spread over the warp. Warps take stages
-//    round-robin, so the CTA streams consecutive tokens.
-//  * QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, in the
+//    of the issuing warp looks up and copies the j-th block piece of the stage.
+//  * Each warp owns a private ring of NS stages in shared memory and both
+//    issues and consumes them, so warps never wait on one another.
+//  * QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation in the
 //    transposed orientation S^T = K Q^T (M = 16 tokens, N = 8 query heads of
 //    the group, K = head_dim) and O^T = V^T P^T (M = 16 head-dim rows, N = 8
 //    heads, K = 16 tokens). The group's heads fill N, so each K/V row is read
 //    once per KV head whatever g is. P^T reaches the B-operand layout with
 //    movmatrix; P is split into a 16-bit high and low part so the PV product
 //    keeps ~16 bits of the fp32 weights.
-//  * Softmax state per head lives in registers; warps merge at the end through
-//    shared memory with the rescale identity, then the CTA writes either the
-//    normalised output (one partition) or (m, l, o) partials for the reduce.
 //  * Slots past the length, pieces of blocks whose id is out of range and the
 //    padding rows of blocks smaller than 8 tokens are masked: their logits are
 //    -inf and their V rows are zeroed in shared memory before PV, so stale or
 //    NaN bytes in the pool never enter the result.
+//
+// decode_kernel: one CTA per (sequence, KV head, partition); its 4 warps take
+// the partition's stages round-robin and merge through shared memory at the
+// end; the CTA writes the output (one partition) or (m, l, o) partials that
+// decode_reduce_kernel merges.
+//
+// decode_balanced_kernel: a persistent grid. The 16-token stages of all
+// sequences are cut into equal contiguous ranges, one per group of H_kv warps
+// (one warp per KV head), so every warp streams the same number of stages
+// whatever the lengths, and a group reads whole pool blocks together. A warp
+// writes each (sequence, KV head) piece it covers whole straight to the
+// output; a piece cut across ranges leaves one (m, l, o) partial per warp, and
+// the last warp to finish it (an atomicInc counter) merges them in order.
 #pragma once
 
 #include "pa_internal.h"
@@ -61,6 +70,110 @@ __device__ __forceinline__ void store_out(const DecodeArgs& a, int64_t idx, floa
   }
 }
 
+// ---------------------------------------------------------------- warp merges
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// E consecutive floats through L2 (bypassing L1, which is not coherent with
+// other SMs' writes), E = 2, 4 or 8 with matching alignment.
+template <int E>
+__device__ __forceinline__ void ldcg_vec(const float* p, float (&v)[E]) {
+  if constexpr (E == 2) {
+    const float2 t = __ldcg(reinterpret_cast<const float2*>(p));
+    v[0] = t.x; v[1] = t.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; i += 4) {
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(p + i));
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+    }
+  }
+}
+
+// Merges the (m, l, o) partials of `ncols` output rows with the rescale
+// identity M = max m_c, l = sum l_c 2^(m_c - M), out = sum o_c 2^(m_c - M) / l,
+// in contributor order. slot(c) gives contributor c's partial index, or -1 for
+// a contributor that holds none. For partial i and row j, (m, l) sit at
+// ml[i * ml_stride + j * ml_col] (+1) and the output at o[i * o_stride +
+// j * o_col .. + D); row j is written to out row out_row0 + j. Rows go four at
+// a time: lanes scan 32 contributors for the maxima and normalisers of all
+// four, then each lane accumulates D/32 consecutive outputs of the four rows
+// with unrolled vector loads, so a merge costs a few rounds of L2 latency.
+template <int D, typename SlotFn>
+__device__ __forceinline__ void merge_rows(const DecodeArgs& a, int n, SlotFn slot, int ncols,
+                                           const float* ml, int64_t ml_stride, int64_t ml_col,
+                                           const float* o, int64_t o_stride, int64_t o_col,
+                                           int64_t out_row0, int lane) {
+  constexpr int E = D / 32;
+  constexpr int CC = 4;
+  for (int j0 = 0; j0 < ncols; j0 += CC) {
+    float mmax[CC];
+    float lsum[CC];
+    float acc[CC][E];
+#pragma unroll
+    for (int j = 0; j < CC; ++j) {
+      mmax[j] = -INFINITY;
+      lsum[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[j][e] = 0.f;
+    }
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int sid = c0 + lane < n ? slot(c0 + lane) : -1;
+#pragma unroll
+      for (int j = 0; j < CC; ++j) {
+        const bool live = sid >= 0 && j0 + j < ncols;
+        mmax[j] = fmaxf(mmax[j], warp_max(live ? __ldcg(ml + sid * ml_stride + (j0 + j) * ml_col)
+                                              : -INFINITY));
+      }
+    }
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int sid = c0 + lane < n ? slot(c0 + lane) : -1;
+      float f[CC];
+#pragma unroll
+      for (int j = 0; j < CC; ++j) {
+        const bool live = sid >= 0 && j0 + j < ncols && mmax[j] != -INFINITY;
+        const float* p = ml + (live ? sid * ml_stride + (j0 + j) * ml_col : 0);
+        f[j] = live ? exp2f(__ldcg(p) - mmax[j]) : 0.f;
+        lsum[j] += warp_sum(live ? __ldcg(p + 1) * f[j] : 0.f);
+      }
+      const int nch = n - c0 < 32 ? n - c0 : 32;
+      // Branch-free so the unrolled loads of several partials are in flight
+      // together: a contributor or row without a partial reads partial 0 of
+      // row 0 (always in bounds) and its weight 0 selects the value away.
+#pragma unroll 4
+      for (int c = 0; c < nch; ++c) {
+        const int sc = __shfl_sync(0xffffffffu, sid, c);
+#pragma unroll
+        for (int j = 0; j < CC; ++j) {
+          const float fc = __shfl_sync(0xffffffffu, f[j], c);
+          const bool use = sc >= 0 && j0 + j < ncols;
+          float v[E];
+          ldcg_vec<E>(o + (use ? sc * o_stride + (j0 + j) * o_col : 0) + lane * E, v);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[j][e] += fc != 0.f ? v[e] * fc : 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < CC; ++j) {
+      if (j0 + j >= ncols) break;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        store_out(a, (out_row0 + j0 + j) * D + lane * E + e, lsum[j] > 0.f ? acc[j][e] / lsum[j] : 0.f);
+    }
+  }
+}
+
 template <int D, int NT, int NS>
 struct DecodeSmem {
   static constexpr int kHalves = D / 64;                  // 128-byte column pieces of a row
@@ -71,8 +184,226 @@ struct DecodeSmem {
   static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
   static constexpr int kBarOffset = kDataBytes;
   static constexpr int kMaskOffset = kBarOffset + kDecodeWarps * NS * 8;
-  static constexpr int kTotal = kMaskOffset + kDecodeWarps * NS * 4 + 1024;  // + alignment slack
+  static constexpr int kPrefixOffset = kMaskOffset + kDecodeWarps * NS * 4;  // balanced kernel
+  static constexpr int kTotal = kPrefixOffset + 1024;  // + base-alignment slack
 };
+
+// Per-warp online-softmax state for NT tiles of 8 query heads.
+template <int D, int NT>
+struct Acc {
+  float m[NT][2];
+  float l[NT][2];
+  float o[D / 16][NT][4];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int dm = 0; dm < D / 16; ++dm) o[dm][nt][0] = o[dm][nt][1] = o[dm][nt][2] = o[dm][nt][3] = 0.f;
+    }
+  }
+  // Sums the normaliser over the 8 lanes that share each head column.
+  __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v = l[nt][c];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l[nt][c] = v;
+      }
+    }
+  }
+};
+
+// q of the group of KV head kvh as the B operand of S^T = K Q^T
+// (k = head-dim index, n = head within the tile); heads past g are zero.
+template <int D, int NT>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int lane,
+                                       uint32_t (&qb)[NT][D / 16][2]) {
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+  const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int head = nt * 8 + gid;
+    const bool live = head < a.group;
+    const int64_t row =
+        (static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group + head) * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qb[nt][kk][0] = live ? __ldg(q32 + ((row + kk * 16 + tig * 2) >> 1)) : 0u;
+      qb[nt][kk][1] = live ? __ldg(q32 + ((row + kk * 16 + 8 + tig * 2) >> 1)) : 0u;
+    }
+  }
+}
+
+// Issues the TMA copies of one stage - tokens [t0, t0 + tt) of the sequence
+// whose table row starts at `table_row`, KV head kvh, clipped at tok_end -
+// into the stage at shared address `stage`, completing on mbarrier `bar`.
+// Stores the stage's valid-row mask (bit r = row r holds a token < tok_end of
+// a block with a valid id) to *mask. Called by the whole warp.
+template <int D>
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk,
+                                            const CUtensorMap* tmv, int64_t table_row, int kvh,
+                                            int t0, int tok_end, uint32_t stage, uint32_t bar,
+                                            uint32_t* mask, int lane) {
+  constexpr int HALVES = D / 64;
+  constexpr int HB = kStageRows * 128;
+  int blk = 0;
+  int off = 0;
+  bool ok = false;
+  if (lane < a.ops_per_stage) {
+    const int t = t0 + lane * a.tok_per_op;
+    if (t < tok_end) {
+      const int j = t / a.block_size;
+      off = t - j * a.block_size;
+      blk = __ldg(a.block_tables + table_row + j);
+      ok = blk >= 0 && blk < a.num_blocks;
+      if (!ok) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
+    }
+  }
+  const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
+  bool rv = false;
+  if (lane < kStageRows) {
+    const int jr = lane / a.slot_rows;
+    const int o = lane - jr * a.slot_rows;
+    const int tok = t0 + jr * a.tok_per_op + o;
+    rv = o < a.tok_per_op && tok < tok_end && ((okmask >> jr) & 1u);
+  }
+  const uint32_t rowmask = __ballot_sync(0xffffffffu, rv) & ((1u << kStageRows) - 1u);
+  if (lane == 0) {
+    *mask = rowmask;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * a.tok_per_op * D * 4u);
+  }
+  __syncwarp();
+  if (ok) {
+    const uint32_t dk = stage + lane * a.slot_rows * 128;
+    const uint32_t dv = dk + HALVES * HB;
+#pragma unroll
+    for (int c = 0; c < HALVES; ++c) {
+      tma_load_4d(dk + c * HB, tmk, bar, c * 64, kvh, off, blk);
+      tma_load_4d(dv + c * HB, tmv, bar, c * 64, kvh, off, blk);
+    }
+  }
+}
+
+// Folds one loaded stage into the warp's softmax state. `stage` is the
+// stage's shared address and `stage_ptr` the same memory as a generic pointer.
+template <bool IS_BF16, int D, int NT, bool SPLIT_P>
+__device__ __forceinline__ void compute_stage(uint32_t stage, uint8_t* stage_ptr, uint32_t rowmask,
+                                              const uint32_t (&qb)[NT][D / 16][2],
+                                              Acc<D, NT>& acc, float scale_log2, int lane) {
+  constexpr int TS = kStageRows;
+  constexpr int KD = D / 16;
+  constexpr int HALVES = D / 64;
+  constexpr int HB = kStageRows * 128;
+  const int gid = lane >> 2;
+  const uint32_t kb = stage;
+  const uint32_t vb = stage + HALVES * HB;
+
+  if (rowmask != (1u << TS) - 1u) {  // zero V rows that must not contribute
+    uint8_t* vp = stage_ptr + HALVES * HB;
+    for (int idx = lane; idx < TS * HALVES * 8; idx += 32) {
+      const int row = idx / (HALVES * 8);
+      const int rem = idx - row * (HALVES * 8);
+      if (!((rowmask >> row) & 1u)) {
+        *reinterpret_cast<uint4*>(vp + (rem >> 3) * HB + row * 128 + (rem & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    __syncwarp();
+  }
+
+  // S^T = K Q^T over head_dim.
+  float sacc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+  {
+    const int i = lane >> 3;
+    const int row = ((i & 1) << 3) + (lane & 7);
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk) {
+      const int chunk = ((kk & 3) << 1) + (i >> 1);
+      uint32_t af[4];
+      ldsm_x4(kb + (kk >> 2) * HB + row * 128 + ((chunk ^ (row & 7)) << 4), af);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816<IS_BF16>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+    }
+  }
+
+  // Online softmax update (log2 domain).
+  const bool v0 = (rowmask >> gid) & 1u;
+  const bool v1 = (rowmask >> (gid + 8)) & 1u;
+  float p[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float x[4];
+    x[0] = v0 ? sacc[nt][0] * scale_log2 : -INFINITY;
+    x[1] = v0 ? sacc[nt][1] * scale_log2 : -INFINITY;
+    x[2] = v1 ? sacc[nt][2] * scale_log2 : -INFINITY;
+    x[3] = v1 ? sacc[nt][3] * scale_log2 : -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float mx = fmaxf(x[c], x[c + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(acc.m[nt][c], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = exp2f(acc.m[nt][c] - m_use);
+      acc.m[nt][c] = m_new;
+      p[nt][c] = exp2f(x[c] - m_use);
+      p[nt][c + 2] = exp2f(x[c + 2] - m_use);
+      acc.l[nt][c] = acc.l[nt][c] * alpha + p[nt][c] + p[nt][c + 2];
+#pragma unroll
+      for (int dm = 0; dm < KD; ++dm) {
+        acc.o[dm][nt][c] *= alpha;
+        acc.o[dm][nt][c + 2] *= alpha;
+      }
+    }
+  }
+
+  // P^T as the B operand (k = token, n = head): transpose the 8x8 halves.
+  uint32_t bh[NT][2];
+  uint32_t bl[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t h01 = pack2<IS_BF16>(p[nt][0], p[nt][1]);
+    const uint32_t h23 = pack2<IS_BF16>(p[nt][2], p[nt][3]);
+    bh[nt][0] = movmatrix_trans(h01);
+    bh[nt][1] = movmatrix_trans(h23);
+    if constexpr (SPLIT_P) {
+      const float2 f01 = unpack2<IS_BF16>(h01);
+      const float2 f23 = unpack2<IS_BF16>(h23);
+      bl[nt][0] = movmatrix_trans(pack2<IS_BF16>(p[nt][0] - f01.x, p[nt][1] - f01.y));
+      bl[nt][1] = movmatrix_trans(pack2<IS_BF16>(p[nt][2] - f23.x, p[nt][3] - f23.y));
+    }
+  }
+
+  // O^T += V^T P^T over the 16 tokens of the stage.
+  {
+    const int i = lane >> 3;
+    const int row = ((i >> 1) << 3) + (lane & 7);
+#pragma unroll
+    for (int dm = 0; dm < KD; ++dm) {
+      const int chunk = ((dm & 3) << 1) + (i & 1);
+      uint32_t af[4];
+      ldsm_x4_trans(vb + (dm >> 2) * HB + row * 128 + ((chunk ^ (row & 7)) << 4), af);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816<IS_BF16>(acc.o[dm][nt], af, bh[nt][0], bh[nt][1]);
+        if constexpr (SPLIT_P) mma16816<IS_BF16>(acc.o[dm][nt], af, bl[nt][0], bl[nt][1]);
+      }
+    }
+  }
+}
+
+// ============================================================================
+// One CTA per (sequence, KV head, partition).
 
 template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
@@ -80,11 +411,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                   const DecodeArgs a) {
   using S = DecodeSmem<D, NT, NS>;
   constexpr int W = kDecodeWarps;
-  constexpr int TS = kStageRows;
   constexpr int KD = D / 16;
-  constexpr int HALVES = S::kHalves;
-  constexpr int HB = S::kHalfBytes;
-  constexpr uint32_t kAllRows = (1u << TS) - 1u;
   extern __shared__ __align__(16) uint8_t smem_raw[];
 
   const int kvh = blockIdx.x;
@@ -105,29 +432,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sm_base = smem_u32(sm);
-  uint32_t* masks = reinterpret_cast<uint32_t*>(sm + S::kMaskOffset);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(sm + S::kMaskOffset) + warp * NS;
 
   const int tt = a.ops_per_stage * a.tok_per_op;  // tokens per stage
   const int nst = (ntok + tt - 1) / tt;
   const int my_n = nst > warp ? (nst - warp - 1) / W + 1 : 0;
 
-  // q as the B operand of S^T = K Q^T: k = head-dim index, n = head in tile.
   uint32_t qb[NT][KD][2];
-  {
-    const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int head = nt * 8 + gid;
-      const bool live = head < a.group;
-      const int64_t row =
-          (static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group + head) * D;
-#pragma unroll
-      for (int kk = 0; kk < KD; ++kk) {
-        qb[nt][kk][0] = live ? __ldg(q32 + ((row + kk * 16 + tig * 2) >> 1)) : 0u;
-        qb[nt][kk][1] = live ? __ldg(q32 + ((row + kk * 16 + 8 + tig * 2) >> 1)) : 0u;
-      }
-    }
-  }
+  load_q<D, NT>(a, s, kvh, lane, qb);
 
   const uint32_t bar0 = sm_base + S::kBarOffset + warp * NS * 8;
   if (lane == 0) {
@@ -140,61 +452,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const uint32_t ring = sm_base + warp * NS * S::kStageBytes;
   uint8_t* const ring_ptr = sm + warp * NS * S::kStageBytes;
   const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
-
-  // Issue the TMA copies of this warp's it-th stage into slot it % NS.
   auto issue = [&](int it) {
     const int slot = it % NS;
-    const int t0 = tok_begin + (warp + it * W) * tt;
-    int blk = 0;
-    int off = 0;
-    bool ok = false;
-    if (lane < a.ops_per_stage) {
-      const int t = t0 + lane * a.tok_per_op;
-      if (t < tok_end) {
-        const int j = t / a.block_size;
-        off = t - j * a.block_size;
-        blk = __ldg(a.block_tables + table_row + j);
-        ok = blk >= 0 && blk < a.num_blocks;
-        if (!ok) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
-      }
-    }
-    const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
-    bool rv = false;
-    if (lane < TS) {
-      const int jr = lane / a.slot_rows;
-      const int o = lane - jr * a.slot_rows;
-      const int tok = t0 + jr * a.tok_per_op + o;
-      rv = o < a.tok_per_op && tok < tok_end && ((okmask >> jr) & 1u);
-    }
-    const uint32_t rowmask = __ballot_sync(0xffffffffu, rv) & kAllRows;
-    const uint32_t bar = bar0 + 8 * slot;
-    if (lane == 0) {
-      masks[warp * NS + slot] = rowmask;
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * a.tok_per_op * D * 4u);
-    }
-    __syncwarp();
-    if (ok) {
-      const uint32_t dk = ring + slot * S::kStageBytes + lane * a.slot_rows * 128;
-      const uint32_t dv = dk + HALVES * HB;
-#pragma unroll
-      for (int c = 0; c < HALVES; ++c) {
-        tma_load_4d(dk + c * HB, &tmk, bar, c * 64, kvh, off, blk);
-        tma_load_4d(dv + c * HB, &tmv, bar, c * 64, kvh, off, blk);
-      }
-    }
+    issue_stage<D>(a, &tmk, &tmv, table_row, kvh, tok_begin + (warp + it * W) * tt, tok_end,
+                   ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
   };
 
-  float m_run[NT][2];
-  float l_run[NT][2];
-  float o[KD][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-    for (int dm = 0; dm < KD; ++dm) o[dm][nt][0] = o[dm][nt][1] = o[dm][nt][2] = o[dm][nt][3] = 0.f;
-  }
-
+  Acc<D, NT> acc;
+  acc.reset();
   const int pro = my_n < NS ? my_n : NS;
   for (int i = 0; i < pro; ++i) issue(i);
 
@@ -207,106 +472,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       aborted = true;
       break;
     }
-    const uint32_t kb = ring + slot * S::kStageBytes;
-    const uint32_t vb = kb + HALVES * HB;
-    const uint32_t rowmask = masks[warp * NS + slot];
-
-    if (rowmask != kAllRows) {  // zero V rows that must not contribute
-      uint8_t* vp = ring_ptr + slot * S::kStageBytes + HALVES * HB;
-      for (int idx = lane; idx < TS * HALVES * 8; idx += 32) {
-        const int row = idx / (HALVES * 8);
-        const int rem = idx - row * (HALVES * 8);
-        if (!((rowmask >> row) & 1u)) {
-          *reinterpret_cast<uint4*>(vp + (rem >> 3) * HB + row * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      __syncwarp();
-    }
-
-    // S^T = K Q^T over head_dim.
-    float sacc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-    {
-      const int i = lane >> 3;
-      const int row = ((i & 1) << 3) + (lane & 7);
-#pragma unroll
-      for (int kk = 0; kk < KD; ++kk) {
-        const int chunk = ((kk & 3) << 1) + (i >> 1);
-        uint32_t af[4];
-        ldsm_x4(kb + (kk >> 2) * HB + row * 128 + ((chunk ^ (row & 7)) << 4), af);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816<IS_BF16>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
-      }
-    }
-
-    // Online softmax update (log2 domain).
-    const bool v0 = (rowmask >> gid) & 1u;
-    const bool v1 = (rowmask >> (gid + 8)) & 1u;
-    float p[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float x[4];
-      x[0] = v0 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
-      x[1] = v0 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
-      x[2] = v1 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
-      x[3] = v1 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float mx = fmaxf(x[c], x[c + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[nt][c], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = exp2f(m_run[nt][c] - m_use);
-        m_run[nt][c] = m_new;
-        p[nt][c] = exp2f(x[c] - m_use);
-        p[nt][c + 2] = exp2f(x[c + 2] - m_use);
-        l_run[nt][c] = l_run[nt][c] * alpha + p[nt][c] + p[nt][c + 2];
-#pragma unroll
-        for (int dm = 0; dm < KD; ++dm) {
-          o[dm][nt][c] *= alpha;
-          o[dm][nt][c + 2] *= alpha;
-        }
-      }
-    }
-
-    // P^T as the B operand (k = token, n = head): transpose the 8x8 halves.
-    uint32_t bh[NT][2];
-    uint32_t bl[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t h01 = pack2<IS_BF16>(p[nt][0], p[nt][1]);
-      const uint32_t h23 = pack2<IS_BF16>(p[nt][2], p[nt][3]);
-      bh[nt][0] = movmatrix_trans(h01);
-      bh[nt][1] = movmatrix_trans(h23);
-      if constexpr (SPLIT_P) {
-        const float2 f01 = unpack2<IS_BF16>(h01);
-        const float2 f23 = unpack2<IS_BF16>(h23);
-        bl[nt][0] = movmatrix_trans(pack2<IS_BF16>(p[nt][0] - f01.x, p[nt][1] - f01.y));
-        bl[nt][1] = movmatrix_trans(pack2<IS_BF16>(p[nt][2] - f23.x, p[nt][3] - f23.y));
-      }
-    }
-
-    // O^T += V^T P^T over the 16 tokens of the stage.
-    {
-      const int i = lane >> 3;
-      const int row = ((i >> 1) << 3) + (lane & 7);
-#pragma unroll
-      for (int dm = 0; dm < KD; ++dm) {
-        const int chunk = ((dm & 3) << 1) + (i & 1);
-        uint32_t af[4];
-        ldsm_x4_trans(vb + (dm >> 2) * HB + row * 128 + ((chunk ^ (row & 7)) << 4), af);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma16816<IS_BF16>(o[dm][nt], af, bh[nt][0], bh[nt][1]);
-          if constexpr (SPLIT_P) mma16816<IS_BF16>(o[dm][nt], af, bl[nt][0], bl[nt][1]);
-        }
-      }
-    }
-
+    compute_stage<IS_BF16, D, NT, SPLIT_P>(ring + slot * S::kStageBytes,
+                                           ring_ptr + slot * S::kStageBytes, masks[slot], qb, acc,
+                                           a.scale_log2, lane);
     fence_proxy_async_smem();  // our generic reads/writes of this slot precede the next TMA into it
     __syncwarp();
     if (it + NS < my_n) issue(it + NS);
@@ -316,27 +484,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
     const int last = (it + NS < my_n) ? it + NS : my_n;
     for (int j = it; j < last; ++j) mbar_wait_bounded(bar0 + 8 * (j % NS), (j / NS) & 1, kWaitLimitNs);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m_run[nt][0] = m_run[nt][1] = -INFINITY;
-      l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-      for (int dm = 0; dm < KD; ++dm) o[dm][nt][0] = o[dm][nt][1] = o[dm][nt][2] = o[dm][nt][3] = 0.f;
-    }
+    acc.reset();
   }
-
-  // Per-head normaliser: sum the 8 lanes that share a head column.
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float v = l_run[nt][c];
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      l_run[nt][c] = v;
-    }
-  }
+  acc.reduce_l();
 
   // Merge the warps' states through shared memory (the rings are free now).
   __syncthreads();
@@ -352,7 +502,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       for (int r = 0; r < 4; ++r) {
         const int d = dm * 16 + gid + ((r >> 1) << 3);
         const int col = nt * 8 + tig * 2 + (r & 1);
-        c_o[(warp * COLS + col) * D + d] = o[dm][nt][r];
+        c_o[(warp * COLS + col) * D + d] = acc.o[dm][nt][r];
       }
     }
   }
@@ -362,8 +512,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col = nt * 8 + tig * 2 + c;
-        c_m[warp * COLS + col] = m_run[nt][c];
-        c_l[warp * COLS + col] = l_run[nt][c];
+        c_m[warp * COLS + col] = acc.m[nt][c];
+        c_l[warp * COLS + col] = acc.l[nt][c];
       }
     }
   }
@@ -375,23 +525,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     float mmax = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) mmax = fmaxf(mmax, c_m[w * COLS + col]);
-    float acc = 0.f;
+    float o = 0.f;
     float lsum = 0.f;
     if (mmax != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < W; ++w) {
         const float f = exp2f(c_m[w * COLS + col] - mmax);
-        acc += c_o[(w * COLS + col) * D + d] * f;
+        o += c_o[(w * COLS + col) * D + d] * f;
         lsum += c_l[w * COLS + col] * f;
       }
     }
     const int64_t head = static_cast<int64_t>(kvh) * a.group + col;
     const int64_t sh = static_cast<int64_t>(s) * a.num_q_heads + head;
     if (direct) {
-      store_out(a, sh * D + d, lsum > 0.f ? acc / lsum : 0.f);
+      store_out(a, sh * D + d, lsum > 0.f ? o / lsum : 0.f);
     } else {
       const int64_t pidx = sh * a.max_parts + part;
-      a.part_o[pidx * D + d] = acc;
+      a.part_o[pidx * D + d] = o;
       if (d == 0) {
         a.part_ml[pidx * 2] = mmax;
         a.part_ml[pidx * 2 + 1] = lsum;
@@ -399,6 +549,288 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
   }
 }
+
+// ============================================================================
+// Balanced: persistent warps, equal stage ranges per group of H_kv warps.
+//
+// The 16-token stages of all sequences, in sequence order, form one line of
+// S "head-stages" (pre[s] = stages before sequence s). The line is cut into
+// G = floor(warps / H_kv) equal ranges; warp grp*H_kv + h streams KV head h of
+// range grp. The H_kv warps of a range read the same token rows of every
+// head at the same time, so each pool block is consumed whole, as in the
+// per-partition grid, while every warp gets the same amount of work.
+
+// Position of one warp's stream on the line: sequence s, stage j of it.
+struct Cursor {
+  int s;     // sequence
+  int j;     // stage within the sequence
+  int n;     // stages of this sequence
+  int ps;    // line index of the sequence's first stage
+  int len;   // sequence length (tokens)
+};
+
+__device__ __forceinline__ Cursor cursor_at(const DecodeArgs& a, const int32_t* pre, int g) {
+  int lo = 0;
+  int hi = a.num_seqs - 1;  // largest s with pre[s] <= g: a non-empty sequence
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  Cursor c;
+  c.s = lo;
+  c.n = pre[lo + 1] - pre[lo];
+  c.j = g - pre[lo];
+  c.ps = pre[lo];
+  c.len = decode_seq_len(a, lo, false);
+  return c;
+}
+
+__device__ __forceinline__ void cursor_next(const DecodeArgs& a, const int32_t* pre, Cursor& c) {
+  if (++c.j < c.n) return;
+  c.j = 0;
+  do {
+    ++c.s;
+  } while (c.s < a.num_seqs && pre[c.s + 1] == pre[c.s]);
+  if (c.s < a.num_seqs) {
+    c.n = pre[c.s + 1] - pre[c.s];
+    c.ps = pre[c.s];
+    c.len = decode_seq_len(a, c.s, false);
+  }
+}
+
+// Range owning line index g when S stages are cut into R ranges, range r taking
+// [r*S/R, (r+1)*S/R). Ranges can be empty when R > S.
+__device__ __forceinline__ int64_t stage_owner(int64_t g, int64_t S, int64_t R) {
+  return ((g + 1) * R - 1) / S;
+}
+
+__device__ __forceinline__ int64_t range_start(int64_t r, int64_t S, int64_t R) {
+  return (r * S) / R;
+}
+
+template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    decode_balanced_kernel(const __grid_constant__ CUtensorMap tmk,
+                           const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
+  using S = DecodeSmem<D, NT, NS>;
+  constexpr int W = kDecodeWarps;
+  constexpr int KD = D / 16;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ int warp_tot[W];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+  const int N = a.num_seqs;
+  const int hkv = a.num_kv_heads;
+  const int tt = a.ops_per_stage * a.tok_per_op;
+
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sm_base = smem_u32(sm);
+  int32_t* pre = reinterpret_cast<int32_t*>(sm + S::kPrefixOffset);  // [N + 1]
+
+  // ---- line offset of every sequence: pre[s] = sum_{s'<s} ceil(L_s'/tt)
+  {
+    const int per = (N + W * 32 - 1) / (W * 32);
+    const int beg = min(N, static_cast<int>(threadIdx.x) * per);
+    const int end = min(N, beg + per);
+    int local = 0;
+    for (int s = beg; s < end; ++s) {
+      const int L = decode_seq_len(a, s, blockIdx.x == 0);
+      local += (L + tt - 1) / tt;
+    }
+    int x = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    int run = x - local;
+    int total = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      if (w < warp) run += warp_tot[w];
+      total += warp_tot[w];
+    }
+    for (int s = beg; s < end; ++s) {
+      pre[s] = run;
+      run += (decode_seq_len(a, s, false) + tt - 1) / tt;
+    }
+    if (threadIdx.x == 0) pre[N] = total;
+    __syncthreads();
+  }
+
+  // ---- zero the output rows of empty sequences (CTA c takes s = c mod grid)
+  for (int s = blockIdx.x; s < N; s += gridDim.x) {
+    if (pre[s + 1] != pre[s]) continue;
+    const int64_t base = static_cast<int64_t>(s) * a.num_q_heads * D;
+    for (int i = threadIdx.x; i < a.num_q_heads * D; i += W * 32) store_out(a, base + i, 0.f);
+  }
+
+  // ---- this warp's KV head and range of the line
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * W + warp;
+  const int64_t ranges = static_cast<int64_t>(gridDim.x) * W / hkv;
+  const int kvh = static_cast<int>(wid % hkv);
+  const int64_t grp = wid / hkv;
+  const int64_t stot = pre[N];
+  if (grp >= ranges) return;  // no CTA-wide barrier follows
+  const int g0 = static_cast<int>(range_start(grp, stot, ranges));
+  const int g1 = static_cast<int>(range_start(grp + 1, stot, ranges));
+  if (g0 >= g1) return;
+  const int count = g1 - g0;
+
+  uint32_t* masks = reinterpret_cast<uint32_t*>(sm + S::kMaskOffset) + warp * NS;
+  const uint32_t bar0 = sm_base + S::kBarOffset + warp * NS * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8 * i, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint32_t ring = sm_base + warp * NS * S::kStageBytes;
+  uint8_t* const ring_ptr = sm + warp * NS * S::kStageBytes;
+
+  Cursor ic = cursor_at(a, pre, g0);  // next stage to issue
+  Cursor cc = ic;                     // stage being computed
+  auto issue = [&](int it) {
+    const int slot = it % NS;
+    issue_stage<D>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, kvh, ic.j * tt,
+                   ic.len, ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
+    cursor_next(a, pre, ic);
+  };
+  const int pro = count < NS ? count : NS;
+  for (int i = 0; i < pro; ++i) issue(i);
+
+  uint32_t qb[NT][KD][2];
+  load_q<D, NT>(a, cc.s, kvh, lane, qb);
+  Acc<D, NT> acc;
+  acc.reset();
+  bool aborted = false;
+
+  for (int it = 0; it < count; ++it) {
+    const int slot = it % NS;
+    if (!aborted) {
+      const bool got = mbar_wait_bounded(bar0 + 8 * slot, (it / NS) & 1, kWaitLimitNs);
+      if (__any_sync(0xffffffffu, !got)) {
+        aborted = true;
+        if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+        const int last = (it + NS < count) ? it + NS : count;
+        for (int j = it; j < last; ++j)
+          mbar_wait_bounded(bar0 + 8 * (j % NS), (j / NS) & 1, kWaitLimitNs);
+      }
+    }
+    if (!aborted) {
+      compute_stage<IS_BF16, D, NT, SPLIT_P>(ring + slot * S::kStageBytes,
+                                             ring_ptr + slot * S::kStageBytes, masks[slot], qb,
+                                             acc, a.scale_log2, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (it + NS < count) issue(it + NS);
+    }
+
+    const bool piece_end = (cc.j == cc.n - 1) || (it == count - 1);
+    if (!piece_end) {
+      cursor_next(a, pre, cc);
+      continue;
+    }
+
+    // ---- the warp is done with its share of piece (cc.s, kvh)
+    if (aborted) acc.reset();  // contribute nothing, but still take part
+    acc.reduce_l();
+    const int ps = cc.ps;
+    const int pe = cc.ps + cc.n;
+    const int64_t row0 = static_cast<int64_t>(cc.s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group;
+    if (ps >= g0 && pe <= g1) {
+      // whole piece: normalise and write
+#pragma unroll
+      for (int dm = 0; dm < KD; ++dm) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int col = nt * 8 + tig * 2 + (r & 1);
+            if (col < a.group) {
+              const int d = dm * 16 + gid + ((r >> 1) << 3);
+              const float l = acc.l[nt][r & 1];
+              store_out(a, (row0 + col) * D + d, l > 0.f ? acc.o[dm][nt][r] / l : 0.f);
+            }
+          }
+        }
+      }
+    } else {
+      // cut piece: leave a partial, the last contributor merges
+      const int64_t slot_id = wid * 2 + (ps <= g0 ? 0 : 1);
+      float* po = a.part_o + slot_id * a.group * D;
+      float* pml = a.part_ml + slot_id * a.group * 2;
+#pragma unroll
+      for (int dm = 0; dm < KD; ++dm) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int col = nt * 8 + tig * 2 + (r & 1);
+            if (col < a.group) po[col * D + dm * 16 + gid + ((r >> 1) << 3)] = acc.o[dm][nt][r];
+          }
+        }
+      }
+      if (gid == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int col = nt * 8 + tig * 2 + c;
+            if (col < a.group) {
+              pml[col * 2] = acc.m[nt][c];
+              pml[col * 2 + 1] = acc.l[nt][c];
+            }
+          }
+        }
+      }
+      __threadfence();
+      __syncwarp();
+      // Contributors: the warps of head kvh in the non-empty ranges ra..rb that
+      // meet [ps, pe). Ranges in between are empty only when there are more
+      // ranges than stages.
+      const int64_t ra = stage_owner(ps, stot, ranges);
+      const int64_t rb = stage_owner(pe - 1, stot, ranges);
+      const int span = static_cast<int>(rb - ra + 1);
+      auto nonempty = [&](int64_t r) {
+        return range_start(r, stot, ranges) < range_start(r + 1, stot, ranges);
+      };
+      int contrib = 0;
+      for (int c0 = 0; c0 < span; c0 += 32)
+        contrib += __popc(__ballot_sync(0xffffffffu, c0 + lane < span && nonempty(ra + c0 + lane)));
+      unsigned int old = 0;
+      if (lane == 0)
+        old = atomicInc(a.counters + static_cast<int64_t>(cc.s) * hkv + kvh,
+                        static_cast<unsigned int>(contrib - 1));
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old == static_cast<unsigned int>(contrib - 1)) {
+        __threadfence();
+        const bool ra_first = range_start(ra, stot, ranges) == ps;  // piece is ra's first
+        auto slot = [&](int c) -> int {
+          const int64_t r = ra + c;
+          if (!nonempty(r)) return -1;
+          return static_cast<int>((r * hkv + kvh) * 2 + ((c == 0 && !ra_first) ? 1 : 0));
+        };
+        merge_rows<D>(a, span, slot, a.group, a.part_ml, a.group * 2, 2, a.part_o,
+                      static_cast<int64_t>(a.group) * D, D, row0, lane);
+      }
+    }
+
+    if (it + 1 < count) {
+      cursor_next(a, pre, cc);
+      load_q<D, NT>(a, cc.s, kvh, lane, qb);
+      acc.reset();
+    }
+  }
+}
+
+// ============================================================================
+// launch helpers
 
 // Stages per warp: keeps 2 CTAs (8 warps) resident per SM for D <= 128.
 template <int D>
@@ -408,9 +840,17 @@ constexpr int decode_stages() {
 
 template <bool IS_BF16, int D, int NT>
 cudaError_t launch_decode_tiles(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                dim3 grid, cudaStream_t st) {
+                                dim3 grid, bool balanced, cudaStream_t st) {
   constexpr int NS = decode_stages<D>();
   using S = DecodeSmem<D, NT, NS>;
+  if (balanced) {
+    auto kern = decode_balanced_kernel<IS_BF16, D, NT, NS, true>;
+    const int smem = S::kTotal + (a.num_seqs + 1) * 4;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kDecodeWarps * 32, smem, st>>>(tk, tv, a);
+    return cudaGetLastError();
+  }
   auto kern = decode_kernel<IS_BF16, D, NT, NS, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
   if (e != cudaSuccess) return e;
@@ -420,9 +860,9 @@ cudaError_t launch_decode_tiles(const CUtensorMap& tk, const CUtensorMap& tv, co
 
 template <bool IS_BF16, int D>
 cudaError_t launch_decode_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                   int group_tiles, dim3 grid, cudaStream_t st) {
-  if (group_tiles == 1) return launch_decode_tiles<IS_BF16, D, 1>(tk, tv, a, grid, st);
-  if (group_tiles == 2) return launch_decode_tiles<IS_BF16, D, 2>(tk, tv, a, grid, st);
+                                   int group_tiles, dim3 grid, bool balanced, cudaStream_t st) {
+  if (group_tiles == 1) return launch_decode_tiles<IS_BF16, D, 1>(tk, tv, a, grid, balanced, st);
+  if (group_tiles == 2) return launch_decode_tiles<IS_BF16, D, 2>(tk, tv, a, grid, balanced, st);
   return cudaErrorInvalidValue;
 }
 

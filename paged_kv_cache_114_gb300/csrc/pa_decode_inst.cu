@@ -21,8 +21,9 @@
 namespace pa {
 
 cudaError_t PA_FN(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int group_tiles,
-                  dim3 grid, cudaStream_t st) {
-  return launch_decode_dispatch<PA_INST_BF16 != 0, PA_INST_D>(tk, tv, a, group_tiles, grid, st);
+                  dim3 grid, bool balanced, cudaStream_t st) {
+  return launch_decode_dispatch<PA_INST_BF16 != 0, PA_INST_D>(tk, tv, a, group_tiles, grid, balanced,
+                                                              st);
 }
 
 }  // namespace pa

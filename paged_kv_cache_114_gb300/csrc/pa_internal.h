@@ -17,6 +17,7 @@ struct DecodeArgs {
   void* out;                     // [N][Hq][D] of out_dtype
   float* part_o;                 // [N][Hq][max_parts][D]   (split-K only)
   float* part_ml;                // [N][Hq][max_parts][2]   (max in log2 units, normaliser)
+  unsigned int* counters;        // balanced mode: [N][H_kv] arrival counters, zero between calls
   const int32_t* block_tables;   // [N][max_blocks]
   const int32_t* seq_lens;       // [N]
   int* err;                      // device error word
@@ -38,19 +39,31 @@ constexpr int kStageRows = 16;
 constexpr int kDecodeWarps = 4;
 
 // Decode launchers, one per (dtype, head_dim) translation unit.
-// group_tiles = ceil(group / 8) in {1, 2}.
+// group_tiles = ceil(group / 8) in {1, 2}; balanced selects the persistent
+// equal-range kernel (grid = its CTA count) over the per-partition one.
 cudaError_t launch_decode_f16_64(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                 int group_tiles, dim3 grid, cudaStream_t st);
+                                 int group_tiles, dim3 grid, bool balanced,
+                                  cudaStream_t st);
 cudaError_t launch_decode_f16_128(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                  int group_tiles, dim3 grid, cudaStream_t st);
+                                  int group_tiles, dim3 grid, bool balanced,
+                                  cudaStream_t st);
 cudaError_t launch_decode_f16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                  int group_tiles, dim3 grid, cudaStream_t st);
+                                  int group_tiles, dim3 grid, bool balanced,
+                                  cudaStream_t st);
 cudaError_t launch_decode_bf16_64(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                  int group_tiles, dim3 grid, cudaStream_t st);
+                                  int group_tiles, dim3 grid, bool balanced,
+                                  cudaStream_t st);
 cudaError_t launch_decode_bf16_128(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                   int group_tiles, dim3 grid, cudaStream_t st);
+                                   int group_tiles, dim3 grid, bool balanced,
+                                  cudaStream_t st);
 cudaError_t launch_decode_bf16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                   int group_tiles, dim3 grid, cudaStream_t st);
+                                   int group_tiles, dim3 grid, bool balanced,
+                                  cudaStream_t st);
+
+// Balanced mode: resident CTAs per SM of the persistent grid, and the largest
+// batch whose per-sequence offsets fit the kernel's shared memory.
+constexpr int balanced_ctas_per_sm(int head_dim) { return head_dim > 128 ? 1 : 2; }
+constexpr int kMaxBalancedSeqs = 2048;
 
 // Merges split-K partials into out (pa_decode_reduce.cu).
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);

@@ -51,8 +51,8 @@ extern "C" int pa_decode_static_workspace(const void* q, int32_t num_seqs, int32
                                           pa_dtype out_dtype, int32_t partition_tokens,
                                           void* stream) {
   if (cache == nullptr) return PA_ERR_NULL;
-  const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, cache->head_dim,
-                                                max_seq_len, partition_tokens);
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, cache->num_kv_heads,
+                                                cache->head_dim, max_seq_len, partition_tokens);
   if (need > PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
   void* ws = nullptr;
   if (need > 0) {

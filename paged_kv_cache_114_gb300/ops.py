@@ -100,15 +100,25 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
     _lib.check("pa_copy_blocks", st)
 
 
-def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int,
-                           partition_tokens: int) -> int:
-    return int(_lib.lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len,
-                                                    partition_tokens))
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           max_seq_len: int, partition_tokens: int) -> int:
+    return int(_lib.lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                    max_seq_len, partition_tokens))
+
+
+def new_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                  max_seq_len: int, partition_tokens: int, device) -> Optional[torch.Tensor]:
+    """A workspace for pa_decode (None when the call needs none); reusable for
+    any later call of the same mode and shape."""
+    n = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                               partition_tokens)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
 
 
 def default_partition(num_seqs: int, num_kv_heads: int, max_seq_len: int, block_size: int) -> int:
     v = int(_lib.lib().pa_decode_default_partition(num_seqs, num_kv_heads, max_seq_len, block_size))
-    _lib.check("pa_decode_default_partition", min(v, 0))
+    if v < 0 and v != _lib.PA_PARTITION_BALANCED:
+        _lib.check("pa_decode_default_partition", v)
     return v
 
 
@@ -122,8 +132,10 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     ``max_seq_len`` bounds ``seq_lens`` (it sizes the launch, so the call never
     reads the lengths back). ``partition_tokens`` = 0 runs one pass per
     (sequence, KV head); a multiple of 16 runs split-K with a reduce;
-    None picks the library's default for this shape. The workspace, when a
-    split needs one, comes from the caller or from torch's allocator.
+    ``PA_PARTITION_BALANCED`` (-1) gives every warp an equal share of the
+    work; None picks the library's default for this shape. The workspace,
+    when a split needs one, comes from the caller (see :func:`new_workspace`)
+    or is allocated here.
     """
     dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens)
     _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [N, Hq, D] with the cache's D")
@@ -139,9 +151,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     nb, b, hkv, _ = k_cache.shape
     if partition_tokens is None:
         partition_tokens = default_partition(n, hkv, max_seq_len, b)
-    ws_bytes = decode_workspace_bytes(n, hq, d, max_seq_len, partition_tokens)
-    if ws_bytes and workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = new_workspace(n, hq, hkv, d, max_seq_len, partition_tokens, dev)
     if workspace is not None:
         _cuda(workspace, q)
     cache = make_cache(k_cache, v_cache)

@@ -35,9 +35,11 @@ def gpu_scenario(w, dev, *, partition_tokens=None, out_dtype=torch.float32, pair
                             w.block_size, w.num_blocks)
     if len(w.positions):
         pa.write_kv(to_dev(w.key, dev, w.dtype), to_dev(w.value, dev, w.dtype), slots, k, v)
-    out = pa.decode(to_dev(w.q, dev, w.dtype), k, v, tables, to_dev(w.seq_lens, dev), w.scale,
-                    max_seq_len=max(w.max_seq_len, 1), out_dtype=out_dtype,
-                    partition_tokens=partition_tokens)
+    # NaN-filled so a row the kernel fails to write cannot pass on stale memory
+    out = torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype,
+                     device=dev)
+    pa.decode(to_dev(w.q, dev, w.dtype), k, v, tables, to_dev(w.seq_lens, dev), w.scale,
+              max_seq_len=max(w.max_seq_len, 1), out=out, partition_tokens=partition_tokens)
     err = pa.get_device_error(dev)
     return {"k": k, "v": v, "slots": slots, "out": out, "err": err}
 

@@ -49,10 +49,14 @@ def test_version_and_status_strings(lib):
 
 def test_workspace_bytes(lib):
     # N * Hq * ceil(L / P) * (D + 2) floats; no workspace when one partition covers L
-    assert lib.pa_decode_workspace_bytes(8, 32, 128, 32768, 512) == 8 * 32 * 64 * 130 * 4
-    assert lib.pa_decode_workspace_bytes(8, 32, 128, 512, 512) == 0
-    assert lib.pa_decode_workspace_bytes(8, 32, 128, 4096, 0) == 0
-    assert lib.pa_decode_workspace_bytes(4, 4, 64, 33, 16) == 4 * 4 * 3 * 66 * 4
+    assert lib.pa_decode_workspace_bytes(8, 32, 8, 128, 32768, 512) == 8 * 32 * 64 * 130 * 4
+    assert lib.pa_decode_workspace_bytes(8, 32, 8, 128, 512, 512) == 0
+    assert lib.pa_decode_workspace_bytes(8, 32, 8, 128, 4096, 0) == 0
+    assert lib.pa_decode_workspace_bytes(4, 4, 4, 64, 33, 16) == 4 * 4 * 3 * 66 * 4
+    # the balanced mode's size depends on the device's SM count: 0 without a device
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.pa_decode_workspace_bytes(8, 32, 8, 128, 4096, -1) == 0
 
 
 def test_check_copy_pairs(lib):

@@ -50,16 +50,18 @@ def test_config1_tiny(dev, partition, out_dtype):
 
 CASES = [
     # dtype, D, Hq, Hkv, b, lens, partitions
-    ("f16", 64, 8, 8, 16, [1, 15, 16, 17, 100, 333], (0, 64)),
-    ("bf16", 128, 32, 8, 16, [5, 512, 513, 1000], (0, 128, 512)),
-    ("f16", 128, 16, 1, 32, [1, 31, 32, 33, 700], (0, 96)),
-    ("bf16", 256, 8, 4, 8, [3, 64, 257], (0, 64)),
-    ("f16", 128, 12, 4, 4, [1, 4, 5, 99], (0, 32)),
-    ("bf16", 64, 6, 6, 1, [1, 2, 17], (0, 16)),
-    ("f16", 128, 20, 2, 64, [1, 63, 64, 65, 1000], (0, 256)),
-    ("f16", 128, 4, 4, 2, [0, 7, 0, 40], (0, 16)),
-    ("bf16", 128, 64, 8, 16, [1, 2, 3, 16, 17, 4097], (0, 512)),
-    ("f16", 256, 16, 16, 16, [300, 1], (0, 128)),
+    ("f16", 64, 8, 8, 16, [1, 15, 16, 17, 100, 333], (0, 64, -1)),
+    ("bf16", 128, 32, 8, 16, [5, 512, 513, 1000], (0, 128, 512, -1)),
+    ("f16", 128, 16, 1, 32, [1, 31, 32, 33, 700], (0, 96, -1)),
+    ("bf16", 256, 8, 4, 8, [3, 64, 257], (0, 64, -1)),
+    ("f16", 128, 12, 4, 4, [1, 4, 5, 99], (0, 32, -1)),
+    ("bf16", 64, 6, 6, 1, [1, 2, 17], (0, 16, -1)),
+    ("f16", 128, 20, 2, 64, [1, 63, 64, 65, 1000], (0, 256, -1)),
+    ("f16", 128, 4, 4, 2, [0, 7, 0, 40], (0, 16, -1)),
+    ("bf16", 128, 64, 8, 16, [1, 2, 3, 16, 17, 4097], (0, 512, -1)),
+    ("f16", 256, 16, 16, 16, [300, 1], (0, 128, -1)),
+    ("bf16", 128, 8, 8, 16, [0, 0, 0], (0, -1)),
+    ("f16", 128, 32, 32, 16, [1] * 300 + [2048], (0, -1)),
 ]
 
 
@@ -85,7 +87,7 @@ def test_split_matches_single_pass(dev):
     w = make_random_case(77, num_seqs=3, num_q_heads=32, num_kv_heads=8, head_dim=128,
                          block_size=32, seq_lens=[4096, 3000, 17], dtype="bf16")
     one = gpu_scenario(w, dev, partition_tokens=0)["out"]
-    for p in (512, 256, 1024, 16):
+    for p in (512, 256, 1024, 16, -1):
         split = gpu_scenario(w, dev, partition_tokens=p)["out"]
         assert torch.max(torch.abs(split - one)).item() <= 1e-5
 
@@ -94,7 +96,7 @@ def test_placement_permutation_bit_identical(dev):
     """Moving blocks to other physical ids leaves the kernel's output bit-identical."""
     w = make_random_case(31, num_seqs=5, num_q_heads=16, num_kv_heads=4, head_dim=128,
                          block_size=16, seq_lens=[1, 17, 200, 513, 999], dtype="f16")
-    base = gpu_scenario(w, dev, partition_tokens=128)["out"]
+    base = gpu_scenario(w, dev, partition_tokens=-1)["out"]
     perm = np.random.default_rng(3).permutation(w.num_blocks)
     k2 = np.empty_like(w.k_cache)
     v2 = np.empty_like(w.v_cache)
@@ -102,16 +104,17 @@ def test_placement_permutation_bit_identical(dev):
     v2[perm] = w.v_cache
     w.k_cache, w.v_cache = k2, v2
     w.block_tables = perm[w.block_tables].astype(np.int32)
-    moved = gpu_scenario(w, dev, partition_tokens=128)["out"]
+    moved = gpu_scenario(w, dev, partition_tokens=-1)["out"]
     assert torch.equal(base, moved)
 
 
 def test_repeat_is_deterministic(dev):
     w = make_random_case(32, num_seqs=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
                          block_size=16, seq_lens=[2000, 1500, 900, 3], dtype="bf16")
-    a = gpu_scenario(w, dev, partition_tokens=256)["out"]
-    b = gpu_scenario(w, dev, partition_tokens=256)["out"]
-    assert torch.equal(a, b)
+    for p in (256, -1):
+        a = gpu_scenario(w, dev, partition_tokens=p)["out"]
+        b = gpu_scenario(w, dev, partition_tokens=p)["out"]
+        assert torch.equal(a, b)
 
 
 # ---------------------------------------------------------------- full-size configs
@@ -138,11 +141,12 @@ def test_config3_gqa_full(dev):
     assert_close(res["out"], ref["out"], heads, what="config 3")
 
 
+@pytest.mark.parametrize("partition", [512, -1])
 @pytest.mark.parametrize("b", [8, 16, 32])
-def test_config4_long_split_full(dev, b):
+def test_config4_long_split_full(dev, b, partition):
     w = make_config(4, block_size=b)
-    res, ref, heads = _full_config(dev, w, n_heads=24, partition=512)
-    assert_close(res["out"], ref["out"], heads, what=f"config 4 b={b}")
+    res, ref, heads = _full_config(dev, w, n_heads=24, partition=partition)
+    assert_close(res["out"], ref["out"], heads, what=f"config 4 b={b} partition {partition}")
 
 
 def test_config5_prefix_cow_full(dev):
@@ -187,10 +191,10 @@ def test_bad_block_id_is_flagged_not_faulted(dev):
     tables[1, 1] = w.num_blocks + 5  # sequence 1's second block id is out of range
     k = to_dev(w.k_cache, dev, w.dtype)
     v = to_dev(w.v_cache, dev, w.dtype)
-    for partition in (0, 16):
-        out = pa.decode(to_dev(w.q, dev, w.dtype), k, v, to_dev(tables, dev),
-                        to_dev(w.seq_lens, dev), w.scale, max_seq_len=40, out_dtype=torch.float32,
-                        partition_tokens=partition)
+    for partition in (0, 16, -1):
+        out = torch.full((3, 8, 64), float("nan"), dtype=torch.float32, device=dev)
+        pa.decode(to_dev(w.q, dev, w.dtype), k, v, to_dev(tables, dev), to_dev(w.seq_lens, dev),
+                  w.scale, max_seq_len=40, out=out, partition_tokens=partition)
         assert pa.get_device_error(dev) & pa.DEVERR_BLOCK_ID
         assert torch.all(torch.isfinite(out))
         assert_close(out[0:1], want[0:1])

@@ -35,13 +35,14 @@ def _upload(w, dev):
                 lens=to_dev(w.seq_lens, dev))
 
 
-def test_static_workspace_matches_caller_workspace(dev):
+@pytest.mark.parametrize("part", [512, -1])
+def test_static_workspace_matches_caller_workspace(dev, part):
     import paged_kv_cache_114_gb300 as pa
     w = make_random_case(2024, num_seqs=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
                          block_size=32, seq_lens=[8192, 5000, 300, 1], dtype="bf16")
     t = _upload(w, dev)
-    part = 512
-    need = pa.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim, w.max_seq_len, part)
+    need = pa.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     w.max_seq_len, part)
     assert 0 < need <= pa.STATIC_WORKSPACE_BYTES
     rng = np.random.default_rng(5)
     for call in range(2):
@@ -50,9 +51,10 @@ def test_static_workspace_matches_caller_workspace(dev):
             rng.standard_normal(tuple(t["q"].shape)).astype(np.float32)).to(dev).to(t["q"].dtype)
         want = pa.decode(q, t["k"], t["v"], t["tables"], t["lens"], w.scale,
                          max_seq_len=w.max_seq_len, out_dtype=torch.float32, partition_tokens=part)
-        got = pa.decode_static_workspace(q, t["k"], t["v"], t["tables"], t["lens"], w.scale,
-                                         max_seq_len=w.max_seq_len, partition_tokens=part,
-                                         out_dtype=torch.float32)
+        # NaN-filled so a row left unwritten cannot pass on stale memory
+        got = torch.full(tuple(q.shape), float("nan"), dtype=torch.float32, device=dev)
+        pa.decode_static_workspace(q, t["k"], t["v"], t["tables"], t["lens"], w.scale,
+                                   max_seq_len=w.max_seq_len, partition_tokens=part, out=got)
         assert pa.get_device_error(dev) == 0
         assert torch.all(torch.isfinite(got))
         assert torch.max(torch.abs(got - want)).item() <= ATOL
@@ -65,7 +67,8 @@ def test_static_workspace_refuses_oversize(dev):
     t = _upload(w, dev)
     # claimed lengths this long would need more partials than the array holds
     max_len = 1 << 20
-    need = pa.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim, max_len, 16)
+    need = pa.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     max_len, 16)
     assert need > pa.STATIC_WORKSPACE_BYTES
     with pytest.raises(pa.PagedKVError, match="workspace"):
         pa.decode_static_workspace(t["q"], t["k"], t["v"], t["tables"], t["lens"], w.scale,
