@@ -173,7 +173,7 @@ class ClockSampler:
 
 
 class Run:
-    """One workload resident on the device, with the step's inputs."""
+    """One workload resident on the device, driven through pa.DecodeStep."""
 
     def __init__(self, w, dev, partition):
         import torch
@@ -182,53 +182,41 @@ class Run:
         self.w, self.dev, self.pa, self.torch = w, dev, pa, torch
         self.k = to_dev(w.k_cache, dev, w.dtype)
         self.v = to_dev(w.v_cache, dev, w.dtype)
-        self.tables = to_dev(w.block_tables, dev)
-        self.lens = to_dev(w.seq_lens, dev)
-        self.q = to_dev(w.q, dev, w.dtype)
         idx = step_tokens(w)
         # scenario rows written before timing (config 5's suffixes, after its copies)
         setup = np.setdiff1d(np.arange(len(w.positions)), idx)
+        tables = to_dev(w.block_tables, dev)
         if len(w.copy_pairs):
             pa.copy_blocks([self.k], [self.v], to_dev(w.copy_pairs, dev))
         if len(setup):
-            sl = pa.slot_mapping(self.tables, to_dev(w.seq_idx[setup], dev),
+            sl = pa.slot_mapping(tables, to_dev(w.seq_idx[setup], dev),
                                  to_dev(w.positions[setup], dev), w.block_size, w.num_blocks)
             pa.write_kv(to_dev(w.key[setup], dev, w.dtype), to_dev(w.value[setup], dev, w.dtype),
                         sl, self.k, self.v)
-        self.host = {
-            "seq_idx": w.seq_idx[idx], "positions": w.positions[idx],
-            "key": w.key[idx], "value": w.value[idx],
-        }
-        self.seq_idx = to_dev(self.host["seq_idx"], dev)
-        self.positions = to_dev(self.host["positions"], dev)
-        self.key = to_dev(self.host["key"], dev, w.dtype)
-        self.value = to_dev(self.host["value"], dev, w.dtype)
         self.n_tokens = len(idx)
-        self.slots = torch.empty(self.n_tokens, dtype=torch.int64, device=dev)
-        self.out = torch.empty(self.q.shape, dtype=torch.float32, device=dev)
         self.partition = partition
-        self.ws = pa.new_workspace(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                   w.max_seq_len, partition, dev)
+        self.step_obj = pa.DecodeStep(
+            self.k, self.v, num_seqs=w.num_seqs, num_q_heads=w.num_q_heads,
+            num_tokens=self.n_tokens, max_blocks_per_seq=w.max_blocks_per_seq,
+            max_seq_len=w.max_seq_len, scale=w.scale, out_dtype=torch.float32,
+            partition_tokens=partition)
+        host, _ = self.step_obj.host_buffers()
+        fill = {"q": w.q, "key": w.key[idx], "value": w.value[idx], "seq_idx": w.seq_idx[idx],
+                "positions": w.positions[idx], "block_tables": w.block_tables,
+                "seq_lens": w.seq_lens}
+        for name, arr in fill.items():
+            t = host[name]
+            src = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16 if arr.dtype == np.uint16
+                                                                  else arr.dtype))
+            t.view(src.dtype).copy_(src.view(t.shape))
+        with torch.cuda.stream(self.step_obj.stream):
+            self.step_obj.staging.copy_(self.step_obj._host_staging)
         # slot mapping + KV write + decode (+ the reduce of fixed split-K partitions)
-        self.launches_per_step = 3 + (1 if (self.ws is not None and partition > 0) else 0)
-
-    def decode(self, q=None, lens=None, tables=None, out=None):
-        return self.pa.decode(self.q if q is None else q, self.k, self.v,
-                              self.tables if tables is None else tables,
-                              self.lens if lens is None else lens, self.w.scale,
-                              max_seq_len=self.w.max_seq_len, out=self.out if out is None else out,
-                              partition_tokens=self.partition, workspace=self.ws)
+        ws = self.step_obj.workspace
+        self.launches_per_step = 3 + (1 if (ws is not None and partition > 0) else 0)
 
     def step(self, ev=None):
-        pa = self.pa
-        pa.slot_mapping(self.tables, self.seq_idx, self.positions, self.w.block_size,
-                        self.w.num_blocks, out=self.slots)
-        pa.write_kv(self.key, self.value, self.slots, self.k, self.v)
-        if ev is not None:
-            ev[0].record()
-        self.decode()
-        if ev is not None:
-            ev[1].record()
+        self.step_obj.run(decode_events=ev)
 
 
 def to_dev(a, dev, dtype=None):
@@ -296,7 +284,7 @@ def run_gpu(args):
     if pa.get_device_error(dev):
         raise RuntimeError("device error during warm-up")
 
-    stream = torch.cuda.current_stream(dev)
+    stream = run.step_obj.stream  # every timed launch goes to the step's stream
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -371,47 +359,31 @@ def run_gpu(args):
 
 
 def run_e2e(run, K, W, world, dev, step_bytes):
-    """Same step through the public API with pinned host buffers; every step
-    copies its inputs to the device and reads the output back."""
+    """The same step through pa.DecodeStep.run_from_host: every step copies its
+    pinned host staging buffer (all inputs) to the device, runs, and reads the
+    output back before the next step starts. The step is replayed from a CUDA
+    graph captured once (copies and library calls), as a serving loop would."""
     import torch
-    w = run.w
-    pin = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if dt else
-                                              np.ascontiguousarray(a)).pin_memory()
-    h = {
-        "q": pin(w.q, 1), "key": pin(run.host["key"], 1), "value": pin(run.host["value"], 1),
-        "seq_idx": pin(run.host["seq_idx"]), "positions": pin(run.host["positions"]),
-        "tables": pin(w.block_tables), "lens": pin(w.seq_lens),
-    }
-    out_host = torch.empty(run.out.shape, dtype=torch.float32).pin_memory()
-    tdt = run.q.dtype
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    st = run.step_obj
+    host, out_host = st.host_buffers()
+    st.capture_graph()
+    h2d = st.nbytes
     d2h = out_host.numel() * out_host.element_size()
-    pa = run.pa
-
-    def one():
-        d = {k: t.to(dev, non_blocking=True) for k, t in h.items()}
-        q = d["q"].view(tdt)
-        key, value = d["key"].view(tdt), d["value"].view(tdt)
-        pa.slot_mapping(d["tables"], d["seq_idx"], d["positions"], w.block_size, w.num_blocks,
-                        out=run.slots)
-        pa.write_kv(key, value, run.slots, run.k, run.v)
-        run.decode(q=q, lens=d["lens"], tables=d["tables"])
-        out_host.copy_(run.out, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
-
     for _ in range(W):
-        one()
+        st.run_from_host()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(K):
-        one()
+        st.run_from_host()
     t1 = time.perf_counter()
     barrier(world)
     secs = reduce_max(t1 - t0, world, dev)
     return {"value": round(step_bytes * K * world / secs / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(secs / K * 1e3, 5)}
+            "ms_per_step": round(secs / K * 1e3, 5),
+            "path": "pa.DecodeStep.run_from_host replaying its captured graph: one pinned "
+                    "H2D copy, the 3 library calls, one D2H copy; stream synchronize per step"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

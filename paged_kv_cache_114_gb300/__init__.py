@@ -6,12 +6,14 @@ C ABI, declared in ``include/pa.h``); this package is its Python binding.
 * :func:`slot_mapping` - pool slot of each new token;
 * :func:`write_kv` - slot-mapped write of new K/V rows;
 * :func:`copy_blocks` - whole-block copies for copy-on-write;
-* :func:`decode` - decode attention through block tables (single pass or
-  split-K with a reduce), GQA heads packed per KV head.
+* :func:`decode` - decode attention through block tables (single pass,
+  split-K with a reduce, or a balanced split), GQA heads packed per KV head;
+* :class:`DecodeStep` - the three calls bound to fixed buffers for loops.
 """
 from ._lib import (DEVERR_BLOCK_ID, DEVERR_POSITION, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT,
                    EXPORTED, LIB_PATH, PagedKVError, lib)
 from ._lib import PA_PARTITION_BALANCED, STATIC_WORKSPACE_BYTES
+from .step import DecodeStep
 from .ops import (check_copy_pairs, copy_blocks, decode, decode_static_workspace,
                   decode_workspace_bytes, default_partition, get_device_error, make_cache,
                   new_workspace, slot_mapping, write_kv)
@@ -21,5 +23,5 @@ __all__ = [
     "EXPORTED", "LIB_PATH", "PagedKVError", "lib", "check_copy_pairs", "copy_blocks", "decode",
     "decode_workspace_bytes", "default_partition", "get_device_error", "make_cache",
     "slot_mapping", "write_kv", "decode_static_workspace", "STATIC_WORKSPACE_BYTES",
-    "PA_PARTITION_BALANCED", "new_workspace",
+    "PA_PARTITION_BALANCED", "new_workspace", "DecodeStep",
 ]
