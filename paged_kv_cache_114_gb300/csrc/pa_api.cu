@@ -98,22 +98,75 @@ int64_t decode_parts(int32_t max_seq_len, int32_t partition_tokens) {
 }
 
 // Balanced-mode workspace: arrival counters [N][H_kv] (cleared by every call),
-// then per warp two partial slots of (m, l) and o for the g heads of a group.
+// then kBalancedSlotsPerSm * SMs partial slots of (m, l) and o for the g query
+// heads of a KV head. Both balanced kernels stay within that many slots.
 struct BalancedLayout {
   size_t ml_offset, o_offset, total;
-  int64_t warps;
 };
 
 BalancedLayout balanced_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                int32_t head_dim, int sms) {
   BalancedLayout l{};
   const int64_t g = num_q_heads / num_kv_heads;
-  l.warps = static_cast<int64_t>(pa::balanced_ctas_per_sm(head_dim)) * sms * pa::kDecodeWarps;
+  const int64_t slots = static_cast<int64_t>(pa::kBalancedSlotsPerSm) * sms;
   const size_t counters = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(unsigned int);
   l.ml_offset = (counters + 255) / 256 * 256;
-  l.o_offset = l.ml_offset + static_cast<size_t>(2 * l.warps * g * 2) * sizeof(float);
-  l.total = l.o_offset + static_cast<size_t>(2 * l.warps * g * head_dim) * sizeof(float);
+  l.o_offset = l.ml_offset + static_cast<size_t>(slots * g * 2) * sizeof(float);
+  l.total = l.o_offset + static_cast<size_t>(slots * g * head_dim) * sizeof(float);
   return l;
+}
+
+// Which balanced kernel runs, on how many CTAs. The head-grouped kernel needs
+// blocks of at least 8 tokens (no padding rows in its boxes) and a divisor HG
+// HG of H_kv, 8 or 4, whose 64 KB-or-smaller stages fit three to a CTA; it runs
+// 8 / HG CTAs per SM (8 consumer warps). Otherwise each warp issues its own
+// per-head boxes (2 or 1 CTAs of 4 warps per SM).
+struct BalancedPlan {
+  int kernel;
+  int head_group;
+  unsigned ctas;
+};
+
+BalancedPlan balanced_plan(int32_t num_kv_heads, int32_t group, int32_t head_dim, int32_t block_size,
+                          int sms) {
+  BalancedPlan p{pa::kPerWarpRanges, 1,
+                 static_cast<unsigned>(pa::balanced_ctas_per_sm(head_dim) * sms)};
+  if (block_size < 8) return p;
+  // mirrors max_head_group(): 4 when a consumer warp needs more registers
+  const int limit = (head_dim > 128 || group > 8) ? 4 : 8;
+  int hg = 0;
+  for (int c = limit; c >= 4; c /= 2) {  // the grouped kernel is built for HG = 8 and 4
+    if (num_kv_heads % c == 0 && c * head_dim <= 1024) {
+      hg = c;
+      break;
+    }
+  }
+  if (hg == 0) return p;
+  p.kernel = pa::kGroupedRanges;
+  p.head_group = hg;
+  p.ctas = static_cast<unsigned>((8 / hg) * sms);
+  return p;
+}
+
+// Tensor map for the grouped kernel: the cache viewed as (D, token, head,
+// block) - token before head, strides permuted - with box 64 x tok_per_op x
+// HG x 1, so one box lands head-major in shared memory.
+bool encode_grouped_map(CUtensorMap* m, const void* base, const pa_cache& c, int tok_per_op,
+                        int hg) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t e = 2;
+  const cuuint64_t D = c.head_dim, H = c.num_kv_heads, B = c.block_size;
+  cuuint64_t dims[4] = {D, B, H, static_cast<cuuint64_t>(c.num_blocks)};
+  cuuint64_t strides[3] = {D * H * e, D * e, D * H * B * e};
+  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(tok_per_op), static_cast<cuuint32_t>(hg), 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapDataType dt =
+      c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -344,21 +397,33 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   a.err = di.err;
+  int kernel = pa::kPerPartition;
+  int head_group = 1;
   if (balanced) {
     const BalancedLayout lay = balanced_layout(num_seqs, num_q_heads, hkv, D, di.sms);
-    if (hkv > lay.warps) return PA_ERR_SHAPE;  // a range group needs one warp per KV head
+    const BalancedPlan plan = balanced_plan(hkv, g, D, b, di.sms);
+    // every range needs one warp per KV head (or one CTA per head group)
+    const int64_t units = plan.kernel == pa::kGroupedRanges
+                              ? static_cast<int64_t>(plan.ctas) / (hkv / plan.head_group)
+                              : static_cast<int64_t>(plan.ctas) * pa::kDecodeWarps / hkv;
+    if (units < 1) return PA_ERR_SHAPE;
     if (workspace == nullptr || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
     char* ws = static_cast<char*>(workspace);
     a.counters = reinterpret_cast<unsigned int*>(ws);
     a.part_ml = reinterpret_cast<float*>(ws + lay.ml_offset);
     a.part_o = reinterpret_cast<float*>(ws + lay.o_offset);
-    grid = dim3(static_cast<unsigned>(lay.warps / pa::kDecodeWarps), 1, 1);
+    head_group = plan.head_group;
+    kernel = plan.kernel;
+    grid = dim3(plan.ctas, 1, 1);
   }
 
   CUtensorMap tk, tv;
-  if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
-      !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
+  const bool grouped = kernel == pa::kGroupedRanges;
+  if (grouped ? (!encode_grouped_map(&tk, cache->k, *cache, a.tok_per_op, head_group) ||
+                 !encode_grouped_map(&tv, cache->v, *cache, a.tok_per_op, head_group))
+              : (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
+                 !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op)))
     return PA_ERR_CUDA;
 
   const int tiles = (g + 7) / 8;
@@ -366,17 +431,18 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   cudaError_t e;
   if (balanced) {
     // arrival counters start each call at zero, whatever the workspace held
+    static_assert(pa::kPerWarpRanges == 1, "kernel ids");
     e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(num_seqs) * hkv * sizeof(unsigned int), st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (cache->dtype == PA_F16) {
-    e = D == 64 ? pa::launch_decode_f16_64(tk, tv, a, tiles, grid, balanced, st)
-        : D == 128 ? pa::launch_decode_f16_128(tk, tv, a, tiles, grid, balanced, st)
-                   : pa::launch_decode_f16_256(tk, tv, a, tiles, grid, balanced, st);
+    e = D == 64 ? pa::launch_decode_f16_64(tk, tv, a, tiles, head_group, grid, kernel, st)
+        : D == 128 ? pa::launch_decode_f16_128(tk, tv, a, tiles, head_group, grid, kernel, st)
+                   : pa::launch_decode_f16_256(tk, tv, a, tiles, head_group, grid, kernel, st);
   } else {
-    e = D == 64 ? pa::launch_decode_bf16_64(tk, tv, a, tiles, grid, balanced, st)
-        : D == 128 ? pa::launch_decode_bf16_128(tk, tv, a, tiles, grid, balanced, st)
-                   : pa::launch_decode_bf16_256(tk, tv, a, tiles, grid, balanced, st);
+    e = D == 64 ? pa::launch_decode_bf16_64(tk, tv, a, tiles, head_group, grid, kernel, st)
+        : D == 128 ? pa::launch_decode_bf16_128(tk, tv, a, tiles, head_group, grid, kernel, st)
+                   : pa::launch_decode_bf16_256(tk, tv, a, tiles, head_group, grid, kernel, st);
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (!balanced && parts > 1) {

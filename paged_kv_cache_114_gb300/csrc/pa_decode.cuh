@@ -291,28 +291,56 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
   }
 }
 
-// Folds one loaded stage into the warp's softmax state. `stage` is the
-// stage's shared address and `stage_ptr` the same memory as a generic pointer.
-template <bool IS_BF16, int D, int NT, bool SPLIT_P>
-__device__ __forceinline__ void compute_stage(uint32_t stage, uint8_t* stage_ptr, uint32_t rowmask,
+// Where one KV head's rows of a loaded stage sit in shared memory. Views
+// give the shared addresses of K and V (column half 0), the bytes between
+// 64-element column halves, and the offset of row r. Rows sit in groups of
+// 8 or 16 contiguous 128-byte lines, each group starting on a 1024-byte
+// boundary, so the 128-byte swizzle of row r is r & 7. The layout constants
+// are compile-time so the compiler schedules ldmatrix/mma freely.
+
+// Per-warp stage: 16 consecutive lines, halves kStageRows * 128 bytes apart.
+struct WarpView {
+  uint32_t k, v;
+  static constexpr uint32_t half_stride = kStageRows * 128u;
+  __device__ __forceinline__ uint32_t row(int r) const { return static_cast<uint32_t>(r) * 128u; }
+};
+
+__device__ __forceinline__ WarpView warp_stage_view(uint32_t stage, int halves) {
+  return WarpView{stage, stage + halves * WarpView::half_stride};
+}
+
+// Head-grouped stage (box of 64 x TPO tokens x HG heads per column half):
+// per token group, HG heads of TPO lines each; this head's lines at head_off.
+template <int HG, int TPO>
+struct GroupView {
+  uint32_t k, v, head_off;
+  static constexpr uint32_t half_stride = HG * kStageRows * 128u;
+  static constexpr uint32_t op_stride = HG * TPO * 128u;
+  __device__ __forceinline__ uint32_t row(int r) const {
+    return static_cast<uint32_t>(r / TPO) * op_stride + head_off + static_cast<uint32_t>(r % TPO) * 128u;
+  }
+};
+
+// Folds one loaded stage into the warp's softmax state. `sv` (a WarpView or
+// GroupView) places the warp's rows; `smem_base` / `smem_base_ptr` are one shared address and its
+// generic pointer, used to zero masked V rows.
+template <bool IS_BF16, int D, int NT, bool SPLIT_P, class View>
+__device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
+                                              uint8_t* smem_base_ptr, uint32_t rowmask,
                                               const uint32_t (&qb)[NT][D / 16][2],
                                               Acc<D, NT>& acc, float scale_log2, int lane) {
   constexpr int TS = kStageRows;
   constexpr int KD = D / 16;
   constexpr int HALVES = D / 64;
-  constexpr int HB = kStageRows * 128;
   const int gid = lane >> 2;
-  const uint32_t kb = stage;
-  const uint32_t vb = stage + HALVES * HB;
 
   if (rowmask != (1u << TS) - 1u) {  // zero V rows that must not contribute
-    uint8_t* vp = stage_ptr + HALVES * HB;
     for (int idx = lane; idx < TS * HALVES * 8; idx += 32) {
       const int row = idx / (HALVES * 8);
       const int rem = idx - row * (HALVES * 8);
       if (!((rowmask >> row) & 1u)) {
-        *reinterpret_cast<uint4*>(vp + (rem >> 3) * HB + row * 128 + (rem & 7) * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t a = sv.v + (rem >> 3) * View::half_stride + sv.row(row) + (rem & 7) * 16;
+        *reinterpret_cast<uint4*>(smem_base_ptr + (a - smem_base)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     __syncwarp();
@@ -329,7 +357,7 @@ __device__ __forceinline__ void compute_stage(uint32_t stage, uint8_t* stage_ptr
     for (int kk = 0; kk < KD; ++kk) {
       const int chunk = ((kk & 3) << 1) + (i >> 1);
       uint32_t af[4];
-      ldsm_x4(kb + (kk >> 2) * HB + row * 128 + ((chunk ^ (row & 7)) << 4), af);
+      ldsm_x4(sv.k + (kk >> 2) * View::half_stride + sv.row(row) + ((chunk ^ (row & 7)) << 4), af);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816<IS_BF16>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
     }
@@ -392,7 +420,8 @@ __device__ __forceinline__ void compute_stage(uint32_t stage, uint8_t* stage_ptr
     for (int dm = 0; dm < KD; ++dm) {
       const int chunk = ((dm & 3) << 1) + (i & 1);
       uint32_t af[4];
-      ldsm_x4_trans(vb + (dm >> 2) * HB + row * 128 + ((chunk ^ (row & 7)) << 4), af);
+      ldsm_x4_trans(sv.v + (dm >> 2) * View::half_stride + sv.row(row) + ((chunk ^ (row & 7)) << 4),
+                    af);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         mma16816<IS_BF16>(acc.o[dm][nt], af, bh[nt][0], bh[nt][1]);
@@ -472,7 +501,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       aborted = true;
       break;
     }
-    compute_stage<IS_BF16, D, NT, SPLIT_P>(ring + slot * S::kStageBytes,
+    compute_stage<IS_BF16, D, NT, SPLIT_P>(warp_stage_view(ring + slot * S::kStageBytes, D / 64),
+                                           ring + slot * S::kStageBytes,
                                            ring_ptr + slot * S::kStageBytes, masks[slot], qb, acc,
                                            a.scale_log2, lane);
     fence_proxy_async_smem();  // our generic reads/writes of this slot precede the next TMA into it
@@ -608,6 +638,136 @@ __device__ __forceinline__ int64_t range_start(int64_t r, int64_t S, int64_t R) 
   return (r * S) / R;
 }
 
+// pre[s] = number of 16-token stages of sequences before s (lengths clamped),
+// pre[N] = all of them; built by the whole CTA (nwarps warps, nwarps <= 16).
+__device__ __forceinline__ void build_line_prefix(const DecodeArgs& a, int32_t* pre, int tt,
+                                                  int* warp_tot, int nwarps) {
+  const int N = a.num_seqs;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int per = (N + blockDim.x - 1) / blockDim.x;
+  const int beg = min(N, static_cast<int>(threadIdx.x) * per);
+  const int end = min(N, beg + per);
+  int local = 0;
+  for (int s = beg; s < end; ++s) local += (decode_seq_len(a, s, blockIdx.x == 0) + tt - 1) / tt;
+  int x = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  int run = x - local;
+  int total = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    if (w < warp) run += warp_tot[w];
+    total += warp_tot[w];
+  }
+  for (int s = beg; s < end; ++s) {
+    pre[s] = run;
+    run += (decode_seq_len(a, s, false) + tt - 1) / tt;
+  }
+  if (threadIdx.x == 0) pre[N] = total;
+  __syncthreads();
+}
+
+// A warp finished its share of piece (sequence s, KV head kvh), which covers
+// line stages [ps, pe); its own stages are [g0, g1), range `range` of `ranges`
+// cut from the line of stot stages. A piece the warp covered whole is
+// normalised and written; otherwise the warp leaves an (m, l, o) partial in
+// slot (range * H_kv + kvh) * 2 + (0: its first piece, 1: its last) and the
+// last contributor to arrive merges the piece.
+template <int D, int NT>
+__device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& acc, int s, int ps,
+                                             int pe, int g0, int g1, int64_t stot, int64_t ranges,
+                                             int64_t range, int kvh, int lane) {
+  constexpr int KD = D / 16;
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+  const int hkv = a.num_kv_heads;
+  acc.reduce_l();
+  const int64_t row0 = static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group;
+  if (ps >= g0 && pe <= g1) {
+    // whole piece: normalise and write
+#pragma unroll
+    for (int dm = 0; dm < KD; ++dm) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int col = nt * 8 + tig * 2 + (r & 1);
+          if (col < a.group) {
+            const int d = dm * 16 + gid + ((r >> 1) << 3);
+            const float l = acc.l[nt][r & 1];
+            store_out(a, (row0 + col) * D + d, l > 0.f ? acc.o[dm][nt][r] / l : 0.f);
+          }
+        }
+      }
+    }
+  } else {
+    // cut piece: leave a partial, the last contributor merges
+    const int64_t slot_id = (range * hkv + kvh) * 2 + (ps <= g0 ? 0 : 1);
+    float* po = a.part_o + slot_id * a.group * D;
+    float* pml = a.part_ml + slot_id * a.group * 2;
+#pragma unroll
+    for (int dm = 0; dm < KD; ++dm) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int col = nt * 8 + tig * 2 + (r & 1);
+          if (col < a.group) po[col * D + dm * 16 + gid + ((r >> 1) << 3)] = acc.o[dm][nt][r];
+        }
+      }
+    }
+    if (gid == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = nt * 8 + tig * 2 + c;
+          if (col < a.group) {
+            pml[col * 2] = acc.m[nt][c];
+            pml[col * 2 + 1] = acc.l[nt][c];
+          }
+        }
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    // Contributors: the warps of head kvh in the non-empty ranges ra..rb that
+    // meet [ps, pe). Ranges in between are empty only when there are more
+    // ranges than stages.
+    const int64_t ra = stage_owner(ps, stot, ranges);
+    const int64_t rb = stage_owner(pe - 1, stot, ranges);
+    const int span = static_cast<int>(rb - ra + 1);
+    auto nonempty = [&](int64_t r) {
+      return range_start(r, stot, ranges) < range_start(r + 1, stot, ranges);
+    };
+    int contrib = 0;
+    for (int c0 = 0; c0 < span; c0 += 32)
+      contrib += __popc(__ballot_sync(0xffffffffu, c0 + lane < span && nonempty(ra + c0 + lane)));
+    unsigned int old = 0;
+    if (lane == 0)
+      old = atomicInc(a.counters + static_cast<int64_t>(s) * hkv + kvh,
+                      static_cast<unsigned int>(contrib - 1));
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == static_cast<unsigned int>(contrib - 1)) {
+      __threadfence();
+      const bool ra_first = range_start(ra, stot, ranges) == ps;  // piece is ra's first
+      auto slot = [&](int c) -> int {
+        const int64_t r = ra + c;
+        if (!nonempty(r)) return -1;
+        return static_cast<int>((r * hkv + kvh) * 2 + ((c == 0 && !ra_first) ? 1 : 0));
+      };
+      merge_rows<D>(a, span, slot, a.group, a.part_ml, a.group * 2, 2, a.part_o,
+                    static_cast<int64_t>(a.group) * D, D, row0, lane);
+    }
+  }
+
+}
+
 template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_balanced_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -616,7 +776,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   constexpr int W = kDecodeWarps;
   constexpr int KD = D / 16;
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  __shared__ int warp_tot[W];
+  __shared__ int warp_tot[16];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -631,37 +791,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   int32_t* pre = reinterpret_cast<int32_t*>(sm + S::kPrefixOffset);  // [N + 1]
 
   // ---- line offset of every sequence: pre[s] = sum_{s'<s} ceil(L_s'/tt)
-  {
-    const int per = (N + W * 32 - 1) / (W * 32);
-    const int beg = min(N, static_cast<int>(threadIdx.x) * per);
-    const int end = min(N, beg + per);
-    int local = 0;
-    for (int s = beg; s < end; ++s) {
-      const int L = decode_seq_len(a, s, blockIdx.x == 0);
-      local += (L + tt - 1) / tt;
-    }
-    int x = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    if (lane == 31) warp_tot[warp] = x;
-    __syncthreads();
-    int run = x - local;
-    int total = 0;
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      if (w < warp) run += warp_tot[w];
-      total += warp_tot[w];
-    }
-    for (int s = beg; s < end; ++s) {
-      pre[s] = run;
-      run += (decode_seq_len(a, s, false) + tt - 1) / tt;
-    }
-    if (threadIdx.x == 0) pre[N] = total;
-    __syncthreads();
-  }
+  build_line_prefix(a, pre, tt, warp_tot, W);
 
   // ---- zero the output rows of empty sequences (CTA c takes s = c mod grid)
   for (int s = blockIdx.x; s < N; s += gridDim.x) {
@@ -723,9 +853,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
     }
     if (!aborted) {
-      compute_stage<IS_BF16, D, NT, SPLIT_P>(ring + slot * S::kStageBytes,
-                                             ring_ptr + slot * S::kStageBytes, masks[slot], qb,
-                                             acc, a.scale_log2, lane);
+      compute_stage<IS_BF16, D, NT, SPLIT_P>(
+          warp_stage_view(ring + slot * S::kStageBytes, D / 64), ring, ring_ptr, masks[slot], qb,
+          acc, a.scale_log2, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (it + NS < count) issue(it + NS);
@@ -739,87 +869,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     // ---- the warp is done with its share of piece (cc.s, kvh)
     if (aborted) acc.reset();  // contribute nothing, but still take part
-    acc.reduce_l();
-    const int ps = cc.ps;
-    const int pe = cc.ps + cc.n;
-    const int64_t row0 = static_cast<int64_t>(cc.s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group;
-    if (ps >= g0 && pe <= g1) {
-      // whole piece: normalise and write
-#pragma unroll
-      for (int dm = 0; dm < KD; ++dm) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int col = nt * 8 + tig * 2 + (r & 1);
-            if (col < a.group) {
-              const int d = dm * 16 + gid + ((r >> 1) << 3);
-              const float l = acc.l[nt][r & 1];
-              store_out(a, (row0 + col) * D + d, l > 0.f ? acc.o[dm][nt][r] / l : 0.f);
-            }
-          }
-        }
-      }
-    } else {
-      // cut piece: leave a partial, the last contributor merges
-      const int64_t slot_id = wid * 2 + (ps <= g0 ? 0 : 1);
-      float* po = a.part_o + slot_id * a.group * D;
-      float* pml = a.part_ml + slot_id * a.group * 2;
-#pragma unroll
-      for (int dm = 0; dm < KD; ++dm) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int col = nt * 8 + tig * 2 + (r & 1);
-            if (col < a.group) po[col * D + dm * 16 + gid + ((r >> 1) << 3)] = acc.o[dm][nt][r];
-          }
-        }
-      }
-      if (gid == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int col = nt * 8 + tig * 2 + c;
-            if (col < a.group) {
-              pml[col * 2] = acc.m[nt][c];
-              pml[col * 2 + 1] = acc.l[nt][c];
-            }
-          }
-        }
-      }
-      __threadfence();
-      __syncwarp();
-      // Contributors: the warps of head kvh in the non-empty ranges ra..rb that
-      // meet [ps, pe). Ranges in between are empty only when there are more
-      // ranges than stages.
-      const int64_t ra = stage_owner(ps, stot, ranges);
-      const int64_t rb = stage_owner(pe - 1, stot, ranges);
-      const int span = static_cast<int>(rb - ra + 1);
-      auto nonempty = [&](int64_t r) {
-        return range_start(r, stot, ranges) < range_start(r + 1, stot, ranges);
-      };
-      int contrib = 0;
-      for (int c0 = 0; c0 < span; c0 += 32)
-        contrib += __popc(__ballot_sync(0xffffffffu, c0 + lane < span && nonempty(ra + c0 + lane)));
-      unsigned int old = 0;
-      if (lane == 0)
-        old = atomicInc(a.counters + static_cast<int64_t>(cc.s) * hkv + kvh,
-                        static_cast<unsigned int>(contrib - 1));
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == static_cast<unsigned int>(contrib - 1)) {
-        __threadfence();
-        const bool ra_first = range_start(ra, stot, ranges) == ps;  // piece is ra's first
-        auto slot = [&](int c) -> int {
-          const int64_t r = ra + c;
-          if (!nonempty(r)) return -1;
-          return static_cast<int>((r * hkv + kvh) * 2 + ((c == 0 && !ra_first) ? 1 : 0));
-        };
-        merge_rows<D>(a, span, slot, a.group, a.part_ml, a.group * 2, 2, a.part_o,
-                      static_cast<int64_t>(a.group) * D, D, row0, lane);
-      }
-    }
+    finish_piece<D, NT>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, grp, kvh, lane);
 
     if (it + 1 < count) {
       cursor_next(a, pre, cc);

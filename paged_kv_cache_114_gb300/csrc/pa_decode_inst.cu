@@ -1,7 +1,7 @@
 // pa_decode_inst.cu - one decode instantiation per (dtype, head_dim).
 // Compiled once per combination with -DPA_INST_BF16={0,1} -DPA_INST_D={64,128,256}
 // so the variants build in parallel.
-#include "pa_decode.cuh"
+#include "pa_decode_grouped.cuh"
 
 #ifndef PA_INST_BF16
 #error "PA_INST_BF16 must be defined"
@@ -21,9 +21,15 @@
 namespace pa {
 
 cudaError_t PA_FN(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int group_tiles,
-                  dim3 grid, bool balanced, cudaStream_t st) {
-  return launch_decode_dispatch<PA_INST_BF16 != 0, PA_INST_D>(tk, tv, a, group_tiles, grid, balanced,
-                                                              st);
+                  int head_group, dim3 grid, int kernel, cudaStream_t st) {
+  constexpr bool kBf16 = PA_INST_BF16 != 0;
+  if (kernel == kGroupedRanges) {
+    if (group_tiles == 1) return launch_grouped_tiles<kBf16, PA_INST_D, 1>(tk, tv, a, head_group, grid, st);
+    if (group_tiles == 2) return launch_grouped_tiles<kBf16, PA_INST_D, 2>(tk, tv, a, head_group, grid, st);
+    return cudaErrorInvalidValue;
+  }
+  return launch_decode_dispatch<kBf16, PA_INST_D>(tk, tv, a, group_tiles, grid,
+                                                  kernel == kPerWarpRanges, st);
 }
 
 }  // namespace pa

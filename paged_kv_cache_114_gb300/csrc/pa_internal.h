@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/pa.h"
+#include "pa.h"  // from include/, on the compiler include path
 
 namespace pa {
 
@@ -38,32 +38,37 @@ constexpr int kStageRows = 16;
 // Warps per decode CTA; each owns a private ring of stages.
 constexpr int kDecodeWarps = 4;
 
+// Which decode kernel a launch runs.
+enum DecodeKernel { kPerPartition = 0, kPerWarpRanges = 1, kGroupedRanges = 2 };
+
 // Decode launchers, one per (dtype, head_dim) translation unit.
-// group_tiles = ceil(group / 8) in {1, 2}; balanced selects the persistent
-// equal-range kernel (grid = its CTA count) over the per-partition one.
+// group_tiles = ceil(group / 8) in {1, 2}; `kernel` is a DecodeKernel and
+// head_group the KV heads per CTA of the grouped kernel (8 or 4).
 cudaError_t launch_decode_f16_64(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                 int group_tiles, dim3 grid, bool balanced,
+                                 int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
 cudaError_t launch_decode_f16_128(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                  int group_tiles, dim3 grid, bool balanced,
+                                  int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
 cudaError_t launch_decode_f16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                  int group_tiles, dim3 grid, bool balanced,
+                                  int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
 cudaError_t launch_decode_bf16_64(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                  int group_tiles, dim3 grid, bool balanced,
+                                  int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
 cudaError_t launch_decode_bf16_128(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                   int group_tiles, dim3 grid, bool balanced,
+                                   int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
 cudaError_t launch_decode_bf16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                                   int group_tiles, dim3 grid, bool balanced,
+                                   int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
 
-// Balanced mode: resident CTAs per SM of the persistent grid, and the largest
-// batch whose per-sequence offsets fit the kernel's shared memory.
+// Balanced mode: resident CTAs per SM of the per-warp-range kernel, the
+// largest batch whose per-sequence offsets fit shared memory, and the partial
+// slots per SM either balanced kernel may use (the workspace is sized by it).
 constexpr int balanced_ctas_per_sm(int head_dim) { return head_dim > 128 ? 1 : 2; }
 constexpr int kMaxBalancedSeqs = 2048;
+constexpr int kBalancedSlotsPerSm = 16;
 
 // Merges split-K partials into out (pa_decode_reduce.cu).
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);
