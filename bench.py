@@ -35,8 +35,8 @@ METRIC = "paged decode attention achieved HBM GB/s (% of peak) and decode tokens
 SPEC_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
-KERNEL_SOURCES = ["pa_decode.cuh", "pa_ptx.cuh", "pa_decode_reduce.cu", "pa_decode_inst.cu",
-                  "pa_internal.h"]
+KERNEL_SOURCES = ["pa_decode.cuh", "pa_decode_grouped.cuh", "pa_ptx.cuh", "pa_decode_reduce.cu",
+                  "pa_decode_inst.cu", "pa_internal.h"]
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -319,9 +319,8 @@ def run_gpu(args):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy rate)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "frac_of_8tbs_spec": round(achieved / SPEC_HBM_GBS, 4),
-                "kernel": {0: "decode_kernel (single pass)",
-                           -1: "decode_balanced_kernel (equal stage ranges per warp)"}.get(
-                               partition, "decode_kernel + decode_reduce_kernel (split-K)"),
+                "kernel": pa.decode_kernel_name(w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                w.block_size, w.max_seq_len, partition),
                 "algorithmic_bytes_per_call": dec_bytes, "mean_call_us": round(dec_ms * 1e3, 2)}
 
     line = {

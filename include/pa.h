@@ -181,6 +181,16 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
 int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                                     int32_t block_size);
 
+/* Name of the kernel(s) pa_decode launches for this shape and partition_tokens:
+ * "decode_kernel" (single pass), "decode_kernel+decode_reduce_kernel" (fixed
+ * split with more than one partition), "decode_grouped_kernel" (balanced, one
+ * TMA box per stage for a group of KV heads) or "decode_balanced_kernel"
+ * (balanced, per-warp boxes). NULL when pa_decode would reject the shape.
+ * Host only: reads no device state. */
+const char* pa_decode_kernel_name(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t max_seq_len,
+                                  int32_t partition_tokens);
+
 /*
  * pa_decode_static_workspace - pa_decode for callers that cannot allocate
  * device memory. The pages have no counterpart; this call is a library

@@ -25,7 +25,7 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_POSITION, DEVERR_TIMEOUT = 
 EXPORTED = (
     "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_check_copy_pairs", "pa_decode",
     "pa_decode_workspace_bytes", "pa_decode_default_partition", "pa_get_device_error",
-    "pa_status_string", "pa_abi_version", "pa_decode_static_workspace",
+    "pa_status_string", "pa_abi_version", "pa_decode_static_workspace", "pa_decode_kernel_name",
 )
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
@@ -68,6 +68,7 @@ def _declare(lib):
                                                       ctypes.c_float, vp, ctypes.c_int, i32, vp]),
         "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "pa_decode_default_partition": (i32, [i32, i32, i32, i32]),
+        "pa_decode_kernel_name": (ctypes.c_char_p, [i32, i32, i32, i32, i32, i32]),
         "pa_get_device_error": (ctypes.c_int, [ctypes.POINTER(i32), vp]),
         "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pa_abi_version": (ctypes.c_int, []),

@@ -305,6 +305,24 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
   return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
 }
 
+const char* pa_decode_kernel_name(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t max_seq_len,
+                                  int32_t partition_tokens) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return nullptr;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return nullptr;
+  if (block_size <= 0 || !(block_size % pa::kStageRows == 0 || pa::kStageRows % block_size == 0))
+    return nullptr;
+  if (max_seq_len < 0 || partition_tokens < PA_PARTITION_BALANCED) return nullptr;
+  if (partition_tokens == PA_PARTITION_BALANCED) {
+    const BalancedPlan plan =
+        balanced_plan(num_kv_heads, num_q_heads / num_kv_heads, head_dim, block_size, 1);
+    return plan.kernel == pa::kGroupedRanges ? "decode_grouped_kernel" : "decode_balanced_kernel";
+  }
+  if (partition_tokens != 0 && partition_tokens % pa::kStageRows != 0) return nullptr;
+  return decode_parts(max_seq_len, partition_tokens) > 1 ? "decode_kernel+decode_reduce_kernel"
+                                                         : "decode_kernel";
+}
+
 int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                                     int32_t block_size) {
   if (num_seqs < 0 || num_kv_heads <= 0 || max_seq_len < 0 || block_size <= 0) return PA_ERR_ARG;

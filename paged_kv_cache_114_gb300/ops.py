@@ -122,6 +122,16 @@ def default_partition(num_seqs: int, num_kv_heads: int, max_seq_len: int, block_
     return v
 
 
+def decode_kernel_name(num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                       max_seq_len: int, partition_tokens: int) -> str:
+    """Which kernel(s) :func:`decode` launches for this shape and partition choice."""
+    name = _lib.lib().pa_decode_kernel_name(num_q_heads, num_kv_heads, head_dim, block_size,
+                                            max_seq_len, partition_tokens)
+    if name is None:
+        raise _lib.PagedKVError("pa_decode_kernel_name", -3)  # PA_ERR_SHAPE
+    return name.decode()
+
+
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            seq_lens: torch.Tensor, scale: float, *, max_seq_len: int,
            out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,

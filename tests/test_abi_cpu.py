@@ -59,6 +59,28 @@ def test_workspace_bytes(lib):
         assert lib.pa_decode_workspace_bytes(8, 32, 8, 128, 4096, -1) == 0
 
 
+def test_decode_kernel_name(lib):
+    def name(*a):
+        r = lib.pa_decode_kernel_name(*a)
+        return None if r is None else r.decode()
+    # balanced: grouped boxes need b >= 8 and 4 | H_kv; otherwise per-warp boxes
+    assert name(32, 32, 128, 16, 2048, -1) == "decode_grouped_kernel"
+    assert name(64, 8, 128, 16, 8192, -1) == "decode_grouped_kernel"
+    assert name(32, 8, 128, 8, 32768, -1) == "decode_grouped_kernel"
+    assert name(4, 4, 64, 4, 33, -1) == "decode_balanced_kernel"
+    assert name(6, 6, 128, 16, 100, -1) == "decode_balanced_kernel"
+    # fixed split: a reduce only when there is more than one partition
+    assert name(32, 8, 128, 32, 32768, 512) == "decode_kernel+decode_reduce_kernel"
+    assert name(32, 8, 128, 32, 512, 512) == "decode_kernel"
+    assert name(32, 32, 128, 16, 2048, 0) == "decode_kernel"
+    # shapes pa_decode rejects
+    assert name(32, 32, 96, 16, 2048, 0) is None
+    assert name(30, 8, 128, 16, 2048, 0) is None
+    assert name(32, 8, 128, 12, 2048, 0) is None
+    assert name(32, 8, 128, 16, 2048, 24) is None
+    assert name(32, 8, 128, 16, 2048, -2) is None
+
+
 def test_check_copy_pairs(lib):
     def chk(pairs, nb=16):
         a = np.ascontiguousarray(np.array(pairs, dtype=np.int64).reshape(-1, 2))
