@@ -780,8 +780,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int gid = lane >> 2;
-  const int tig = lane & 3;
   const int N = a.num_seqs;
   const int hkv = a.num_kv_heads;
   const int tt = a.ops_per_stage * a.tok_per_op;

@@ -17,7 +17,7 @@ struct DecodeArgs {
   void* out;                     // [N][Hq][D] of out_dtype
   float* part_o;                 // [N][Hq][max_parts][D]   (split-K only)
   float* part_ml;                // [N][Hq][max_parts][2]   (max in log2 units, normaliser)
-  unsigned int* counters;        // balanced mode: [N][H_kv] arrival counters, zero between calls
+  unsigned int* counters;        // balanced mode: [N][H_kv] arrival counters, cleared by each call
   const int32_t* block_tables;   // [N][max_blocks]
   const int32_t* seq_lens;       // [N]
   int* err;                      // device error word
