@@ -4,8 +4,9 @@ Only the tests, the smoke check and the benchmark's CPU baseline / reference
 arm may import this package. The library never imports it.
 """
 from .paged_attention import (attention, bits_to_f64, combine_partitions, copy_blocks, decode,
-                              gather_kv, online_softmax_blocks, partition_state, slot_mapping,
-                              write_kv)
+                              gather_kv, online_softmax_blocks, partition_state, prefill,
+                              slot_mapping, write_kv)
 
 __all__ = ["attention", "bits_to_f64", "combine_partitions", "copy_blocks", "decode",
-           "gather_kv", "online_softmax_blocks", "partition_state", "slot_mapping", "write_kv"]
+           "gather_kv", "online_softmax_blocks", "partition_state", "prefill", "slot_mapping",
+           "write_kv"]

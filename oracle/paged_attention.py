@@ -22,6 +22,14 @@ Each function is the plain definition of one step, written from the pages:
   ailinkdeeptech.com §3 standard attention softmax(QK^T/sqrt(d_k))V). Query
   head h reads KV head h // g with g = H_q / H_kv (repeat_interleave grouping,
   ailinkdeeptech.com Step 2 and pofe.ai §Minimal implementation).
+* multi-token (chunked prefill / speculative verify) attention: the i-th of a
+  sequence's n new queries sits at position L - n + i, its K/V and those of
+  every earlier position already in the cache (pofe.ai §How it works: prefill
+  writes into the blocks, then attention reads them), and attends to tokens
+  0..L - n + i only: the causal mask describes the allowed attention edges,
+  the block table only where the rows are stored (neelmishra.github.io §The
+  kernel must understand the mapping). Same gather and textbook softmax as
+  decode, which is the case n = 1.
 * the blockwise online-softmax recurrence and the partition-combine rule of
   ailinkdeeptech.com §3 (running max m, normaliser l, unnormalised o), used to
   pin the split-K reduction.
@@ -160,6 +168,49 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
         V = bits_to_f64(gather_kv(v_cache, block_tables[s], L, kvh), dtype)
         Q = bits_to_f64(q[s, heads], dtype)
         out[s, heads] = attention(Q, K, V, scale)
+    return out
+
+
+def prefill(q: np.ndarray, q_start: Sequence[int], k_cache: np.ndarray, v_cache: np.ndarray,
+            block_tables: np.ndarray, seq_lens: Sequence[int], scale: float, dtype: str,
+            rows: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+    """Causal multi-token attention over the paged cache.
+
+    ``q`` is ``[T, H_q, D]``; sequence s owns query rows ``q_start[s] ..
+    q_start[s + 1]``. With n of them and L = seq_lens[s], query i sits at
+    position L - n + i and attends to the tokens at positions 0 .. L - n + i,
+    read through the block table. Returns fp64 ``[T, H_q, D]``; with ``rows``
+    (a list of (query row, query head)) only those are computed and the rest
+    are NaN.
+    """
+    t_all, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    g = hq // hkv
+    out = np.full((t_all, hq, d), np.nan)
+    owner = {}
+    for s in range(len(seq_lens)):
+        for t in range(int(q_start[s]), int(q_start[s + 1])):
+            owner[t] = s
+    if rows is None:
+        want = {(t, kvh): list(range(kvh * g, (kvh + 1) * g)) for t in range(t_all) for kvh in range(hkv)}
+    else:
+        want = {}
+        for t, h in rows:
+            want.setdefault((int(t), int(h) // g), []).append(int(h))
+    cache = {}
+    for (t, kvh), heads in sorted(want.items(), key=lambda kv: (owner[kv[0][0]], kv[0][1], kv[0][0])):
+        s = owner[t]
+        L = int(seq_lens[s])
+        n = int(q_start[s + 1]) - int(q_start[s])
+        if n > L:
+            raise ValueError(f"sequence {s}: {n} queries but only {L} tokens")
+        pos = L - n + (t - int(q_start[s]))
+        if (s, kvh) not in cache:
+            cache = {(s, kvh): (bits_to_f64(gather_kv(k_cache, block_tables[s], L, kvh), dtype),
+                                bits_to_f64(gather_kv(v_cache, block_tables[s], L, kvh), dtype))}
+        K, V = cache[(s, kvh)]
+        Q = bits_to_f64(q[t, heads], dtype)
+        out[t, heads] = attention(Q, K[:pos + 1], V[:pos + 1], scale)
     return out
 
 

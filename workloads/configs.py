@@ -106,6 +106,9 @@ class Workload:
     partition_tokens: int = 0
     shared_blocks: List[int] = field(default_factory=list)
     meta: Dict[str, object] = field(default_factory=dict)
+    # Multi-token cases: sequence s owns query rows q_start[s] .. q_start[s+1]
+    # of q [T, H_q, D] (None: decode, one query row per sequence).
+    q_start: Optional[np.ndarray] = None
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -231,6 +234,53 @@ def make_random_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads
         seq_idx=np.array(writers, dtype=np.int32),
         positions=np.array([lens[i] - 1 for i in writers], dtype=np.int32),
         copy_pairs=np.zeros((0, 2), dtype=np.int64), partition_tokens=partition_tokens)
+
+
+def make_prefill_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                      head_dim: int, block_size: int, seq_lens: Sequence[int],
+                      q_lens: Sequence[int], dtype: str = "f16", pool_factor: float = 1.25,
+                      scale: Optional[float] = None, name: str = "prefill") -> Workload:
+    """A multi-token batch: sequence s ends with q_lens[s] new tokens.
+
+    The pool holds the first L - n tokens of each sequence (n = q_lens[s]); the
+    scenario writes the K/V of the n new tokens (positions L - n .. L - 1) and
+    then runs causal attention for their n queries. Query rows are laid out
+    sequence by sequence in ``q [sum(q_lens), H_q, D]``.
+    """
+    rng = np.random.default_rng(seed)
+    b = block_size
+    lens = [int(x) for x in seq_lens]
+    qn = [int(x) for x in q_lens]
+    assert len(lens) == num_seqs and len(qn) == num_seqs
+    assert all(0 <= n <= L for n, L in zip(qn, lens))
+    need = sum(-(-L // b) for L in lens)
+    nb = max(1, int(np.ceil(pool_factor * need)))
+    pool = BlockPool(nb, b, free_order=rng.permutation(nb))
+    seqs = []
+    for L in lens:
+        s = SeqTable(pool)
+        s.admit(L)
+        seqs.append(s)
+    tables = [s.table for s in seqs]
+    k, v, nan = _new_pool(nb, b, num_kv_heads, head_dim, dtype)
+    fk, fv = _Filler(rng, dtype), _Filler(rng, dtype)
+    _fill_sequences(k, v, tables, lens, fk, fv, nan)
+    t_all = sum(qn)
+    q = _normal_bits(rng, (t_all, num_q_heads, head_dim), dtype)
+    key = _normal_bits(rng, (t_all, num_kv_heads, head_dim), dtype)
+    value = _normal_bits(rng, (t_all, num_kv_heads, head_dim), dtype)
+    seq_idx = np.concatenate([np.full(n, i, dtype=np.int32) for i, n in enumerate(qn)] +
+                             [np.zeros(0, dtype=np.int32)])
+    positions = np.concatenate([np.arange(L - n, L, dtype=np.int32) for n, L in zip(qn, lens)] +
+                               [np.zeros(0, dtype=np.int32)])
+    q_start = np.concatenate([[0], np.cumsum(qn)]).astype(np.int32)
+    return Workload(
+        name=name, dtype=dtype, num_seqs=num_seqs, num_q_heads=num_q_heads,
+        num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=b, num_blocks=nb,
+        scale=float(scale if scale is not None else 1.0 / np.sqrt(head_dim)),
+        q=q, k_cache=k, v_cache=v, block_tables=_pad_tables(tables, 0),
+        seq_lens=np.array(lens, dtype=np.int32), key=key, value=value, seq_idx=seq_idx,
+        positions=positions, copy_pairs=np.zeros((0, 2), dtype=np.int64), q_start=q_start)
 
 
 # ----------------------------------------------------------------------------
