@@ -166,6 +166,42 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
               int32_t max_seq_len, float scale, void* out, pa_dtype out_dtype,
               int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pa_prefill - causal attention for several new tokens per sequence over the
+ * paged cache: a prefill chunk, the draft tokens of speculative decoding, or
+ * the re-run prompt of a preempted sequence ("PagedAttention: paging the KV
+ * cache", How it works: prefill writes into the blocks; When memory runs out:
+ * recomputation re-runs prompt and generated tokens as one prefill).
+ * Sequence s owns query rows q_start[s] .. q_start[s+1] - 1 (n_s of them). With
+ * L_s = seq_lens[s], its query i sits at position L_s - n_s + i and attends to
+ * the tokens at positions 0 .. L_s - n_s + i: the mask gives the attention
+ * edges, the block table only where each row is stored ("PagedAttention:
+ * Manage the Cache Without Moving the Sequence", The kernel must understand
+ * the mapping). For query row t of sequence s and query head h (KV head
+ * h / g):
+ *   out[t][h] = sum_{u <= p} softmax_u(scale * q[t][h] . K_s[u]) V_s[u],
+ *   p = L_s - n_s + (t - q_start[s]).
+ * The K/V of all L_s positions, the new ones included, must already be in
+ * the cache (pa_slot_mapping + pa_write_kv first). Decode is the case n_s = 1.
+ *   q            device [q_start[num_seqs]][num_q_heads][head_dim], cache dtype
+ *   q_start      device int32 [num_seqs + 1], non-decreasing, q_start[0] = 0
+ *   max_q_len    host upper bound of every n_s (sizes the launch)
+ *   cache        host pointer to one pa_cache; head_dim 64, 128 or 256;
+ *                block_size >= 8 and a divisor or a multiple of 64
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens     device int32 [num_seqs]
+ *   out          device [q_start[num_seqs]][num_q_heads][head_dim] of out_dtype
+ * No workspace. num_seqs <= 65535 and num_kv_heads <= 65535.
+ * Errors (device): n_s > L_s, L_s above the table's capacity or n_s above
+ * max_q_len set PA_DEVERR_SEQ_LEN and the sequence's rows (or those past
+ * max_q_len) are not written; a table entry out of range sets
+ * PA_DEVERR_BLOCK_ID and its tokens are left out.
+ */
+int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t max_q_len,
+               int32_t num_q_heads, const pa_cache* cache, const int32_t* block_tables,
+               int32_t max_blocks_per_seq, const int32_t* seq_lens, float scale, void* out,
+               pa_dtype out_dtype, void* stream);
+
 /* Workspace bytes pa_decode needs for these sizes (0 when one partition covers
  * max_seq_len or partition_tokens == 0). The balanced mode's size depends on
  * the current device's SM count. */

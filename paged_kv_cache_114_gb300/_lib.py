@@ -26,6 +26,7 @@ EXPORTED = (
     "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_check_copy_pairs", "pa_decode",
     "pa_decode_workspace_bytes", "pa_decode_default_partition", "pa_get_device_error",
     "pa_status_string", "pa_abi_version", "pa_decode_static_workspace", "pa_decode_kernel_name",
+    "pa_prefill",
 )
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
@@ -64,6 +65,8 @@ def _declare(lib):
         "pa_check_copy_pairs": (ctypes.c_int, [vp, i64, i64]),
         "pa_decode": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32, ctypes.c_float, vp,
                                      ctypes.c_int, i32, vp, sz, vp]),
+        "pa_prefill": (ctypes.c_int, [vp, i32, vp, i32, i32, cache_p, vp, i32, vp, ctypes.c_float,
+                                      vp, ctypes.c_int, vp]),
         "pa_decode_static_workspace": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32,
                                                       ctypes.c_float, vp, ctypes.c_int, i32, vp]),
         "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),

@@ -347,6 +347,61 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
   return pt >= max_seq_len ? 0 : static_cast<int32_t>(pt);
 }
 
+int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t max_q_len,
+               int32_t num_q_heads, const pa_cache* cache, const int32_t* block_tables,
+               int32_t max_blocks_per_seq, const int32_t* seq_lens, float scale, void* out,
+               pa_dtype out_dtype, void* stream) {
+  int rc = check_cache(cache);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_ARG;
+  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (!q || !q_start || !block_tables || !seq_lens || !out) return PA_ERR_NULL;
+  if (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32) return PA_ERR_DTYPE;
+  const int D = cache->head_dim;
+  const int b = cache->block_size;
+  const int hkv = cache->num_kv_heads;
+  if (D != 64 && D != 128 && D != 256) return PA_ERR_SHAPE;
+  if (b < 8 || !(64 % b == 0 || b % 64 == 0)) return PA_ERR_SHAPE;
+  if (num_q_heads % hkv != 0) return PA_ERR_SHAPE;
+  if (num_seqs > 65535 || hkv > 65535) return PA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return PA_ERR_ARG;
+  if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  const int g = num_q_heads / hkv;
+  const int64_t tiles = (static_cast<int64_t>(max_q_len) * g + 63) / 64;
+  if (tiles > 0x7fffffffLL) return PA_ERR_SHAPE;
+
+  pa::PrefillArgs a{};
+  a.q = q;
+  a.out = out;
+  a.q_start = q_start;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.num_blocks = cache->num_blocks;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = hkv;
+  a.group = g;
+  a.block_size = b;
+  a.max_blocks = max_blocks_per_seq;
+  a.tok_per_op = b < 64 ? b : 64;
+  a.ops_per_stage = 64 / a.tok_per_op;
+  a.out_dtype = out_dtype;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  a.err = di.err;
+  CUtensorMap tk, tv;
+  if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
+      !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
+    return PA_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
+                  static_cast<unsigned>(num_seqs));
+  const cudaError_t e = pa::launch_prefill(tk, tv, a, D, cache->dtype == PA_BF16, grid,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cache* cache,
               const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
               int32_t max_seq_len, float scale, void* out, pa_dtype out_dtype,

@@ -70,6 +70,26 @@ constexpr int balanced_ctas_per_sm(int head_dim) { return head_dim > 128 ? 1 : 2
 constexpr int kMaxBalancedSeqs = 2048;
 constexpr int kBalancedSlotsPerSm = 16;
 
+// Multi-token causal attention (pa_prefill.cu).
+struct PrefillArgs {
+  const void* q;                 // [T][Hq][D]
+  void* out;                     // [T][Hq][D] of out_dtype
+  const int32_t* q_start;        // [N + 1] query rows of each sequence
+  const int32_t* block_tables;   // [N][max_blocks]
+  const int32_t* seq_lens;       // [N]
+  int* err;                      // device error word
+  int64_t num_blocks;
+  int32_t num_seqs, num_q_heads, num_kv_heads, group;
+  int32_t block_size, max_blocks;
+  int32_t tok_per_op;            // tokens one TMA box covers: min(block_size, 64)
+  int32_t ops_per_stage;         // boxes per 64-token stage
+  int32_t out_dtype;             // pa_dtype
+  float scale_log2;              // scale * log2(e)
+};
+// Grid: (ceil(max_q_len * g / 64), H_kv, N).
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
+                           int head_dim, bool bf16, dim3 grid, cudaStream_t st);
+
 // Merges split-K partials into out (pa_decode_reduce.cu).
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);
 
