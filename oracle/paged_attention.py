@@ -33,6 +33,15 @@ Each function is the plain definition of one step, written from the pages:
 * the blockwise online-softmax recurrence and the partition-combine rule of
   ailinkdeeptech.com §3 (running max m, normaliser l, unnormalised o), used to
   pin the split-K reduction.
+* an FP8 cache: the same pool with one byte per element, which "halves the
+  bytes per block; nothing else about paging changes" (pofe.ai §Fine-tuned
+  models and adapters, quantised caches). The pages fix no format or scale, so
+  the reading taken is the OCP E4M3 encoding (1 sign, 4 exponent bits with
+  bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN, largest finite
+  448) with one float scale per layer for K and one for V: a stored code c
+  stands for value(c) * scale. A write stores e4m3(x / scale), the quotient
+  taken in float32 and rounded to the nearest code (ties to the even code),
+  magnitudes above 448 saturating to 448.
 
 Half-precision inputs arrive as uint16 bit patterns and are widened exactly to
 fp64 before any arithmetic. Parity unpinned: none (every function is checked
@@ -52,13 +61,77 @@ import numpy as np
 
 
 def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact fp64 value of fp16 / bf16 bit patterns."""
+    """Exact fp64 value of fp16 / bf16 bit patterns (uint16) or of E4M3 codes
+    (uint8, dtype "e4m3")."""
+    if dtype == "e4m3":
+        return e4m3_to_f64(bits)
     bits = np.asarray(bits, dtype=np.uint16)
     if dtype == "f16":
         return bits.view(np.float16).astype(np.float64)
     if dtype == "bf16":
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     raise ValueError(f"unknown dtype {dtype!r}")
+
+
+# ----------------------------------------------------------------------------
+# FP8 E4M3 codes (the reading of the pages' "FP8 cache")
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact value of E4M3 codes: sign bit 7, exponent bits 6..3 (bias 7),
+    mantissa bits 2..0. Exponent 0 is subnormal, m / 8 * 2^-6; otherwise
+    (1 + m / 8) * 2^(e - 7); exponent 15 with mantissa 7 is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_MAX = 448.0
+
+
+def _e4m3_grid() -> np.ndarray:
+    """Values of the non-negative finite codes 0x00 .. 0x7E, in code order
+    (which is also increasing value order)."""
+    return e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+
+
+def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Encode float32 values as E4M3 codes: nearest representable value, ties
+    to the even code, magnitudes beyond 448 saturate to 448, NaN gives 0x7F.
+    The sign is kept, so values that round to zero give +0 or -0."""
+    v = np.asarray(x, dtype=np.float32).astype(np.float64)
+    grid = _e4m3_grid()
+    a = np.abs(v)
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 1, len(grid) - 1)  # grid[hi] >= a
+    lo = hi - 1
+    d_lo = a - grid[lo]
+    d_hi = grid[hi] - a
+    code = np.where(d_lo < d_hi, lo, hi)
+    code = np.where(d_lo == d_hi, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(a == 0.0, 0, code)
+    code = np.where(a >= _E4M3_MAX, 0x7E, code)
+    out = (np.where(np.signbit(v), 0x80, 0) | code).astype(np.uint8)
+    return np.where(np.isnan(v), np.uint8(0x7F), out).astype(np.uint8)
+
+
+def quantize_e4m3(bits: np.ndarray, dtype: str, scale: float) -> np.ndarray:
+    """Codes a write stores for fp16 / bf16 inputs: e4m3(x / scale), the
+    quotient rounded once to float32."""
+    x = bits_to_f64(bits, dtype).astype(np.float32)
+    return f32_to_e4m3(x / np.float32(scale))
+
+
+def write_kv_e4m3(k_cache: np.ndarray, v_cache: np.ndarray, key: np.ndarray, value: np.ndarray,
+                  slots: Sequence[int], dtype: str, k_scale: float, v_scale: float
+                  ) -> Tuple[np.ndarray, np.ndarray]:
+    """write_kv into E4M3 caches: each token's k, v rows (fp16 / bf16 bits of
+    ``dtype``) are quantised with the layer's scale, then stored at the slot."""
+    return write_kv(k_cache, v_cache, quantize_e4m3(key, dtype, k_scale),
+                    quantize_e4m3(value, dtype, v_scale), slots)
 
 
 # ----------------------------------------------------------------------------
@@ -141,13 +214,26 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.n
     return p @ V
 
 
+def _cache_rows(cache: np.ndarray, table_row, length: int, kv_head: int, dtype: str,
+                kv_dtype: Optional[str], kv_scale: float) -> np.ndarray:
+    """fp64 K or V rows of one sequence and KV head: the gathered stored values,
+    times the layer's scale for an E4M3 cache."""
+    rows = gather_kv(cache, table_row, length, kv_head)
+    if kv_dtype == "e4m3":
+        return e4m3_to_f64(rows) * float(np.float32(kv_scale))
+    return bits_to_f64(rows, dtype)
+
+
 def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.ndarray,
            seq_lens: Sequence[int], scale: float, dtype: str,
-           pairs: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+           pairs: Optional[Sequence[Tuple[int, int]]] = None, kv_dtype: Optional[str] = None,
+           k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """Decode attention for every (sequence, query head), or for ``pairs`` only.
 
     Returns fp64 ``[N, H_q, D]``; rows not in ``pairs`` are NaN. A sequence of
-    length 0 attends to nothing and yields zeros.
+    length 0 attends to nothing and yields zeros. ``dtype`` is that of q (and of
+    the cache unless ``kv_dtype`` is "e4m3", whose codes stand for
+    value * k_scale and value * v_scale).
     """
     n, hq, d = q.shape
     hkv = k_cache.shape[2]
@@ -164,8 +250,8 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
         if L == 0:
             out[s, heads] = 0.0
             continue
-        K = bits_to_f64(gather_kv(k_cache, block_tables[s], L, kvh), dtype)
-        V = bits_to_f64(gather_kv(v_cache, block_tables[s], L, kvh), dtype)
+        K = _cache_rows(k_cache, block_tables[s], L, kvh, dtype, kv_dtype, k_scale)
+        V = _cache_rows(v_cache, block_tables[s], L, kvh, dtype, kv_dtype, v_scale)
         Q = bits_to_f64(q[s, heads], dtype)
         out[s, heads] = attention(Q, K, V, scale)
     return out
@@ -173,7 +259,8 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, block_tables
 
 def prefill(q: np.ndarray, q_start: Sequence[int], k_cache: np.ndarray, v_cache: np.ndarray,
             block_tables: np.ndarray, seq_lens: Sequence[int], scale: float, dtype: str,
-            rows: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+            rows: Optional[Sequence[Tuple[int, int]]] = None, kv_dtype: Optional[str] = None,
+            k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """Causal multi-token attention over the paged cache.
 
     ``q`` is ``[T, H_q, D]``; sequence s owns query rows ``q_start[s] ..
@@ -181,7 +268,7 @@ def prefill(q: np.ndarray, q_start: Sequence[int], k_cache: np.ndarray, v_cache:
     position L - n + i and attends to the tokens at positions 0 .. L - n + i,
     read through the block table. Returns fp64 ``[T, H_q, D]``; with ``rows``
     (a list of (query row, query head)) only those are computed and the rest
-    are NaN.
+    are NaN. ``kv_dtype`` and the scales are those of :func:`decode`.
     """
     t_all, hq, d = q.shape
     hkv = k_cache.shape[2]
@@ -206,8 +293,8 @@ def prefill(q: np.ndarray, q_start: Sequence[int], k_cache: np.ndarray, v_cache:
             raise ValueError(f"sequence {s}: {n} queries but only {L} tokens")
         pos = L - n + (t - int(q_start[s]))
         if (s, kvh) not in cache:
-            cache = {(s, kvh): (bits_to_f64(gather_kv(k_cache, block_tables[s], L, kvh), dtype),
-                                bits_to_f64(gather_kv(v_cache, block_tables[s], L, kvh), dtype))}
+            cache = {(s, kvh): (_cache_rows(k_cache, block_tables[s], L, kvh, dtype, kv_dtype, k_scale),
+                                _cache_rows(v_cache, block_tables[s], L, kvh, dtype, kv_dtype, v_scale))}
         K, V = cache[(s, kvh)]
         Q = bits_to_f64(q[t, heads], dtype)
         out[t, heads] = attention(Q, K[:pos + 1], V[:pos + 1], scale)

@@ -16,6 +16,11 @@ Recipe (shared by every config):
   into its arithmetic produces NaN, so masking is checked at every size.
 * Physical placement comes from :mod:`workloads.block_manager` with a seeded
   shuffle of the free list; block tables are zero padded to the longest table.
+* FP8 (E4M3) caches (``kv_dtype="e4m3"``) hold uniformly drawn byte codes
+  (every code but the two NaN codes, 0x7F and 0xFF) in owned rows and the NaN
+  code elsewhere; q and the new K/V rows stay fp16/bf16 and the layer scales
+  are FP8_K_SCALE / FP8_V_SCALE. The generator draws bytes only: it encodes
+  nothing.
 
 Five named configs follow the decode scenarios the pages discuss: a tiny case
 holding the ten-token, b=4, table [7, 2, 11] example; a 7B/13B-style MHA batch;
@@ -32,7 +37,12 @@ import numpy as np
 
 from .block_manager import BlockPool, SeqTable
 
-NAN_BITS = {"f16": np.uint16(0x7E00), "bf16": np.uint16(0x7FC0)}
+NAN_BITS = {"f16": np.uint16(0x7E00), "bf16": np.uint16(0x7FC0), "e4m3": np.uint8(0x7F)}
+# Per-layer scales of E4M3 caches in the generated workloads: a stored code c
+# stands for value(c) * scale. Uniform codes times these give K and V of rms
+# about 0.8 and 0.65; N(0,1) inputs beyond |x| = 3 (K) and 2.5 (V) saturate.
+FP8_K_SCALE = float(np.float32(3.0 / 448.0))
+FP8_V_SCALE = float(np.float32(2.5 / 448.0))
 _BASE_LEN = 1 << 24
 
 CONFIG_NAMES = {
@@ -109,6 +119,15 @@ class Workload:
     # Multi-token cases: sequence s owns query rows q_start[s] .. q_start[s+1]
     # of q [T, H_q, D] (None: decode, one query row per sequence).
     q_start: Optional[np.ndarray] = None
+    # E4M3 caches: "e4m3" (uint8 codes, K/V values code * k_scale / v_scale);
+    # None: the cache holds ``dtype`` bit patterns.
+    kv_dtype: Optional[str] = None
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def cache_dtype(self) -> str:
+        return self.kv_dtype or self.dtype
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -140,11 +159,17 @@ def decode_step_tokens(w: Workload) -> np.ndarray:
 
 
 class _Filler:
-    """Fills pool blocks with windows of one N(0,1) sample."""
+    """Fills pool blocks with windows of one N(0,1) sample (fp16 / bf16), or of
+    one sample of uniform non-NaN byte codes (e4m3)."""
 
     def __init__(self, rng: np.random.Generator, dtype: str) -> None:
         self.rng = rng
-        self.base = to_bits(rng.standard_normal(_BASE_LEN, dtype=np.float32), dtype)
+        if dtype == "e4m3":
+            mag = rng.integers(0, 0x7F, size=_BASE_LEN, dtype=np.uint8)  # 0x00 .. 0x7E
+            sign = rng.integers(0, 2, size=_BASE_LEN, dtype=np.uint8) << np.uint8(7)
+            self.base = mag | sign
+        else:
+            self.base = to_bits(rng.standard_normal(_BASE_LEN, dtype=np.float32), dtype)
 
     def block(self, n: int) -> np.ndarray:
         off = int(self.rng.integers(0, _BASE_LEN - n))
@@ -186,9 +211,17 @@ def _fill_sequences(k: np.ndarray, v: np.ndarray, tables, lens, filler_k: _Fille
 
 def _new_pool(nb: int, b: int, hkv: int, d: int, dtype: str):
     nan = NAN_BITS[dtype]
-    k = np.full((nb, b, hkv, d), nan, dtype=np.uint16)
-    v = np.full((nb, b, hkv, d), nan, dtype=np.uint16)
+    k = np.full((nb, b, hkv, d), nan, dtype=nan.dtype)
+    v = np.full((nb, b, hkv, d), nan, dtype=nan.dtype)
     return k, v, nan
+
+
+def _fp8_fields(kv_dtype: Optional[str]) -> dict:
+    if kv_dtype is None:
+        return {}
+    if kv_dtype != "e4m3":
+        raise ValueError(f"unknown kv_dtype {kv_dtype!r}")
+    return {"kv_dtype": "e4m3", "k_scale": FP8_K_SCALE, "v_scale": FP8_V_SCALE}
 
 
 # ----------------------------------------------------------------------------
@@ -199,11 +232,12 @@ def make_random_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads
                      head_dim: int, block_size: int, seq_lens: Sequence[int],
                      dtype: str = "f16", pool_factor: float = 1.25, pad: int = 0,
                      scale: Optional[float] = None, partition_tokens: int = 0,
-                     name: str = "random") -> Workload:
+                     name: str = "random", kv_dtype: Optional[str] = None) -> Workload:
     """A decode batch with given lengths and a shuffled pool.
 
     The scenario writes each sequence's newest token (position L-1) and decodes.
-    Sequences of length 0 own no block and write nothing.
+    Sequences of length 0 own no block and write nothing. ``kv_dtype="e4m3"``
+    gives an FP8 pool (q and the new rows stay ``dtype``).
     """
     rng = np.random.default_rng(seed)
     b = block_size
@@ -218,8 +252,9 @@ def make_random_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads
         s.admit(L)
         seqs.append(s)
     tables = [s.table for s in seqs]
-    k, v, nan = _new_pool(nb, b, num_kv_heads, head_dim, dtype)
-    fk, fv = _Filler(rng, dtype), _Filler(rng, dtype)
+    cdt = kv_dtype or dtype
+    k, v, nan = _new_pool(nb, b, num_kv_heads, head_dim, cdt)
+    fk, fv = _Filler(rng, cdt), _Filler(rng, cdt)
     _fill_sequences(k, v, tables, lens, fk, fv, nan)
     q = _normal_bits(rng, (num_seqs, num_q_heads, head_dim), dtype)
     writers = [i for i, L in enumerate(lens) if L > 0]
@@ -233,13 +268,15 @@ def make_random_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads
         seq_lens=np.array(lens, dtype=np.int32), key=key, value=value,
         seq_idx=np.array(writers, dtype=np.int32),
         positions=np.array([lens[i] - 1 for i in writers], dtype=np.int32),
-        copy_pairs=np.zeros((0, 2), dtype=np.int64), partition_tokens=partition_tokens)
+        copy_pairs=np.zeros((0, 2), dtype=np.int64), partition_tokens=partition_tokens,
+        **_fp8_fields(kv_dtype))
 
 
 def make_prefill_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_heads: int,
                       head_dim: int, block_size: int, seq_lens: Sequence[int],
                       q_lens: Sequence[int], dtype: str = "f16", pool_factor: float = 1.25,
-                      scale: Optional[float] = None, name: str = "prefill") -> Workload:
+                      scale: Optional[float] = None, name: str = "prefill",
+                      kv_dtype: Optional[str] = None) -> Workload:
     """A multi-token batch: sequence s ends with q_lens[s] new tokens.
 
     The pool holds the first L - n tokens of each sequence (n = q_lens[s]); the
@@ -262,8 +299,9 @@ def make_prefill_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_head
         s.admit(L)
         seqs.append(s)
     tables = [s.table for s in seqs]
-    k, v, nan = _new_pool(nb, b, num_kv_heads, head_dim, dtype)
-    fk, fv = _Filler(rng, dtype), _Filler(rng, dtype)
+    cdt = kv_dtype or dtype
+    k, v, nan = _new_pool(nb, b, num_kv_heads, head_dim, cdt)
+    fk, fv = _Filler(rng, cdt), _Filler(rng, cdt)
     _fill_sequences(k, v, tables, lens, fk, fv, nan)
     t_all = sum(qn)
     q = _normal_bits(rng, (t_all, num_q_heads, head_dim), dtype)
@@ -280,7 +318,8 @@ def make_prefill_case(seed: int, *, num_seqs: int, num_q_heads: int, num_kv_head
         scale=float(scale if scale is not None else 1.0 / np.sqrt(head_dim)),
         q=q, k_cache=k, v_cache=v, block_tables=_pad_tables(tables, 0),
         seq_lens=np.array(lens, dtype=np.int32), key=key, value=value, seq_idx=seq_idx,
-        positions=positions, copy_pairs=np.zeros((0, 2), dtype=np.int64), q_start=q_start)
+        positions=positions, copy_pairs=np.zeros((0, 2), dtype=np.int64), q_start=q_start,
+        **_fp8_fields(kv_dtype))
 
 
 # ----------------------------------------------------------------------------
@@ -320,14 +359,16 @@ def _config1(rng: np.random.Generator) -> Workload:
         copy_pairs=np.zeros((0, 2), dtype=np.int64), partition_tokens=0)
 
 
-def _decode_batch(rng, name, *, n, hq, hkv, d, b, dtype, lens, partition_tokens) -> Workload:
+def _decode_batch(rng, name, *, n, hq, hkv, d, b, dtype, lens, partition_tokens,
+                  kv_dtype=None) -> Workload:
     w = make_random_case(int(rng.integers(0, 2**31)), num_seqs=n, num_q_heads=hq,
                          num_kv_heads=hkv, head_dim=d, block_size=b, seq_lens=lens,
-                         dtype=dtype, partition_tokens=partition_tokens, name=name)
+                         dtype=dtype, partition_tokens=partition_tokens, name=name,
+                         kv_dtype=kv_dtype)
     return w
 
 
-def _config5(rng: np.random.Generator) -> Workload:
+def _config5(rng: np.random.Generator, kv_dtype: Optional[str] = None) -> Workload:
     """256 sequences sharing one 1000-token prefix, private suffixes U[16,512].
 
     The prefix fills 62 full blocks and 8 rows of a 63rd. Each sequence's first
@@ -355,8 +396,9 @@ def _config5(rng: np.random.Generator) -> Workload:
             p = s.append()
             if p is not None:
                 pairs.append(p)
-    k, v, nan = _new_pool(nb, b, hkv, d, dtype)
-    fk, fv = _Filler(rng, dtype), _Filler(rng, dtype)
+    cdt = kv_dtype or dtype
+    k, v, nan = _new_pool(nb, b, hkv, d, cdt)
+    fk, fv = _Filler(rng, cdt), _Filler(rng, cdt)
     _fill_sequences(k, v, [prefix_blocks], [prefix], fk, fv, nan)
     lens = [prefix + int(s) for s in suffix]
     total = len(seq_idx)
@@ -371,27 +413,36 @@ def _config5(rng: np.random.Generator) -> Workload:
         seq_idx=np.array(seq_idx, dtype=np.int32), positions=np.array(positions, dtype=np.int32),
         copy_pairs=np.array(pairs, dtype=np.int64).reshape(-1, 2), partition_tokens=512,
         shared_blocks=prefix_blocks[:62],
-        meta={"prefix_tokens": prefix, "suffix_tokens": suffix.astype(np.int64)})
+        meta={"prefix_tokens": prefix, "suffix_tokens": suffix.astype(np.int64)},
+        **_fp8_fields(kv_dtype))
 
 
-def make_config(cid: int, *, block_size: Optional[int] = None) -> Workload:
-    """Build named config ``cid`` (1..5). ``block_size`` overrides config 4's b."""
+def make_config(cid: int, *, block_size: Optional[int] = None,
+                kv_dtype: Optional[str] = None) -> Workload:
+    """Build named config ``cid`` (1..5). ``block_size`` overrides config 4's b;
+    ``kv_dtype="e4m3"`` gives configs 2-5 an FP8 pool of the same shape and
+    lengths (tables and values are drawn afresh)."""
     rng = np.random.default_rng(1000 + cid)
+    if kv_dtype is not None and cid == 1:
+        raise ValueError("config 1 (head_dim 64) has no FP8 variant")
+    suffix = "_e4m3" if kv_dtype == "e4m3" else ""
     if cid == 1:
         return _config1(rng)
     if cid == 2:
         lens = rng.integers(128, 2048, size=64, endpoint=True)
-        return _decode_batch(rng, CONFIG_NAMES[2], n=64, hq=32, hkv=32, d=128, b=16,
-                             dtype="f16", lens=lens, partition_tokens=512)
+        return _decode_batch(rng, CONFIG_NAMES[2] + suffix, n=64, hq=32, hkv=32, d=128, b=16,
+                             dtype="f16", lens=lens, partition_tokens=512, kv_dtype=kv_dtype)
     if cid == 3:
         lens = rng.integers(512, 8192, size=128, endpoint=True)
-        return _decode_batch(rng, CONFIG_NAMES[3], n=128, hq=64, hkv=8, d=128, b=16,
-                             dtype="bf16", lens=lens, partition_tokens=512)
+        return _decode_batch(rng, CONFIG_NAMES[3] + suffix, n=128, hq=64, hkv=8, d=128, b=16,
+                             dtype="bf16", lens=lens, partition_tokens=512, kv_dtype=kv_dtype)
     if cid == 4:
         b = 32 if block_size is None else int(block_size)
-        name = CONFIG_NAMES[4] + f"_b{b}"
+        name = CONFIG_NAMES[4] + f"_b{b}" + suffix
         return _decode_batch(rng, name, n=8, hq=32, hkv=8, d=128, b=b, dtype="bf16",
-                             lens=[32768] * 8, partition_tokens=512)
+                             lens=[32768] * 8, partition_tokens=512, kv_dtype=kv_dtype)
     if cid == 5:
-        return _config5(rng)
+        w = _config5(rng, kv_dtype)
+        w.name += suffix
+        return w
     raise ValueError(f"unknown config {cid}")
