@@ -22,10 +22,20 @@
  *    pa_get_device_error reads and clears.
  *
  * Cache layout (per layer): k and v are each [num_blocks][block_size]
- * [num_kv_heads][head_dim], row-major, fp16 or bf16; element (blk, off, h, d)
- * is at ((blk*block_size + off)*num_kv_heads + h)*head_dim + d. A "slot" numbers
- * pool rows: slot = blk*block_size + off. Layers are separate pools that share
- * block ids.
+ * [num_kv_heads][head_dim], row-major, fp16, bf16 or FP8 E4M3 codes; element
+ * (blk, off, h, d) is at ((blk*block_size + off)*num_kv_heads + h)*head_dim + d.
+ * A "slot" numbers pool rows: slot = blk*block_size + off. Layers are separate
+ * pools that share block ids.
+ *
+ * FP8 caches ("PagedAttention: paging the KV cache", section "Fine-tuned models
+ * and adapters": an FP8 cache halves the bytes per block and nothing else about
+ * paging changes). The pages fix no format, so this library takes OCP E4M3
+ * (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * 0x7F/0xFF NaN, largest finite 448) with one float scale per layer for K and
+ * one for V: a stored code c stands for value(c) * k_scale (or v_scale).
+ * Writes store e4m3(x / scale): the quotient rounded once to float32, then to
+ * the nearest code, ties to even, magnitudes past 448 saturating to 448.
+ * q, the new key/value rows and the outputs stay fp16/bf16 (act_dtype).
  */
 #ifndef PAGED_KV_CACHE_114_GB300_PA_H
 #define PAGED_KV_CACHE_114_GB300_PA_H
@@ -37,9 +47,9 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
-typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 enum {
   PA_OK = 0,
@@ -68,7 +78,13 @@ typedef struct {
   int32_t block_size;   /* tokens per block b */
   int32_t num_kv_heads; /* H_kv */
   int32_t head_dim;     /* D */
-  pa_dtype dtype;       /* PA_F16 or PA_BF16 */
+  pa_dtype dtype;       /* element type of k and v: PA_F16, PA_BF16 or PA_FP8_E4M3 */
+  pa_dtype act_dtype;   /* PA_FP8_E4M3 caches: dtype of q, key and value (PA_F16 or
+                           PA_BF16); ignored for 16-bit caches, whose q, key and
+                           value have the cache's own dtype */
+  float k_scale;        /* PA_FP8_E4M3 caches: K code c stands for value(c) * k_scale;
+                           finite and > 0. Ignored for 16-bit caches. */
+  float v_scale;        /* the same for V */
 } pa_cache;
 
 /*
@@ -96,8 +112,10 @@ int pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_b
  * k_cache[slot / b][slot % b][h][:] = key[i][h][:], same for v (pofe.ai,
  * sections "How it works", "write k, v of the new token into slot len(s) % b of
  * block table[s][-1]", and "Minimal implementation", Sequence.append).
- *   key, value    device [num_tokens][num_kv_heads][head_dim], cache dtype,
- *                 16-byte aligned
+ *   key, value    device [num_tokens][num_kv_heads][head_dim], 16-byte aligned,
+ *                 of the cache's dtype (16-bit caches) or of act_dtype (FP8
+ *                 caches, whose rows are quantised: code = e4m3(x / k_scale)
+ *                 for K and e4m3(x / v_scale) for V, see the FP8 note above)
  *   slot_mapping  device int64 [num_tokens]; -1 marks a padding token (skipped)
  *   cache         host pointer to one pa_cache
  * Errors: a slot outside [-1, num_blocks*block_size) skips the token and sets
@@ -111,7 +129,8 @@ int pa_write_kv(const void* key, const void* value, const int64_t* slot_mapping,
  * every layer, block dst of k and v becomes a copy of block src (pofe.ai,
  * section "Sharing and copy-on-write" and Sequence.append in "Minimal
  * implementation"; ailinkdeeptech.com section 4, Copy-on-Write step 2).
- *   caches         host array of num_layers pa_cache (same geometry and dtype)
+ *   caches         host array of num_layers pa_cache (same geometry and dtype;
+ *                  FP8 blocks are copied code for code, scales play no part)
  *   src_dst_pairs  device int64 [num_pairs][2]
  * Destinations must be distinct and no destination may also be a source
  * (copy-on-write always copies into a fresh block); pa_check_copy_pairs checks
@@ -135,9 +154,12 @@ int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t nu
  * "PagedAttention", section "The kernel consequence"); the g query heads of a
  * KV head share each loaded block (ailinkdeeptech.com Step 2, grouped-query
  * ratio). Slots at t >= L_s are never part of the result.
- *   q              device [num_seqs][num_q_heads][head_dim], cache dtype
- *   cache          host pointer to one pa_cache; head_dim 64, 128 or 256;
- *                  block_size a divisor of 16 or a multiple of 16
+ *   q              device [num_seqs][num_q_heads][head_dim], of the cache's
+ *                  dtype (16-bit caches) or of act_dtype (FP8 caches)
+ *   cache          host pointer to one pa_cache; head_dim 64, 128 or 256
+ *                  (128 or 256 for FP8 caches); block_size a divisor of 16 or
+ *                  a multiple of 16. With an FP8 cache, K[t] and V[t] are the
+ *                  stored codes' values times k_scale and v_scale.
  *   block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries past
  *                  ceil(L_s/b) are never read
  *   seq_lens       device int32 [num_seqs]; 0 gives a zero output row
@@ -186,7 +208,8 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
  *   q            device [q_start[num_seqs]][num_q_heads][head_dim], cache dtype
  *   q_start      device int32 [num_seqs + 1], non-decreasing, q_start[0] = 0
  *   max_q_len    host upper bound of every n_s (sizes the launch)
- *   cache        host pointer to one pa_cache; head_dim 64, 128 or 256;
+ *   cache        host pointer to one pa_cache (fp16 or bf16; an FP8 cache
+ *                returns PA_ERR_DTYPE); head_dim 64, 128 or 256;
  *                block_size >= 8 and a divisor or a multiple of 64
  *   block_tables device int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens     device int32 [num_seqs]

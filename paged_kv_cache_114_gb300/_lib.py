@@ -11,7 +11,8 @@ import threading
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
 
-PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+PA_F16, PA_BF16, PA_F32, PA_FP8_E4M3 = 0, 1, 2, 3
+ABI_VERSION = 2  # PA_ABI_VERSION this binding is written for
 PA_OK = 0
 PA_PARTITION_BALANCED = -1
 STATUS = {
@@ -40,6 +41,9 @@ class PaCache(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
         ("dtype", ctypes.c_int),
+        ("act_dtype", ctypes.c_int),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -93,7 +97,12 @@ def lib():
                     raise RuntimeError(
                         f"{LIB_PATH} is missing: build it with "
                         "`python -m paged_kv_cache_114_gb300.build` (there is no fallback)")
-                _lib = _declare(ctypes.CDLL(LIB_PATH))
+                loaded = _declare(ctypes.CDLL(LIB_PATH))
+                if loaded.pa_abi_version() != ABI_VERSION:
+                    raise RuntimeError(
+                        f"{LIB_PATH} has ABI version {loaded.pa_abi_version()}, this binding needs "
+                        f"{ABI_VERSION}: rebuild it with `python -m paged_kv_cache_114_gb300.build`")
+                _lib = loaded
     return _lib
 
 

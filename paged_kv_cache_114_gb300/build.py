@@ -1,7 +1,7 @@
 """Builds libpagedkv.so in-tree with nvcc for sm_103a (GB300).
 
 Each translation unit compiles in its own nvcc process, in parallel; the decode
-kernel is compiled once per (dtype, head_dim). The library links the CUDA
+kernel is compiled once per (cache type, dtype, head_dim). The library links the CUDA
 runtime statically and needs no libcuda at link time (the tensor-map encoder
 is fetched through the runtime's driver entry-point query).
 
@@ -36,6 +36,10 @@ def _units():
         for d in (64, 128, 256):
             tag = f"pa_decode_{'bf16' if bf else 'f16'}_{d}"
             units.append((tag, "pa_decode_inst.cu", [f"-DPA_INST_BF16={bf}", f"-DPA_INST_D={d}"]))
+        for d in (128, 256):  # E4M3 caches
+            tag = f"pa_decode_e4m3_{'bf16' if bf else 'f16'}_{d}"
+            units.append((tag, "pa_decode_inst.cu", [f"-DPA_INST_BF16={bf}", f"-DPA_INST_D={d}",
+                                                     "-DPA_INST_FP8=1"]))
     return units
 
 

@@ -61,19 +61,30 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+bool is_fp8(const pa_cache& c) { return c.dtype == PA_FP8_E4M3; }
+
+// Bytes per stored element of a cache.
+cuuint64_t elem_bytes(const pa_cache& c) { return is_fp8(c) ? 1 : 2; }
+
+// Element type of the tensor maps; a box's inner extent is one 128-byte line.
+CUtensorMapDataType map_type(const pa_cache& c) {
+  if (is_fp8(c)) return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
 // Tensor map over one cache [num_blocks][b][H_kv][D] viewed as 4-D
-// (D, H_kv, b, num_blocks), box = 64 x 1 x tok_per_op x 1, 128-byte swizzle.
+// (D, H_kv, b, num_blocks), box = (128 bytes of D) x 1 x tok_per_op x 1,
+// 128-byte swizzle.
 bool encode_cache_map(CUtensorMap* m, const void* base, const pa_cache& c, int tok_per_op) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  const cuuint64_t e = 2;  // bytes per element
+  const cuuint64_t e = elem_bytes(c);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.head_dim), static_cast<cuuint64_t>(c.num_kv_heads),
                         static_cast<cuuint64_t>(c.block_size), static_cast<cuuint64_t>(c.num_blocks)};
   cuuint64_t strides[3] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e};
-  cuuint32_t box[4] = {64u, 1u, static_cast<cuuint32_t>(tok_per_op), 1u};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / e), 1u, static_cast<cuuint32_t>(tok_per_op), 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUtensorMapDataType dt =
-      c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = map_type(c);
   CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -84,13 +95,21 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int check_cache(const pa_cache* c) {
   if (c == nullptr || c->k == nullptr || c->v == nullptr) return PA_ERR_NULL;
-  if (c->dtype != PA_F16 && c->dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (c->dtype != PA_F16 && c->dtype != PA_BF16 && c->dtype != PA_FP8_E4M3) return PA_ERR_DTYPE;
   if (c->num_blocks <= 0 || c->num_blocks > 0x7fffffffLL || c->block_size <= 0 ||
       c->num_kv_heads <= 0 || c->head_dim <= 0 || c->head_dim % 8 != 0)
     return PA_ERR_SHAPE;
+  if (is_fp8(*c)) {
+    if (c->act_dtype != PA_F16 && c->act_dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (!(std::isfinite(c->k_scale) && c->k_scale > 0.f && std::isfinite(c->v_scale) &&
+          c->v_scale > 0.f))
+      return PA_ERR_ARG;
+    if (c->head_dim % 16 != 0) return PA_ERR_SHAPE;  // 16-byte rows for the vector copies
+  }
   if (!aligned(c->k, 16) || !aligned(c->v, 16)) return PA_ERR_ALIGN;
   return PA_OK;
 }
+
 
 int64_t decode_parts(int32_t max_seq_len, int32_t partition_tokens) {
   if (partition_tokens <= 0 || max_seq_len <= partition_tokens) return 1;
@@ -149,20 +168,20 @@ BalancedPlan balanced_plan(int32_t num_kv_heads, int32_t group, int32_t head_dim
 }
 
 // Tensor map for the grouped kernel: the cache viewed as (D, token, head,
-// block) - token before head, strides permuted - with box 64 x tok_per_op x
-// HG x 1, so one box lands head-major in shared memory.
+// block) - token before head, strides permuted - with box (128 bytes of D) x
+// tok_per_op x HG x 1, so one box lands head-major in shared memory.
 bool encode_grouped_map(CUtensorMap* m, const void* base, const pa_cache& c, int tok_per_op,
                         int hg) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  const cuuint64_t e = 2;
+  const cuuint64_t e = elem_bytes(c);
   const cuuint64_t D = c.head_dim, H = c.num_kv_heads, B = c.block_size;
   cuuint64_t dims[4] = {D, B, H, static_cast<cuuint64_t>(c.num_blocks)};
   cuuint64_t strides[3] = {D * H * e, D * e, D * H * B * e};
-  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(tok_per_op), static_cast<cuuint32_t>(hg), 1u};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / e), static_cast<cuuint32_t>(tok_per_op),
+                       static_cast<cuuint32_t>(hg), 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUtensorMapDataType dt =
-      c.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = map_type(c);
   CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -228,12 +247,20 @@ int pa_write_kv(const void* key, const void* value, const int64_t* slot_mapping,
   if (!key || !value || !slot_mapping) return PA_ERR_NULL;
   if (!aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8)) return PA_ERR_ALIGN;
   if (num_tokens > 0x7fffffffLL) return PA_ERR_SHAPE;
-  const int64_t row_bytes = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim * 2;
+  const int64_t row_elems = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
-  cudaError_t e = pa::launch_write_kv(key, value, slot_mapping, num_tokens, cache->k, cache->v,
-                                      cache->num_blocks, cache->block_size, row_bytes, di.err,
-                                      static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (is_fp8(*cache)) {
+    e = pa::launch_write_kv_e4m3(key, value, cache->act_dtype == PA_BF16, slot_mapping, num_tokens,
+                                 cache->k, cache->v, cache->num_blocks, cache->block_size,
+                                 row_elems, cache->k_scale, cache->v_scale, di.err,
+                                 static_cast<cudaStream_t>(stream));
+  } else {
+    e = pa::launch_write_kv(key, value, slot_mapping, num_tokens, cache->k, cache->v,
+                            cache->num_blocks, cache->block_size, row_elems * 2, di.err,
+                            static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -273,7 +300,7 @@ int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* sr
   if (src_dst_pairs == nullptr) return PA_ERR_NULL;
   if (!aligned(src_dst_pairs, 8)) return PA_ERR_ALIGN;
   const int64_t block_bytes = static_cast<int64_t>(caches[0].block_size) * caches[0].num_kv_heads *
-                              caches[0].head_dim * 2;
+                              caches[0].head_dim * static_cast<int64_t>(elem_bytes(caches[0]));
   if (num_pairs * ((block_bytes + 16383) / 16384) > 0x7fffffffLL) return PA_ERR_SHAPE;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
@@ -353,6 +380,7 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
                pa_dtype out_dtype, void* stream) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
+  if (is_fp8(*cache)) return PA_ERR_DTYPE;
   if (num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
   if (num_seqs == 0 || max_q_len == 0) return PA_OK;
@@ -415,7 +443,9 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   const int D = cache->head_dim;
   const int b = cache->block_size;
   const int hkv = cache->num_kv_heads;
+  const bool fp8 = is_fp8(*cache);
   if (D != 64 && D != 128 && D != 256) return PA_ERR_SHAPE;
+  if (fp8 && D == 64) return PA_ERR_SHAPE;
   if (!(b % pa::kStageRows == 0 || pa::kStageRows % b == 0)) return PA_ERR_SHAPE;
   if (num_q_heads % hkv != 0) return PA_ERR_SHAPE;
   const int g = num_q_heads / hkv;
@@ -456,7 +486,10 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   a.slot_rows = a.tok_per_op < 8 ? 8 : a.tok_per_op;
   a.ops_per_stage = pa::kStageRows / a.slot_rows;
   a.out_dtype = out_dtype;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // E4M3: the logit of code row c is scale * k_scale * (q . value(c))
+  const double kscale = fp8 ? static_cast<double>(cache->k_scale) : 1.0;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kscale * 1.4426950408889634);
+  a.v_scale = fp8 ? cache->v_scale : 1.f;
   dim3 grid(static_cast<unsigned>(hkv), static_cast<unsigned>(parts),
             static_cast<unsigned>(num_seqs));
   if (!balanced && parts > 1) {
@@ -508,7 +541,15 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
     e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(num_seqs) * hkv * sizeof(unsigned int), st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
-  if (cache->dtype == PA_F16) {
+  if (fp8) {
+    if (cache->act_dtype == PA_F16) {
+      e = D == 128 ? pa::launch_decode_e4m3_f16_128(tk, tv, a, tiles, head_group, grid, kernel, st)
+                   : pa::launch_decode_e4m3_f16_256(tk, tv, a, tiles, head_group, grid, kernel, st);
+    } else {
+      e = D == 128 ? pa::launch_decode_e4m3_bf16_128(tk, tv, a, tiles, head_group, grid, kernel, st)
+                   : pa::launch_decode_e4m3_bf16_256(tk, tv, a, tiles, head_group, grid, kernel, st);
+    }
+  } else if (cache->dtype == PA_F16) {
     e = D == 64 ? pa::launch_decode_f16_64(tk, tv, a, tiles, head_group, grid, kernel, st)
         : D == 128 ? pa::launch_decode_f16_128(tk, tv, a, tiles, head_group, grid, kernel, st)
                    : pa::launch_decode_f16_256(tk, tv, a, tiles, head_group, grid, kernel, st);

@@ -3,10 +3,13 @@
 // All three are integer indexing plus byte movement; results are bit-exact.
 // Out-of-range indices never fault: the row is skipped and a bit is OR-ed
 // into the device error word.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "pa_internal.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 namespace {
@@ -58,6 +61,50 @@ __global__ void write_kv_kernel(const uint4* __restrict__ key, const uint4* __re
     const uint4 vx = __ldg(vs + c);
     kd[c] = kx;
     vd[c] = vx;
+  }
+}
+
+// E4M3 caches: one CTA per token quantises its K and V rows (H_kv * D fp16 or
+// bf16 values) to codes e4m3(x / scale) - the quotient rounded once to float32
+// (IEEE division), then to the nearest code, ties to even, saturating at +-448 -
+// and stores them at the slot; 8 values per thread and step (16-byte loads,
+// 8-byte stores). This is the "FP8 cache" of "PagedAttention: paging the KV
+// cache" (Fine-tuned models and adapters) read as E4M3 with per-layer scales.
+template <bool IS_BF16>
+__device__ __forceinline__ uint2 quantize8(const uint4 x, float scale) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 a = unpack2<IS_BF16>(w[2 * i]);
+    const float2 b = unpack2<IS_BF16>(w[2 * i + 1]);
+    const uint32_t lo = e4m3x2_encode(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
+    const uint32_t hi = e4m3x2_encode(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale));
+    out[i] = lo | (hi << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+template <bool IS_BF16>
+__global__ void write_kv_e4m3_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                     const int64_t* __restrict__ slots, uint2* __restrict__ k_cache,
+                                     uint2* __restrict__ v_cache, int64_t num_slots,
+                                     int64_t row_vecs, float k_scale, float v_scale, int* err) {
+  const int64_t tok = blockIdx.x;
+  const int64_t slot = slots[tok];
+  if (slot < 0 || slot >= num_slots) {
+    if (slot != -1 && threadIdx.x == 0) atomicOr(err, PA_DEVERR_SLOT);
+    return;
+  }
+  const uint4* ks = key + tok * row_vecs;
+  const uint4* vs = value + tok * row_vecs;
+  uint2* kd = k_cache + slot * row_vecs;
+  uint2* vd = v_cache + slot * row_vecs;
+  for (int64_t c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+    const uint4 kx = __ldg(ks + c);
+    const uint4 vx = __ldg(vs + c);
+    kd[c] = quantize8<IS_BF16>(kx, k_scale);
+    vd[c] = quantize8<IS_BF16>(vx, v_scale);
   }
 }
 
@@ -118,6 +165,21 @@ cudaError_t launch_write_kv(const void* key, const void* value, const int64_t* s
       static_cast<const uint4*>(key), static_cast<const uint4*>(value), slots,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks * block_size,
       row_vecs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv_e4m3(const void* key, const void* value, bool bf16,
+                                 const int64_t* slots, int64_t num_tokens, void* k_cache,
+                                 void* v_cache, int64_t num_blocks, int32_t block_size,
+                                 int64_t row_elems, float k_scale, float v_scale, int* err,
+                                 cudaStream_t st) {
+  const int64_t row_vecs = row_elems / 8;
+  const int threads = static_cast<int>(row_vecs < 256 ? ((row_vecs + 31) / 32) * 32 : 256);
+  auto kern = bf16 ? write_kv_e4m3_kernel<true> : write_kv_e4m3_kernel<false>;
+  kern<<<static_cast<unsigned>(num_tokens), threads, 0, st>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), slots,
+      static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), num_blocks * block_size,
+      row_vecs, k_scale, v_scale, err);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,16 @@
 //    -inf and their V rows are zeroed in shared memory before PV, so stale or
 //    NaN bytes in the pool never enter the result.
 //
+// FP8 caches (E4M3 codes, one scale per layer for K and one for V): a stage
+// row is D bytes instead of 2D, so one 128-byte swizzled line holds 128 head-dim
+// elements. Codes are widened exactly to fp16/bf16 in registers: for S^T the
+// MMA's reduction index k is mapped to head-dim elements four at a time
+// (lane quad t reads dims 4t..4t+3 of its rows with one 32-bit load, q is
+// loaded with the same order); for O^T two token rows' words are byte-permuted
+// into (token, token+1) pairs and the head-dim rows of two m16 tiles
+// interleave (acc_dim gives each accumulator's dim). k_scale folds into the
+// logit scale, v_scale multiplies the output.
+//
 // decode_kernel: one CTA per (sequence, KV head, partition); its 4 warps take
 // the partition's stages round-robin and merge through shared memory at the
 // end; the CTA writes the output (one partition) or (m, l, o) partials that
@@ -46,6 +56,22 @@
 namespace pa {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+// Element layout of a cache: 16-bit values or 8-bit E4M3 codes. A "piece" is
+// the run of head-dim elements in one 128-byte line (one TMA box column).
+template <bool FP8>
+struct KvLayout {
+  static constexpr int kBytes = FP8 ? 1 : 2;
+  static constexpr int kPieceElems = 128 / kBytes;
+};
+
+// Head-dim index of accumulator element r of O^T tile dm held by lane group
+// gid (rows gid and gid + 8 of the m16 tile).
+template <bool FP8>
+__device__ __forceinline__ int acc_dim(int dm, int gid, int r) {
+  if constexpr (FP8) return ((dm >> 1) << 5) + (gid << 2) + ((dm & 1) << 1) + (r >> 1);
+  return dm * 16 + gid + ((r >> 1) << 3);
+}
 
 // Sequence length after range checks; out-of-range lengths are clamped and
 // reported once.
@@ -174,9 +200,9 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, int n, SlotFn sl
   }
 }
 
-template <int D, int NT, int NS>
+template <int D, int NT, int NS, bool FP8>
 struct DecodeSmem {
-  static constexpr int kHalves = D / 64;                  // 128-byte column pieces of a row
+  static constexpr int kHalves = D / KvLayout<FP8>::kPieceElems;  // 128-byte column pieces of a row
   static constexpr int kHalfBytes = kStageRows * 128;     // one piece of 16 rows
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K then V
   static constexpr int kRingBytes = kDecodeWarps * NS * kStageBytes;
@@ -220,8 +246,10 @@ struct Acc {
 };
 
 // q of the group of KV head kvh as the B operand of S^T = K Q^T
-// (k = head-dim index, n = head within the tile); heads past g are zero.
-template <int D, int NT>
+// (k = head-dim index, n = head within the tile); heads past g are zero. For
+// FP8 caches, lane quad t takes dims 16kk + 4t .. + 3 of k-step kk, the order
+// in which compute_stage reads the codes.
+template <int D, int NT, bool FP8>
 __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int lane,
                                        uint32_t (&qb)[NT][D / 16][2]) {
   const int gid = lane >> 2;
@@ -235,8 +263,10 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int 
         (static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group + head) * D;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      qb[nt][kk][0] = live ? __ldg(q32 + ((row + kk * 16 + tig * 2) >> 1)) : 0u;
-      qb[nt][kk][1] = live ? __ldg(q32 + ((row + kk * 16 + 8 + tig * 2) >> 1)) : 0u;
+      const int64_t d0 = FP8 ? kk * 16 + tig * 4 : kk * 16 + tig * 2;
+      const int64_t d1 = FP8 ? d0 + 2 : d0 + 8;
+      qb[nt][kk][0] = live ? __ldg(q32 + ((row + d0) >> 1)) : 0u;
+      qb[nt][kk][1] = live ? __ldg(q32 + ((row + d1) >> 1)) : 0u;
     }
   }
 }
@@ -246,12 +276,13 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int 
 // into the stage at shared address `stage`, completing on mbarrier `bar`.
 // Stores the stage's valid-row mask (bit r = row r holds a token < tok_end of
 // a block with a valid id) to *mask. Called by the whole warp.
-template <int D>
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk,
                                             const CUtensorMap* tmv, int64_t table_row, int kvh,
                                             int t0, int tok_end, uint32_t stage, uint32_t bar,
                                             uint32_t* mask, int lane) {
-  constexpr int HALVES = D / 64;
+  constexpr int PE = KvLayout<FP8>::kPieceElems;
+  constexpr int HALVES = D / PE;
   constexpr int HB = kStageRows * 128;
   int blk = 0;
   int off = 0;
@@ -277,7 +308,8 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
   const uint32_t rowmask = __ballot_sync(0xffffffffu, rv) & ((1u << kStageRows) - 1u);
   if (lane == 0) {
     *mask = rowmask;
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * a.tok_per_op * D * 4u);
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * a.tok_per_op * D * 2u *
+                                   KvLayout<FP8>::kBytes);
   }
   __syncwarp();
   if (ok) {
@@ -285,8 +317,8 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
     const uint32_t dv = dk + HALVES * HB;
 #pragma unroll
     for (int c = 0; c < HALVES; ++c) {
-      tma_load_4d(dk + c * HB, tmk, bar, c * 64, kvh, off, blk);
-      tma_load_4d(dv + c * HB, tmv, bar, c * 64, kvh, off, blk);
+      tma_load_4d(dk + c * HB, tmk, bar, c * PE, kvh, off, blk);
+      tma_load_4d(dv + c * HB, tmv, bar, c * PE, kvh, off, blk);
     }
   }
 }
@@ -324,15 +356,16 @@ struct GroupView {
 // Folds one loaded stage into the warp's softmax state. `sv` (a WarpView or
 // GroupView) places the warp's rows; `smem_base` / `smem_base_ptr` are one shared address and its
 // generic pointer, used to zero masked V rows.
-template <bool IS_BF16, int D, int NT, bool SPLIT_P, class View>
+template <bool IS_BF16, int D, int NT, bool SPLIT_P, bool FP8, class View>
 __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
                                               uint8_t* smem_base_ptr, uint32_t rowmask,
                                               const uint32_t (&qb)[NT][D / 16][2],
                                               Acc<D, NT>& acc, float scale_log2, int lane) {
   constexpr int TS = kStageRows;
   constexpr int KD = D / 16;
-  constexpr int HALVES = D / 64;
+  constexpr int HALVES = D / KvLayout<FP8>::kPieceElems;
   const int gid = lane >> 2;
+  const int tig = lane & 3;
 
   if (rowmask != (1u << TS) - 1u) {  // zero V rows that must not contribute
     for (int idx = lane; idx < TS * HALVES * 8; idx += 32) {
@@ -350,7 +383,21 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
   float sacc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-  {
+  if constexpr (FP8) {
+    // rows gid and gid + 8, dims 16kk + 4tig .. + 3: one 32-bit load per row
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk) {
+      const uint32_t col = ((((kk & 7) ^ (gid & 7)) << 4) + (tig << 2));
+      const uint32_t base = sv.k + (kk >> 3) * View::half_stride + col;
+      const uint32_t w0 = lds_u32(base + sv.row(gid));
+      const uint32_t w1 = lds_u32(base + sv.row(gid + 8));
+      uint32_t af[4];
+      e4m3x4_widen<IS_BF16>(w0, af[0], af[2]);
+      e4m3x4_widen<IS_BF16>(w1, af[1], af[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816<IS_BF16>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+    }
+  } else {
     const int i = lane >> 3;
     const int row = ((i & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -413,7 +460,36 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
   }
 
   // O^T += V^T P^T over the 16 tokens of the stage.
-  {
+  if constexpr (FP8) {
+    // dims 32dp + 4gid .. + 3 of tokens 2tig, 2tig + 1, 2tig + 8, 2tig + 9; the
+    // byte pairs (token, token + 1) of each dim form the A operands of tiles
+    // 2dp (dims +0 / +1 in rows gid / gid + 8) and 2dp + 1 (dims +2 / +3).
+    const int t0 = tig * 2;
+#pragma unroll
+    for (int dp = 0; dp < D / 32; ++dp) {
+      const uint32_t chunk = static_cast<uint32_t>(((dp & 3) << 1) + (gid >> 2));
+      const uint32_t base = sv.v + (dp >> 2) * View::half_stride + ((gid & 3) << 2);
+      const uint32_t w0 = lds_u32(base + sv.row(t0) + ((chunk ^ (t0 & 7)) << 4));
+      const uint32_t w1 = lds_u32(base + sv.row(t0 + 1) + ((chunk ^ ((t0 + 1) & 7)) << 4));
+      const uint32_t w8 = lds_u32(base + sv.row(t0 + 8) + ((chunk ^ (t0 & 7)) << 4));
+      const uint32_t w9 = lds_u32(base + sv.row(t0 + 9) + ((chunk ^ ((t0 + 1) & 7)) << 4));
+      uint32_t fa[4];
+      uint32_t fb[4];
+      e4m3x4_widen<IS_BF16>(prmt(w0, w1, 0x5140u), fa[0], fa[1]);
+      e4m3x4_widen<IS_BF16>(prmt(w8, w9, 0x5140u), fa[2], fa[3]);
+      e4m3x4_widen<IS_BF16>(prmt(w0, w1, 0x7362u), fb[0], fb[1]);
+      e4m3x4_widen<IS_BF16>(prmt(w8, w9, 0x7362u), fb[2], fb[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816<IS_BF16>(acc.o[2 * dp][nt], fa, bh[nt][0], bh[nt][1]);
+        mma16816<IS_BF16>(acc.o[2 * dp + 1][nt], fb, bh[nt][0], bh[nt][1]);
+        if constexpr (SPLIT_P) {
+          mma16816<IS_BF16>(acc.o[2 * dp][nt], fa, bl[nt][0], bl[nt][1]);
+          mma16816<IS_BF16>(acc.o[2 * dp + 1][nt], fb, bl[nt][0], bl[nt][1]);
+        }
+      }
+    }
+  } else {
     const int i = lane >> 3;
     const int row = ((i >> 1) << 3) + (lane & 7);
 #pragma unroll
@@ -434,11 +510,11 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
 // ============================================================================
 // One CTA per (sequence, KV head, partition).
 
-template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P>
+template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P, bool FP8>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
-  using S = DecodeSmem<D, NT, NS>;
+  using S = DecodeSmem<D, NT, NS, FP8>;
   constexpr int W = kDecodeWarps;
   constexpr int KD = D / 16;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -468,7 +544,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int my_n = nst > warp ? (nst - warp - 1) / W + 1 : 0;
 
   uint32_t qb[NT][KD][2];
-  load_q<D, NT>(a, s, kvh, lane, qb);
+  load_q<D, NT, FP8>(a, s, kvh, lane, qb);
 
   const uint32_t bar0 = sm_base + S::kBarOffset + warp * NS * 8;
   if (lane == 0) {
@@ -483,8 +559,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
   auto issue = [&](int it) {
     const int slot = it % NS;
-    issue_stage<D>(a, &tmk, &tmv, table_row, kvh, tok_begin + (warp + it * W) * tt, tok_end,
-                   ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
+    issue_stage<D, FP8>(a, &tmk, &tmv, table_row, kvh, tok_begin + (warp + it * W) * tt, tok_end,
+                        ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
   };
 
   Acc<D, NT> acc;
@@ -501,10 +577,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       aborted = true;
       break;
     }
-    compute_stage<IS_BF16, D, NT, SPLIT_P>(warp_stage_view(ring + slot * S::kStageBytes, D / 64),
-                                           ring + slot * S::kStageBytes,
-                                           ring_ptr + slot * S::kStageBytes, masks[slot], qb, acc,
-                                           a.scale_log2, lane);
+    compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(
+        warp_stage_view(ring + slot * S::kStageBytes, S::kHalves), ring + slot * S::kStageBytes,
+        ring_ptr + slot * S::kStageBytes, masks[slot], qb, acc, a.scale_log2, lane);
     fence_proxy_async_smem();  // our generic reads/writes of this slot precede the next TMA into it
     __syncwarp();
     if (it + NS < my_n) issue(it + NS);
@@ -530,9 +605,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int d = dm * 16 + gid + ((r >> 1) << 3);
+        const int d = acc_dim<FP8>(dm, gid, r);
         const int col = nt * 8 + tig * 2 + (r & 1);
-        c_o[(warp * COLS + col) * D + d] = acc.o[dm][nt][r];
+        c_o[(warp * COLS + col) * D + d] = FP8 ? acc.o[dm][nt][r] * a.v_scale : acc.o[dm][nt][r];
       }
     }
   }
@@ -678,7 +753,7 @@ __device__ __forceinline__ void build_line_prefix(const DecodeArgs& a, int32_t* 
 // normalised and written; otherwise the warp leaves an (m, l, o) partial in
 // slot (range * H_kv + kvh) * 2 + (0: its first piece, 1: its last) and the
 // last contributor to arrive merges the piece.
-template <int D, int NT>
+template <int D, int NT, bool FP8>
 __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& acc, int s, int ps,
                                              int pe, int g0, int g1, int64_t stot, int64_t ranges,
                                              int64_t range, int kvh, int lane) {
@@ -698,9 +773,10 @@ __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& ac
         for (int r = 0; r < 4; ++r) {
           const int col = nt * 8 + tig * 2 + (r & 1);
           if (col < a.group) {
-            const int d = dm * 16 + gid + ((r >> 1) << 3);
+            const int d = acc_dim<FP8>(dm, gid, r);
             const float l = acc.l[nt][r & 1];
-            store_out(a, (row0 + col) * D + d, l > 0.f ? acc.o[dm][nt][r] / l : 0.f);
+            const float o = FP8 ? acc.o[dm][nt][r] * a.v_scale : acc.o[dm][nt][r];
+            store_out(a, (row0 + col) * D + d, l > 0.f ? o / l : 0.f);
           }
         }
       }
@@ -717,7 +793,9 @@ __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& ac
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int col = nt * 8 + tig * 2 + (r & 1);
-          if (col < a.group) po[col * D + dm * 16 + gid + ((r >> 1) << 3)] = acc.o[dm][nt][r];
+          if (col < a.group)
+            po[col * D + acc_dim<FP8>(dm, gid, r)] =
+                FP8 ? acc.o[dm][nt][r] * a.v_scale : acc.o[dm][nt][r];
         }
       }
     }
@@ -768,11 +846,11 @@ __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& ac
 
 }
 
-template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P>
+template <bool IS_BF16, int D, int NT, int NS, bool SPLIT_P, bool FP8>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_balanced_kernel(const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
-  using S = DecodeSmem<D, NT, NS>;
+  using S = DecodeSmem<D, NT, NS, FP8>;
   constexpr int W = kDecodeWarps;
   constexpr int KD = D / 16;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -825,15 +903,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   Cursor cc = ic;                     // stage being computed
   auto issue = [&](int it) {
     const int slot = it % NS;
-    issue_stage<D>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, kvh, ic.j * tt,
-                   ic.len, ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
+    issue_stage<D, FP8>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, kvh, ic.j * tt,
+                        ic.len, ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
     cursor_next(a, pre, ic);
   };
   const int pro = count < NS ? count : NS;
   for (int i = 0; i < pro; ++i) issue(i);
 
   uint32_t qb[NT][KD][2];
-  load_q<D, NT>(a, cc.s, kvh, lane, qb);
+  load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
   Acc<D, NT> acc;
   acc.reset();
   bool aborted = false;
@@ -851,9 +929,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
     }
     if (!aborted) {
-      compute_stage<IS_BF16, D, NT, SPLIT_P>(
-          warp_stage_view(ring + slot * S::kStageBytes, D / 64), ring, ring_ptr, masks[slot], qb,
-          acc, a.scale_log2, lane);
+      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(
+          warp_stage_view(ring + slot * S::kStageBytes, S::kHalves), ring, ring_ptr, masks[slot],
+          qb, acc, a.scale_log2, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (it + NS < count) issue(it + NS);
@@ -867,11 +945,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     // ---- the warp is done with its share of piece (cc.s, kvh)
     if (aborted) acc.reset();  // contribute nothing, but still take part
-    finish_piece<D, NT>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, grp, kvh, lane);
+    finish_piece<D, NT, FP8>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, grp, kvh,
+                             lane);
 
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
-      load_q<D, NT>(a, cc.s, kvh, lane, qb);
+      load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
       acc.reset();
     }
   }
@@ -880,37 +959,38 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 // ============================================================================
 // launch helpers
 
-// Stages per warp: keeps 2 CTAs (8 warps) resident per SM for D <= 128.
-template <int D>
+// Stages per warp: keeps 2 CTAs (8 warps) resident per SM for D <= 128. FP8
+// stages are half the bytes, so twice as many keep the same bytes in flight.
+template <int D, bool FP8>
 constexpr int decode_stages() {
-  return D == 64 ? 6 : (D == 128 ? 3 : 2);
+  return (D == 64 ? 6 : (D == 128 ? 3 : 2)) * (FP8 ? 2 : 1);
 }
 
-template <bool IS_BF16, int D, int NT>
+template <bool IS_BF16, int D, int NT, bool FP8>
 cudaError_t launch_decode_tiles(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                                 dim3 grid, bool balanced, cudaStream_t st) {
-  constexpr int NS = decode_stages<D>();
-  using S = DecodeSmem<D, NT, NS>;
+  constexpr int NS = decode_stages<D, FP8>();
+  using S = DecodeSmem<D, NT, NS, FP8>;
   if (balanced) {
-    auto kern = decode_balanced_kernel<IS_BF16, D, NT, NS, true>;
+    auto kern = decode_balanced_kernel<IS_BF16, D, NT, NS, true, FP8>;
     const int smem = S::kTotal + (a.num_seqs + 1) * 4;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kDecodeWarps * 32, smem, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
-  auto kern = decode_kernel<IS_BF16, D, NT, NS, true>;
+  auto kern = decode_kernel<IS_BF16, D, NT, NS, true, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
   if (e != cudaSuccess) return e;
   kern<<<grid, kDecodeWarps * 32, S::kTotal, st>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
-template <bool IS_BF16, int D>
+template <bool IS_BF16, int D, bool FP8>
 cudaError_t launch_decode_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                                    int group_tiles, dim3 grid, bool balanced, cudaStream_t st) {
-  if (group_tiles == 1) return launch_decode_tiles<IS_BF16, D, 1>(tk, tv, a, grid, balanced, st);
-  if (group_tiles == 2) return launch_decode_tiles<IS_BF16, D, 2>(tk, tv, a, grid, balanced, st);
+  if (group_tiles == 1) return launch_decode_tiles<IS_BF16, D, 1, FP8>(tk, tv, a, grid, balanced, st);
+  if (group_tiles == 2) return launch_decode_tiles<IS_BF16, D, 2, FP8>(tk, tv, a, grid, balanced, st);
   return cudaErrorInvalidValue;
 }
 

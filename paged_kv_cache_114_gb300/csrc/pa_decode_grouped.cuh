@@ -19,6 +19,10 @@
 //
 // Partials, counters and merges are those of the balanced kernel: warp slot
 // (range * H_kv + kv_head), last arriver merges.
+//
+// FP8 caches: a 128-byte line holds 128 head-dim codes, so a box is 128 x 16
+// tokens x HG heads and a stage is half the bytes; the ring has twice the
+// stages to keep the same bytes in flight.
 #pragma once
 
 #include "pa_decode.cuh"
@@ -26,9 +30,9 @@
 namespace pa {
 
 // Shared-memory plan of the grouped kernel for head group HG (runtime).
-template <int D, int NS>
+template <int D, int NS, bool FP8>
 struct GroupedSmem {
-  static constexpr int kHalves = D / 64;
+  static constexpr int kHalves = D / KvLayout<FP8>::kPieceElems;
   __host__ __device__ static constexpr uint32_t half_bytes(int hg) { return hg * kStageRows * 128u; }
   __host__ __device__ static constexpr uint32_t stage_bytes(int hg) { return 2u * kHalves * half_bytes(hg); }
   __host__ __device__ static constexpr uint32_t bar_offset(int hg) { return NS * stage_bytes(hg); }
@@ -44,13 +48,14 @@ struct GroupedSmem {
 // table_row, clipped at tok_end) for KV heads [head0, head0 + hg): one box per
 // block piece and column half, for K and for V, all completing on `bar`.
 // Lane j handles the j-th block piece. Stores the valid-row mask to *mask.
-template <int D>
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUtensorMap* tmk,
                                                   const CUtensorMap* tmv, int64_t table_row,
                                                   int head0, int hg, int t0, int tok_end,
                                                   uint32_t stage, uint32_t half_bytes, uint32_t bar,
                                                   uint32_t* mask, int lane) {
-  constexpr int HALVES = D / 64;
+  constexpr int PE = KvLayout<FP8>::kPieceElems;
+  constexpr int HALVES = D / PE;
   const int tpo = a.tok_per_op;  // 8 or 16 here: a multiple of 8, no padding rows
   int blk = 0;
   int off = 0;
@@ -75,7 +80,8 @@ __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUt
   const uint32_t rowmask = __ballot_sync(0xffffffffu, rv) & ((1u << kStageRows) - 1u);
   if (lane == 0) {
     *mask = rowmask;
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * tpo * hg * D * 4u);
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * tpo * hg * D * 2u *
+                                   KvLayout<FP8>::kBytes);
   }
   __syncwarp();
   if (ok) {
@@ -83,8 +89,8 @@ __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUt
     const uint32_t dv = dk + HALVES * half_bytes;
 #pragma unroll
     for (int c = 0; c < HALVES; ++c) {
-      tma_load_4d(dk + c * half_bytes, tmk, bar, c * 64, off, head0, blk);
-      tma_load_4d(dv + c * half_bytes, tmv, bar, c * 64, off, head0, blk);
+      tma_load_4d(dk + c * half_bytes, tmk, bar, c * PE, off, head0, blk);
+      tma_load_4d(dv + c * half_bytes, tmv, bar, c * PE, off, head0, blk);
     }
   }
 }
@@ -96,13 +102,13 @@ __host__ __device__ constexpr int max_head_group(int d, int nt) { return (d > 12
 
 // Grid: ranges x (H_kv / HG) CTAs of HG + 1 warps; CTA c takes range c / nhg
 // and head group c % nhg, so the head groups of one range run side by side.
-template <bool IS_BF16, int D, int NT, int NS, int HG, int TPO, bool SPLIT_P>
+template <bool IS_BF16, int D, int NT, int NS, int HG, int TPO, bool SPLIT_P, bool FP8>
 __global__ void __launch_bounds__((HG + 1) * 32, 1)
     decode_grouped_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
-  using S = GroupedSmem<D, NS>;
+  using S = GroupedSmem<D, NS, FP8>;
   constexpr int KD = D / 16;
-  constexpr int HALVES = D / 64;
+  constexpr int HALVES = S::kHalves;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int warp_tot[16];
 
@@ -164,9 +170,9 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
           break;
         }
       }
-      issue_group_stage<D>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, head0, hg,
-                           ic.j * tt, ic.len, sm_base + slot * stage_bytes, half_bytes,
-                           full0 + 8 * slot, masks + slot, lane);
+      issue_group_stage<D, FP8>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, head0,
+                                hg, ic.j * tt, ic.len, sm_base + slot * stage_bytes, half_bytes,
+                                full0 + 8 * slot, masks + slot, lane);
       cursor_next(a, pre, ic);
     }
     // the last stages' copies complete before the producer leaves
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
 
   Cursor cc = cursor_at(a, pre, g0);
   uint32_t qb[NT][KD][2];
-  load_q<D, NT>(a, cc.s, kvh, lane, qb);
+  load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
   Acc<D, NT> acc;
   acc.reset();
   bool aborted = false;
@@ -199,9 +205,9 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
     if (!aborted) {
       sv.k = sm_base + slot * stage_bytes;
       sv.v = sv.k + HALVES * half_bytes;
-      compute_stage<IS_BF16, D, NT, SPLIT_P>(sv, sm_base, sm, masks[slot], qb, acc, a.scale_log2,
-                                             lane);
-      static_assert(GroupView<HG, TPO>::half_stride == GroupedSmem<D, NS>::half_bytes(HG), "layout");
+      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(sv, sm_base, sm, masks[slot], qb, acc,
+                                                  a.scale_log2, lane);
+      static_assert(GroupView<HG, TPO>::half_stride == S::half_bytes(HG), "layout");
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
@@ -213,28 +219,29 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
       continue;
     }
     if (aborted) acc.reset();  // contribute nothing, but still take part
-    finish_piece<D, NT>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, range, kvh, lane);
+    finish_piece<D, NT, FP8>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, range, kvh,
+                             lane);
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
-      load_q<D, NT>(a, cc.s, kvh, lane, qb);
+      load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
       acc.reset();
     }
   }
 }
 
 // Stages in the shared ring: 64 KB stages for HG = 8 at D = 128 (HG = 4 at
-// D = 256), three of them.
-template <int D>
+// D = 256), three of them; six of the 32 KB FP8 stages.
+template <int D, bool FP8>
 constexpr int grouped_stages() {
-  return 3;
+  return FP8 ? 6 : 3;
 }
 
-template <bool IS_BF16, int D, int NT, int HG, int TPO>
+template <bool IS_BF16, int D, int NT, int HG, int TPO, bool FP8>
 cudaError_t launch_grouped(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                            dim3 grid, cudaStream_t st) {
-  constexpr int NS = grouped_stages<D>();
-  using S = GroupedSmem<D, NS>;
-  auto kern = decode_grouped_kernel<IS_BF16, D, NT, NS, HG, TPO, true>;
+  constexpr int NS = grouped_stages<D, FP8>();
+  using S = GroupedSmem<D, NS, FP8>;
+  auto kern = decode_grouped_kernel<IS_BF16, D, NT, NS, HG, TPO, true, FP8>;
   const int smem = static_cast<int>(S::total(HG, a.num_seqs));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -244,19 +251,19 @@ cudaError_t launch_grouped(const CUtensorMap& tk, const CUtensorMap& tv, const D
 
 // Head groups of 8 (4 where max_head_group says so) and of 4; boxes of 16
 // tokens (blocks of 16 or more) or 8 (blocks of 8).
-template <bool IS_BF16, int D, int NT>
+template <bool IS_BF16, int D, int NT, bool FP8>
 cudaError_t launch_grouped_tiles(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                                  int head_group, dim3 grid, cudaStream_t st) {
   if (head_group > max_head_group(D, NT)) return cudaErrorInvalidValue;
   if constexpr (max_head_group(D, NT) >= 8) {
     if (head_group == 8) {
-      return a.tok_per_op == 16 ? launch_grouped<IS_BF16, D, NT, 8, 16>(tk, tv, a, grid, st)
-                                : launch_grouped<IS_BF16, D, NT, 8, 8>(tk, tv, a, grid, st);
+      return a.tok_per_op == 16 ? launch_grouped<IS_BF16, D, NT, 8, 16, FP8>(tk, tv, a, grid, st)
+                                : launch_grouped<IS_BF16, D, NT, 8, 8, FP8>(tk, tv, a, grid, st);
     }
   }
   if (head_group == 4) {
-    return a.tok_per_op == 16 ? launch_grouped<IS_BF16, D, NT, 4, 16>(tk, tv, a, grid, st)
-                              : launch_grouped<IS_BF16, D, NT, 4, 8>(tk, tv, a, grid, st);
+    return a.tok_per_op == 16 ? launch_grouped<IS_BF16, D, NT, 4, 16, FP8>(tk, tv, a, grid, st)
+                              : launch_grouped<IS_BF16, D, NT, 4, 8, FP8>(tk, tv, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }

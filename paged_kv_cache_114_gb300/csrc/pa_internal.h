@@ -30,7 +30,8 @@ struct DecodeArgs {
   int32_t slot_rows;             // shared-memory rows reserved per box: max(tok_per_op, 8)
   int32_t ops_per_stage;         // boxes per 16-row stage
   int32_t out_dtype;             // pa_dtype
-  float scale_log2;              // scale * log2(e)
+  float scale_log2;              // scale * log2(e) (times k_scale for E4M3 caches)
+  float v_scale;                 // E4M3 caches: V code c stands for value(c) * v_scale
 };
 
 // Rows of shared memory one pipeline stage holds (one m16 tile of tokens).
@@ -62,6 +63,19 @@ cudaError_t launch_decode_bf16_128(const CUtensorMap& tk, const CUtensorMap& tv,
 cudaError_t launch_decode_bf16_256(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                                    int group_tiles, int head_group, dim3 grid, int kernel,
                                   cudaStream_t st);
+// E4M3 caches (q and outputs fp16 or bf16), head_dim 128 and 256.
+cudaError_t launch_decode_e4m3_f16_128(const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const DecodeArgs& a, int group_tiles, int head_group,
+                                       dim3 grid, int kernel, cudaStream_t st);
+cudaError_t launch_decode_e4m3_f16_256(const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const DecodeArgs& a, int group_tiles, int head_group,
+                                       dim3 grid, int kernel, cudaStream_t st);
+cudaError_t launch_decode_e4m3_bf16_128(const CUtensorMap& tk, const CUtensorMap& tv,
+                                        const DecodeArgs& a, int group_tiles, int head_group,
+                                        dim3 grid, int kernel, cudaStream_t st);
+cudaError_t launch_decode_e4m3_bf16_256(const CUtensorMap& tk, const CUtensorMap& tv,
+                                        const DecodeArgs& a, int group_tiles, int head_group,
+                                        dim3 grid, int kernel, cudaStream_t st);
 
 // Balanced mode: resident CTAs per SM of the per-warp-range kernel, the
 // largest batch whose per-sequence offsets fit shared memory, and the partial
@@ -101,6 +115,12 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t num_seqs, i
 cudaError_t launch_write_kv(const void* key, const void* value, const int64_t* slots,
                             int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
                             int32_t block_size, int64_t row_bytes, int* err, cudaStream_t st);
+// Quantising write into E4M3 caches; row_elems = H_kv * D, a multiple of 8.
+cudaError_t launch_write_kv_e4m3(const void* key, const void* value, bool bf16,
+                                 const int64_t* slots, int64_t num_tokens, void* k_cache,
+                                 void* v_cache, int64_t num_blocks, int32_t block_size,
+                                 int64_t row_elems, float k_scale, float v_scale, int* err,
+                                 cudaStream_t st);
 
 constexpr int kMaxCopyLayers = 64;
 struct CopyLayers {

@@ -1,10 +1,12 @@
 // pa_ptx.cuh - thin inline-PTX wrappers used by the sm_103a kernels:
-// mbarrier phases, TMA tensor loads, ldmatrix, mma.sync m16n8k16, movmatrix.
+// mbarrier phases, TMA tensor loads, ldmatrix, mma.sync m16n8k16, movmatrix,
+// and the E4M3 widening of FP8 cache codes.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -149,6 +151,47 @@ __device__ __forceinline__ float2 unpack2(uint32_t x) {
     __half2 v = *reinterpret_cast<__half2*>(&x);
     return __half22float2(v);
   }
+}
+
+// 32-bit shared-memory load.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Byte permute: result byte i = byte sel_i of the 8-byte pair (hi:lo).
+__device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
+  return r;
+}
+
+// Widens the four E4M3 codes of a 32-bit word into two packed pairs of 16-bit
+// MMA operands: lo <- bytes 0 (low half), 1 (high half); hi <- bytes 2, 3.
+// Every E4M3 value is exact in fp16 and in bf16, so the widening is exact.
+template <bool IS_BF16>
+__device__ __forceinline__ void e4m3x4_widen(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu),
+                                                   __NV_E4M3);
+  const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16),
+                                                   __NV_E4M3);
+  if constexpr (IS_BF16) {
+    const float2 fa = __half22float2(__half2(a));
+    const float2 fb = __half22float2(__half2(b));
+    lo = pack2<true>(fa.x, fa.y);
+    hi = pack2<true>(fb.x, fb.y);
+  } else {
+    lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
+    hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+  }
+}
+
+// Encodes two floats as E4M3 codes (x -> low byte, y -> high byte): nearest
+// code, ties to even, saturating at +-448.
+__device__ __forceinline__ uint16_t e4m3x2_encode(float x, float y) {
+  return static_cast<uint16_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3));
 }
 
 }  // namespace pa

@@ -15,6 +15,12 @@ import torch
 from . import _lib
 
 _DTYPES = {torch.float16: _lib.PA_F16, torch.bfloat16: _lib.PA_BF16, torch.float32: _lib.PA_F32}
+# Storage types of an E4M3 cache: raw bytes, or torch's own float8 type.
+FP8_CACHE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def is_fp8_cache(t: torch.Tensor) -> bool:
+    return t.dtype in FP8_CACHE_DTYPES
 
 
 def _stream(device: torch.device) -> ctypes.c_void_p:
@@ -39,14 +45,37 @@ def _cuda(*ts: torch.Tensor) -> torch.device:
     return dev
 
 
-def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> _lib.PaCache:
-    """pa_cache for one layer's pool, k/v shaped [num_blocks, block_size, H_kv, D]."""
+def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+               act_dtype: Optional[torch.dtype] = None, k_scale: Optional[float] = None,
+               v_scale: Optional[float] = None) -> _lib.PaCache:
+    """pa_cache for one layer's pool, k/v shaped [num_blocks, block_size, H_kv, D].
+
+    16-bit caches (float16 / bfloat16) take no other argument. E4M3 caches
+    (uint8 or float8_e4m3fn codes) take ``act_dtype`` (the dtype of q, key and
+    value) and the layer's ``k_scale`` / ``v_scale``: a code c stands for
+    value(c) * scale.
+    """
     _cuda(k_cache, v_cache)
     _need(k_cache.dim() == 4 and k_cache.shape == v_cache.shape, "k/v caches: [NB, b, H_kv, D], same shape")
-    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in (torch.float16, torch.bfloat16),
-          "caches must both be float16 or both bfloat16")
     nb, b, hkv, d = k_cache.shape
-    return _lib.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, b, hkv, d, _DTYPES[k_cache.dtype])
+    if is_fp8_cache(k_cache):
+        _need(is_fp8_cache(v_cache), "caches must both be E4M3 codes")
+        _need(act_dtype in (torch.float16, torch.bfloat16), "E4M3 caches: act_dtype float16 or bfloat16")
+        _need(k_scale is not None and v_scale is not None, "E4M3 caches need k_scale and v_scale")
+        return _lib.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, b, hkv, d,
+                            _lib.PA_FP8_E4M3, _DTYPES[act_dtype], float(k_scale), float(v_scale))
+    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in (torch.float16, torch.bfloat16),
+          "caches must both be float16, both bfloat16 or both E4M3 codes")
+    code = _DTYPES[k_cache.dtype]
+    return _lib.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, b, hkv, d, code, code, 1.0, 1.0)
+
+
+def _check_act(t: torch.Tensor, k_cache: torch.Tensor, what: str) -> None:
+    if is_fp8_cache(k_cache):
+        _need(t.dtype in (torch.float16, torch.bfloat16),
+              f"{what} must be float16 or bfloat16 with an E4M3 cache")
+    else:
+        _need(t.dtype == k_cache.dtype, f"{what} dtype must match the cache")
 
 
 def slot_mapping(block_tables: torch.Tensor, seq_idx: torch.Tensor, positions: torch.Tensor,
@@ -68,14 +97,19 @@ def slot_mapping(block_tables: torch.Tensor, seq_idx: torch.Tensor, positions: t
 
 
 def write_kv(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
-             k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
-    """k_cache/v_cache row at each slot <- the token's key/value rows (in place)."""
+             k_cache: torch.Tensor, v_cache: torch.Tensor, *, k_scale: Optional[float] = None,
+             v_scale: Optional[float] = None) -> None:
+    """k_cache/v_cache row at each slot <- the token's key/value rows (in place).
+
+    E4M3 caches store e4m3(x / k_scale) and e4m3(x / v_scale) of the float16 /
+    bfloat16 rows."""
     dev = _cuda(key, value, slot_mapping, k_cache, v_cache)
     _need(key.shape == value.shape and key.dim() == 3, "key/value: [T, H_kv, D]")
     _need(key.shape[1:] == k_cache.shape[2:], "key/value rows must match the cache's [H_kv, D]")
-    _need(key.dtype == k_cache.dtype == value.dtype, "key/value dtype must match the cache")
+    _need(key.dtype == value.dtype, "key and value must share a dtype")
+    _check_act(key, k_cache, "key/value")
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == key.shape[:1], "slot_mapping: int64 [T]")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, act_dtype=key.dtype, k_scale=k_scale, v_scale=v_scale)
     st = _lib.lib().pa_write_kv(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
                                 ctypes.byref(cache), _stream(dev))
     _lib.check("pa_write_kv", st)
@@ -95,7 +129,9 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
     _need(len(k_caches) == len(v_caches) and len(k_caches) > 0, "one k and one v cache per layer")
     dev = _cuda(pairs, *k_caches, *v_caches)
     _need(pairs.dtype == torch.int64 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs: int64 [P, 2]")
-    arr = (_lib.PaCache * len(k_caches))(*[make_cache(k, v) for k, v in zip(k_caches, v_caches)])
+    fp8 = dict(act_dtype=torch.float16, k_scale=1.0, v_scale=1.0)  # codes are copied as bytes
+    arr = (_lib.PaCache * len(k_caches))(
+        *[make_cache(k, v, **(fp8 if is_fp8_cache(k) else {})) for k, v in zip(k_caches, v_caches)])
     st = _lib.lib().pa_copy_blocks(arr, len(k_caches), _ptr(pairs), pairs.shape[0], _stream(dev))
     _lib.check("pa_copy_blocks", st)
 
@@ -136,7 +172,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
            seq_lens: torch.Tensor, scale: float, *, max_seq_len: int,
            out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
            partition_tokens: Optional[int] = None,
-           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+           workspace: Optional[torch.Tensor] = None, k_scale: Optional[float] = None,
+           v_scale: Optional[float] = None) -> torch.Tensor:
     """Paged decode attention: out[s, h] over the first seq_lens[s] tokens of sequence s.
 
     ``max_seq_len`` bounds ``seq_lens`` (it sizes the launch, so the call never
@@ -145,11 +182,12 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     ``PA_PARTITION_BALANCED`` (-1) gives every warp an equal share of the
     work; None picks the library's default for this shape. The workspace,
     when a split needs one, comes from the caller (see :func:`new_workspace`)
-    or is allocated here.
+    or is allocated here. E4M3 caches take the layer's ``k_scale`` and
+    ``v_scale``; q is then float16 or bfloat16.
     """
     dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens)
     _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [N, Hq, D] with the cache's D")
-    _need(q.dtype == k_cache.dtype, "q dtype must match the cache")
+    _check_act(q, k_cache, "q")
     _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
           and block_tables.shape[0] == q.shape[0], "block_tables: int32 [N, maxB]")
     _need(seq_lens.dtype == torch.int32 and seq_lens.shape == (q.shape[0],), "seq_lens: int32 [N]")
@@ -165,7 +203,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
         workspace = new_workspace(n, hq, hkv, d, max_seq_len, partition_tokens, dev)
     if workspace is not None:
         _cuda(workspace, q)
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, act_dtype=q.dtype, k_scale=k_scale, v_scale=v_scale)
     st = _lib.lib().pa_decode(_ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables),
                               block_tables.shape[1], _ptr(seq_lens), int(max_seq_len), float(scale),
                               _ptr(out), _DTYPES[out.dtype], int(partition_tokens), _ptr(workspace),
@@ -187,7 +225,7 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
     """
     dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens, q_start)
     _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [T, Hq, D] with the cache's D")
-    _need(q.dtype == k_cache.dtype, "q dtype must match the cache")
+    _need(q.dtype == k_cache.dtype, "q dtype must match the cache (float16 or bfloat16 caches)")
     n = block_tables.shape[0]
     _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2, "block_tables: int32 [N, maxB]")
     _need(seq_lens.dtype == torch.int32 and seq_lens.shape == (n,), "seq_lens: int32 [N]")
@@ -209,7 +247,8 @@ def decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
                             max_seq_len: int, partition_tokens: int,
                             out: Optional[torch.Tensor] = None,
-                            out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
+                            out_dtype: Optional[torch.dtype] = None, k_scale: Optional[float] = None,
+                            v_scale: Optional[float] = None) -> torch.Tensor:
     """Decode like :func:`decode`, with the split-K partials kept in the library's
     fixed device array instead of a workspace from the caller.
 
@@ -220,7 +259,7 @@ def decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     """
     dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens)
     _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [N, Hq, D] with the cache's D")
-    _need(q.dtype == k_cache.dtype, "q dtype must match the cache")
+    _check_act(q, k_cache, "q")
     _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
           and block_tables.shape[0] == q.shape[0], "block_tables: int32 [N, maxB]")
     _need(seq_lens.dtype == torch.int32 and seq_lens.shape == (q.shape[0],), "seq_lens: int32 [N]")
@@ -229,7 +268,7 @@ def decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         out = torch.empty((n, hq, d), dtype=out_dtype or q.dtype, device=dev)
     _cuda(out, q)
     _need(out.shape == q.shape and out.dtype in _DTYPES, "out: [N, Hq, D] of float16/bfloat16/float32")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, act_dtype=q.dtype, k_scale=k_scale, v_scale=v_scale)
     st = _lib.lib().pa_decode_static_workspace(
         _ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), int(max_seq_len), float(scale), _ptr(out), _DTYPES[out.dtype],

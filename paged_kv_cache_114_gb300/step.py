@@ -18,7 +18,7 @@ from typing import Dict, Optional
 import torch
 
 from . import _lib
-from .ops import _DTYPES, _cuda, _need, default_partition, make_cache, new_workspace
+from .ops import _DTYPES, _cuda, _need, default_partition, is_fp8_cache, make_cache, new_workspace
 
 _ALIGN = 256  # bytes; every packed input starts on a 256-byte boundary
 
@@ -31,20 +31,24 @@ class DecodeStep:
     """slot_mapping -> write_kv -> decode over fixed device buffers.
 
     Device inputs are views into one staging buffer, laid out by
-    :meth:`layout`: ``q [N, Hq, D]``, ``key``/``value [T, H_kv, D]`` (cache
-    dtype), ``seq_idx``/``positions`` int32 ``[T]``, ``block_tables`` int32
-    ``[N, maxB]`` and ``seq_lens`` int32 ``[N]``. The caches, the output
-    (``[N, Hq, D]`` of ``out_dtype``) and the decode workspace are allocated or
-    passed once.
+    :meth:`layout`: ``q [N, Hq, D]``, ``key``/``value [T, H_kv, D]`` (the cache
+    dtype, or ``act_dtype`` for an E4M3 cache), ``seq_idx``/``positions`` int32
+    ``[T]``, ``block_tables`` int32 ``[N, maxB]`` and ``seq_lens`` int32
+    ``[N]``. The caches, the output (``[N, Hq, D]`` of ``out_dtype``) and the
+    decode workspace are allocated or passed once. E4M3 caches also take the
+    layer's ``k_scale`` and ``v_scale``.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, *, num_seqs: int,
                  num_q_heads: int, num_tokens: int, max_blocks_per_seq: int, max_seq_len: int,
                  scale: float, out_dtype: torch.dtype = torch.float32,
-                 partition_tokens: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None):
+                 partition_tokens: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None,
+                 act_dtype: Optional[torch.dtype] = None, k_scale: Optional[float] = None,
+                 v_scale: Optional[float] = None):
         dev = _cuda(k_cache, v_cache)
         self.device = dev
         self.k_cache, self.v_cache = k_cache, v_cache
+        self.act_dtype = act_dtype if is_fp8_cache(k_cache) else k_cache.dtype
         nb, b, hkv, d = k_cache.shape
         self.num_blocks, self.block_size = int(nb), int(b)
         _need(num_q_heads % hkv == 0, "num_q_heads must be a multiple of the cache's KV heads")
@@ -57,7 +61,7 @@ class DecodeStep:
         self.stream = stream if stream is not None else torch.cuda.Stream(dev)
         self.stream.wait_stream(torch.cuda.current_stream(dev))
         # one staging buffer for every per-step input
-        self.offsets, self.nbytes = self.layout(k_cache.dtype, **self.shape)
+        self.offsets, self.nbytes = self.layout(self.act_dtype, **self.shape)
         self.staging = torch.empty(self.nbytes, dtype=torch.uint8, device=dev)
         self.inputs = self._views(self.staging)
         self.slots = torch.empty(num_tokens, dtype=torch.int64, device=dev)
@@ -68,7 +72,8 @@ class DecodeStep:
         self.partition_tokens = int(partition_tokens)
         self.workspace = new_workspace(num_seqs, num_q_heads, int(hkv), int(d), self.max_seq_len,
                                        self.partition_tokens, dev)
-        self._cache = make_cache(k_cache, v_cache)
+        self._cache = make_cache(k_cache, v_cache, act_dtype=self.act_dtype, k_scale=k_scale,
+                                 v_scale=v_scale)
         lib = _lib.lib()
         st = ctypes.c_void_p(self.stream.cuda_stream)
         i = self.inputs
@@ -92,9 +97,9 @@ class DecodeStep:
     # ------------------------------------------------------------------ layout
 
     @staticmethod
-    def layout(cache_dtype: torch.dtype, *, N: int, Hq: int, Hkv: int, D: int, T: int, maxB: int):
+    def layout(act_dtype: torch.dtype, *, N: int, Hq: int, Hkv: int, D: int, T: int, maxB: int):
         """Byte offsets of each input in the staging buffer, and its size."""
-        esz = torch.tensor([], dtype=cache_dtype).element_size()
+        esz = torch.tensor([], dtype=act_dtype).element_size()
         sizes = [("q", N * Hq * D * esz), ("key", T * Hkv * D * esz), ("value", T * Hkv * D * esz),
                  ("seq_idx", T * 4), ("positions", T * 4), ("block_tables", N * maxB * 4),
                  ("seq_lens", N * 4)]
@@ -105,7 +110,7 @@ class DecodeStep:
         return offsets, pos
 
     def _views(self, buf: torch.Tensor) -> Dict[str, torch.Tensor]:
-        s, cdt = self.shape, self.k_cache.dtype
+        s, cdt = self.shape, self.act_dtype
         shapes = {"q": ((s["N"], s["Hq"], s["D"]), cdt), "key": ((s["T"], s["Hkv"], s["D"]), cdt),
                   "value": ((s["T"], s["Hkv"], s["D"]), cdt), "seq_idx": ((s["T"],), torch.int32),
                   "positions": ((s["T"],), torch.int32),

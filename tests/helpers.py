@@ -19,14 +19,29 @@ def to_dev(a: np.ndarray, dev, dtype: str = None) -> torch.Tensor:
 
 
 def bits_of(t: torch.Tensor) -> np.ndarray:
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    """Stored bits: uint16 patterns of a 16-bit tensor, bytes of an 8-bit one."""
+    t = t.detach().cpu().contiguous()
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def fp8_kw(w) -> dict:
+    """Scale keywords of the binding's calls for an E4M3 workload (else none)."""
+    return {"k_scale": w.k_scale, "v_scale": w.v_scale} if w.kv_dtype == "e4m3" else {}
+
+
+def cache_to_dev(w, dev):
+    """The workload's K and V pools on the device (uint8 codes for E4M3)."""
+    if w.kv_dtype == "e4m3":
+        return to_dev(w.k_cache, dev), to_dev(w.v_cache, dev)
+    return to_dev(w.k_cache, dev, w.dtype), to_dev(w.v_cache, dev, w.dtype)
 
 
 def gpu_scenario(w, dev, *, partition_tokens=None, out_dtype=torch.float32, pairs=None):
     """copy_blocks -> slot_mapping -> write_kv -> decode on the device."""
     import paged_kv_cache_114_gb300 as pa
-    k = to_dev(w.k_cache, dev, w.dtype)
-    v = to_dev(w.v_cache, dev, w.dtype)
+    k, v = cache_to_dev(w, dev)
     pairs = w.copy_pairs if pairs is None else pairs
     if len(pairs):
         pa.copy_blocks([k], [v], to_dev(np.asarray(pairs, dtype=np.int64), dev))
@@ -34,12 +49,14 @@ def gpu_scenario(w, dev, *, partition_tokens=None, out_dtype=torch.float32, pair
     slots = pa.slot_mapping(tables, to_dev(w.seq_idx, dev), to_dev(w.positions, dev),
                             w.block_size, w.num_blocks)
     if len(w.positions):
-        pa.write_kv(to_dev(w.key, dev, w.dtype), to_dev(w.value, dev, w.dtype), slots, k, v)
+        pa.write_kv(to_dev(w.key, dev, w.dtype), to_dev(w.value, dev, w.dtype), slots, k, v,
+                    **fp8_kw(w))
     # NaN-filled so a row the kernel fails to write cannot pass on stale memory
     out = torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype,
                      device=dev)
     pa.decode(to_dev(w.q, dev, w.dtype), k, v, tables, to_dev(w.seq_lens, dev), w.scale,
-              max_seq_len=max(w.max_seq_len, 1), out=out, partition_tokens=partition_tokens)
+              max_seq_len=max(w.max_seq_len, 1), out=out, partition_tokens=partition_tokens,
+              **fp8_kw(w))
     err = pa.get_device_error(dev)
     return {"k": k, "v": v, "slots": slots, "out": out, "err": err}
 
@@ -52,8 +69,13 @@ def oracle_scenario(w, pairs=None, heads=None):
         ks, vs = oracle.copy_blocks([k], [v], [tuple(p) for p in np.asarray(pairs).tolist()])
         k, v = ks[0], vs[0]
     slots = oracle.slot_mapping(w.block_tables, w.seq_idx, w.positions, w.block_size)
-    k, v = oracle.write_kv(k, v, w.key, w.value, slots)
-    out = oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, pairs=heads)
+    if w.kv_dtype == "e4m3":
+        k, v = oracle.write_kv_e4m3(k, v, w.key, w.value, slots, w.dtype, w.k_scale, w.v_scale)
+        out = oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, pairs=heads,
+                            kv_dtype="e4m3", k_scale=w.k_scale, v_scale=w.v_scale)
+    else:
+        k, v = oracle.write_kv(k, v, w.key, w.value, slots)
+        out = oracle.decode(w.q, k, v, w.block_tables, w.seq_lens, w.scale, w.dtype, pairs=heads)
     return {"k": k, "v": v, "slots": slots, "out": out}
 
 

@@ -41,7 +41,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 1
+    import paged_kv_cache_114_gb300._lib as L
+    assert lib.pa_abi_version() == L.ABI_VERSION == 2
     assert lib.pa_status_string(0) == b"ok"
     assert lib.pa_status_string(-5).startswith(b"workspace")
     assert lib.pa_status_string(12345) == b"unknown status"
@@ -132,6 +133,22 @@ def test_host_argument_errors_launch_nothing(lib):
     b24 = L.PaCache(4096, 8192, 64, 24, 8, 128, L.PA_F16)
     assert lib.pa_decode(vp(4096), 1, 8, ctypes.byref(b24), vp(4096), 1, vp(4096), 1, 1.0,
                          vp(4096), 0, 0, vp(0), 0, vp(0)) == -3
+    # E4M3 caches: act_dtype must be fp16/bf16, scales finite and positive,
+    # head_dim 128 or 256 for decode, and prefill does not take them
+    def fp8(d=128, act=L.PA_BF16, ks=0.01, vs=0.02):
+        return L.PaCache(4096, 8192, 64, 16, 8, d, L.PA_FP8_E4M3, act, ks, vs)
+    dec = lambda c: lib.pa_decode(vp(4096), 1, 8, ctypes.byref(c), vp(4096), 1, vp(4096), 1, 1.0,
+                                  vp(4096), 0, 0, vp(0), 0, vp(0))
+    assert dec(fp8(act=L.PA_F32)) == -2
+    assert dec(fp8(act=L.PA_FP8_E4M3)) == -2
+    assert dec(fp8(ks=0.0)) == -6
+    assert dec(fp8(vs=float("nan"))) == -6
+    assert dec(fp8(ks=float("inf"))) == -6
+    assert dec(fp8(d=64)) == -3
+    assert dec(fp8(d=120)) == -3
+    assert lib.pa_write_kv(vp(4096), vp(4096), vp(4096), 1, ctypes.byref(fp8(vs=-1.0)), vp(0)) == -6
+    assert lib.pa_prefill(vp(4096), 1, vp(4096), 1, 8, ctypes.byref(fp8()), vp(4096), 1, vp(4096),
+                          1.0, vp(4096), 0, vp(0)) == -2
     # zero sequences is a no-op
     assert lib.pa_decode(vp(0), 0, 8, ctypes.byref(good), vp(0), 1, vp(0), 1, 1.0,
                          vp(0), 0, 0, vp(0), 0, vp(0)) == 0
