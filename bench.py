@@ -12,7 +12,12 @@ e2e    = the same metric through the same calls with pinned host buffers:
 roofline = decode call only (partition kernel + reduce): algorithmic bytes per
          call / mean call time from CUDA events on the launching stream.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+With --kv-dtype e4m3 the same workload shape runs on an FP8 (E4M3) pool: one
+byte per cached element, q and the new K/V rows fp16/bf16, codes quantised by
+the write and widened by decode.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--kv-dtype e4m3]
+                       [--impl reference]
 """
 from __future__ import annotations
 
@@ -51,11 +56,22 @@ def step_tokens(w):
     return decode_step_tokens(w)
 
 
+def kv_elem(w):
+    """Bytes per cached element: 1 for an E4M3 pool, else 2."""
+    return 1 if w.kv_dtype == "e4m3" else 2
+
+
+def load_workload(config, block_size=None, kv_dtype="native"):
+    from workloads import make_config
+    return make_config(config, block_size=block_size if config == 4 else None,
+                       kv_dtype="e4m3" if kv_dtype == "e4m3" else None)
+
+
 def decode_bytes(w, out_elem=4):
     """Algorithmic bytes of one decode call: every valid K and V row once, q,
     the output, the table entries the lengths cover, and the lengths."""
     L = w.seq_lens.astype(np.int64)
-    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * kv_elem(w) * 2
     q = w.num_seqs * w.num_q_heads * w.head_dim * 2
     out = w.num_seqs * w.num_q_heads * w.head_dim * out_elem
     tables = int((-(-L // w.block_size)).sum()) * 4
@@ -67,16 +83,16 @@ def unique_decode_bytes(w):
     if not w.shared_blocks:
         return decode_bytes(w)
     shared_tokens = len(w.shared_blocks) * w.block_size
-    L = w.seq_lens.astype(np.int64)
-    row = w.num_kv_heads * w.head_dim * 2 * 2
+    row = w.num_kv_heads * w.head_dim * kv_elem(w) * 2
     return decode_bytes(w) - (w.num_seqs - 1) * shared_tokens * row
 
 
 def write_bytes(w, n_tokens):
     """Slot mapping (ids, positions, table entries in; slots out) and the KV write
-    (key/value rows read once, written once)."""
-    row = w.num_kv_heads * w.head_dim * 2
-    return n_tokens * (4 + 4 + 4 + 8) + n_tokens * (8 + 2 * row + 2 * row)
+    (key/value rows read once at 2 bytes an element, written once at the
+    cache's element size)."""
+    elems = w.num_kv_heads * w.head_dim
+    return n_tokens * (4 + 4 + 4 + 8) + n_tokens * (8 + 2 * elems * 2 + 2 * elems * kv_elem(w))
 
 
 def measured_peaks():
@@ -180,8 +196,10 @@ class Run:
 
         import paged_kv_cache_114_gb300 as pa
         self.w, self.dev, self.pa, self.torch = w, dev, pa, torch
-        self.k = to_dev(w.k_cache, dev, w.dtype)
-        self.v = to_dev(w.v_cache, dev, w.dtype)
+        fp8 = w.kv_dtype == "e4m3"
+        self.k = to_dev(w.k_cache, dev, None if fp8 else w.dtype)
+        self.v = to_dev(w.v_cache, dev, None if fp8 else w.dtype)
+        scales = {"k_scale": w.k_scale, "v_scale": w.v_scale} if fp8 else {}
         idx = step_tokens(w)
         # scenario rows written before timing (config 5's suffixes, after its copies)
         setup = np.setdiff1d(np.arange(len(w.positions)), idx)
@@ -192,14 +210,15 @@ class Run:
             sl = pa.slot_mapping(tables, to_dev(w.seq_idx[setup], dev),
                                  to_dev(w.positions[setup], dev), w.block_size, w.num_blocks)
             pa.write_kv(to_dev(w.key[setup], dev, w.dtype), to_dev(w.value[setup], dev, w.dtype),
-                        sl, self.k, self.v)
+                        sl, self.k, self.v, **scales)
         self.n_tokens = len(idx)
         self.partition = partition
         self.step_obj = pa.DecodeStep(
             self.k, self.v, num_seqs=w.num_seqs, num_q_heads=w.num_q_heads,
             num_tokens=self.n_tokens, max_blocks_per_seq=w.max_blocks_per_seq,
             max_seq_len=w.max_seq_len, scale=w.scale, out_dtype=torch.float32,
-            partition_tokens=partition)
+            partition_tokens=partition,
+            act_dtype=torch.float16 if w.dtype == "f16" else torch.bfloat16, **scales)
         host, _ = self.step_obj.host_buffers()
         fill = {"q": w.q, "key": w.key[idx], "value": w.value[idx], "seq_idx": w.seq_idx[idx],
                 "positions": w.positions[idx], "block_tables": w.block_tables,
@@ -256,7 +275,6 @@ def barrier(world):
 def run_gpu(args):
     import torch
 
-    from workloads import CONFIG_NAMES, make_config
     world, rank, local = _dist()
     if world > 1:
         import torch.distributed as dist
@@ -267,7 +285,7 @@ def run_gpu(args):
     import paged_kv_cache_114_gb300 as pa
     pa.lib()
 
-    w = make_config(args.config, block_size=args.block_size) if args.config == 4 else make_config(args.config)
+    w = load_workload(args.config, args.block_size, args.kv_dtype)
     partition = args.partition if args.partition is not None else pa.default_partition(
         w.num_seqs, w.num_kv_heads, w.max_seq_len, w.block_size)
     run = Run(w, dev, partition)
@@ -326,13 +344,15 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype or w.dtype, "data": "synthetic",
         "config": {
             "workload": workload,
             "shape": f"{w.num_seqs} seqs, {w.num_q_heads} q heads / {w.num_kv_heads} kv heads, "
                      f"head_dim {w.head_dim}, block {w.block_size}, seq_len {int(w.seq_lens.min())}.."
                      f"{int(w.seq_lens.max())} (mean {float(w.seq_lens.mean()):.0f})",
             "step": "pa_slot_mapping + pa_write_kv (one new token per sequence) + pa_decode",
+            "kv_dtype": w.cache_dtype,
+            "act_dtype": w.dtype,
             "partition_tokens": partition,
             "pool_bytes": int(w.k_cache.nbytes + w.v_cache.nbytes),
             "l2": "inputs larger than L2: the K/V pool far exceeds the 129 MB L2; no flush",
@@ -349,7 +369,8 @@ def run_gpu(args):
     if w.shared_blocks:
         line["config"]["unique_decode_bytes"] = unique_decode_bytes(w)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_child(args.config, args.block_size, "cpu_baseline")
+        line["cpu_baseline"] = cpu_baseline_child(args.config, args.block_size, "cpu_baseline",
+                                                  kv_dtype=args.kv_dtype)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -419,17 +440,23 @@ class OracleSample:
         k, v, table = self.inputs(s)
         i = self.newest.get(s)
         n_tok = 0
+        fp8 = {"kv_dtype": "e4m3", "k_scale": w.k_scale, "v_scale": w.v_scale} \
+            if w.kv_dtype == "e4m3" else {}
         if i is not None:
             slots = oracle.slot_mapping(table, [0], [int(w.positions[i])], w.block_size)
-            k, v = oracle.write_kv(k, v, w.key[i:i + 1], w.value[i:i + 1], slots)
+            if fp8:
+                k, v = oracle.write_kv_e4m3(k, v, w.key[i:i + 1], w.value[i:i + 1], slots, w.dtype,
+                                            w.k_scale, w.v_scale)
+            else:
+                k, v = oracle.write_kv(k, v, w.key[i:i + 1], w.value[i:i + 1], slots)
             n_tok = 1
-        oracle.decode(w.q[s:s + 1], k, v, table, w.seq_lens[s:s + 1], w.scale, w.dtype)
+        oracle.decode(w.q[s:s + 1], k, v, table, w.seq_lens[s:s + 1], w.scale, w.dtype, **fp8)
         return n_tok
 
 
 def sample_bytes(w, seqs, n_tok):
     L = w.seq_lens[list(seqs)].astype(np.int64)
-    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 4
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * kv_elem(w)
     q = len(seqs) * w.num_q_heads * w.head_dim * (2 + 4)
     tables = int((-(-L // w.block_size)).sum()) * 4 + 4 * len(seqs)
     return kv + q + tables + write_bytes(w, n_tok)
@@ -446,16 +473,20 @@ def prepared_oracle_state(w):
         k, v = ks[0], vs[0]
     if len(setup):
         sl = oracle.slot_mapping(w.block_tables, w.seq_idx[setup], w.positions[setup], w.block_size)
-        k, v = oracle.write_kv(k, v, w.key[setup], w.value[setup], sl)
+        if w.kv_dtype == "e4m3":
+            k, v = oracle.write_kv_e4m3(k, v, w.key[setup], w.value[setup], sl, w.dtype,
+                                        w.k_scale, w.v_scale)
+        else:
+            k, v = oracle.write_kv(k, v, w.key[setup], w.value[setup], sl)
     return {"k": k, "v": v}
 
 
-def cpu_baseline_child(config, block_size, mode, steps=0, warmup=0):
+def cpu_baseline_child(config, block_size, mode, steps=0, warmup=0, kv_dtype="native"):
     """Runs the oracle timing in a fresh single-threaded process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-child", mode, "--config", str(config),
-           "--steps", str(steps), "--warmup", str(warmup)]
+           "--steps", str(steps), "--warmup", str(warmup), "--kv-dtype", kv_dtype]
     if block_size is not None:
         cmd += ["--block-size", str(block_size)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
@@ -467,8 +498,7 @@ def cpu_baseline_child(config, block_size, mode, steps=0, warmup=0):
 def cpu_child(args):
     """Oracle timing: 'cpu_baseline' = one bounded sample (about 12 s of CPU);
     'reference' = the reference arm's W + K steps, each one random sequence."""
-    from workloads import make_config
-    w = make_config(args.config, block_size=args.block_size) if args.config == 4 else make_config(args.config)
+    w = load_workload(args.config, args.block_size, args.kv_dtype)
     sampler = OracleSample(w)
     rng = np.random.default_rng(0)
     if args.cpu_child == "cpu_baseline":
@@ -509,14 +539,15 @@ def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
-    from workloads import CONFIG_NAMES
-    res = cpu_baseline_child(args.config, args.block_size, "reference", args.steps, args.warmup)
+    res = cpu_baseline_child(args.config, args.block_size, "reference", args.steps, args.warmup,
+                             kv_dtype=args.kv_dtype)
+    w = load_workload(args.config, args.block_size, args.kv_dtype)
     line = {
         "impl": "reference", "metric": METRIC, "value": res.get("value"), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": res.get("ms_per_step"), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": CONFIG_NAMES[args.config],
+        "config": {"workload": w.name,
                    "note": "the pages publish no runnable reference; this arm times the fp64 CPU oracle"},
         "cpu_baseline": {"value": res.get("value"), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": res.get("sample")},
@@ -534,6 +565,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--block-size", type=int, default=None, help="config 4 block size (8/16/32)")
     ap.add_argument("--partition", type=int, default=None, help="split-K partition tokens (default: library's)")
+    ap.add_argument("--kv-dtype", choices=["native", "e4m3"], default="native",
+                    help="pool element type: the config's fp16/bf16, or FP8 E4M3 codes (configs 2-5)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-child", choices=["cpu_baseline", "reference"], default=None,

@@ -28,13 +28,17 @@
 //
 // FP8 caches (E4M3 codes, one scale per layer for K and one for V): a stage
 // row is D bytes instead of 2D, so one 128-byte swizzled line holds 128 head-dim
-// elements. Codes are widened exactly to fp16/bf16 in registers: for S^T the
-// MMA's reduction index k is mapped to head-dim elements four at a time
-// (lane quad t reads dims 4t..4t+3 of its rows with one 32-bit load, q is
-// loaded with the same order); for O^T two token rows' words are byte-permuted
-// into (token, token+1) pairs and the head-dim rows of two m16 tiles
-// interleave (acc_dim gives each accumulator's dim). k_scale folds into the
-// logit scale, v_scale multiplies the output.
+// elements. Codes are widened exactly to fp16 in registers (two conversions
+// per 32-bit word) and every MMA runs in fp16. ldmatrix treats byte pairs as
+// its 16-bit elements: for S^T each lane gets four consecutive codes of a
+// row, so the MMA's reduction index k maps to head-dim elements four at a
+// time (q is loaded in the same order); for O^T the transposing ldmatrix
+// gives each lane two dims of two tokens, which a byte permute turns into
+// (token, token+1) pairs per dim, the two dims landing in rows gid and gid+8
+// of the tile (acc_dim gives each accumulator's dim). bf16 queries become fp16 times a per-head
+// power of two that keeps the row's largest element below 2^14; the logit
+// scale of each head column undoes it. k_scale folds into the logit scale,
+// v_scale multiplies the output.
 //
 // decode_kernel: one CTA per (sequence, KV head, partition); its 4 warps take
 // the partition's stages round-robin and merge through shared memory at the
@@ -69,7 +73,7 @@ struct KvLayout {
 // gid (rows gid and gid + 8 of the m16 tile).
 template <bool FP8>
 __device__ __forceinline__ int acc_dim(int dm, int gid, int r) {
-  if constexpr (FP8) return ((dm >> 1) << 5) + (gid << 2) + ((dm & 1) << 1) + (r >> 1);
+  if constexpr (FP8) return dm * 16 + (gid << 1) + (r >> 1);
   return dm * 16 + gid + ((r >> 1) << 3);
 }
 
@@ -214,6 +218,18 @@ struct DecodeSmem {
   static constexpr int kTotal = kPrefixOffset + 1024;  // + base-alignment slack
 };
 
+// Logit multipliers of the S^T tile's columns, in log2 units: the scalar
+// scale * log2(e) for 16-bit caches; per query head for E4M3 caches, whose
+// fp16 copy of a bf16 query carries a per-head power of two (see load_q).
+template <int NT, bool PER_HEAD>
+struct LogitScale {
+  float s[PER_HEAD ? NT : 1][PER_HEAD ? 2 : 1];
+  __device__ __forceinline__ float operator()(int nt, int c) const {
+    if constexpr (PER_HEAD) return s[nt][c];
+    return s[0][0];
+  }
+};
+
 // Per-warp online-softmax state for NT tiles of 8 query heads.
 template <int D, int NT>
 struct Acc {
@@ -246,12 +262,15 @@ struct Acc {
 };
 
 // q of the group of KV head kvh as the B operand of S^T = K Q^T
-// (k = head-dim index, n = head within the tile); heads past g are zero. For
-// FP8 caches, lane quad t takes dims 16kk + 4t .. + 3 of k-step kk, the order
-// in which compute_stage reads the codes.
-template <int D, int NT, bool FP8>
+// (k = head-dim index, n = head within the tile); heads past g are zero, and
+// the column logit scales. For FP8 caches, lane quad t takes dims 16kk + 4t ..
+// + 3 of k-step kk, the order in which compute_stage reads the codes, and a
+// bf16 query row is stored as fp16 times 2^(13 - e), e the exponent of its
+// largest magnitude (exact for every element at or above 2^-14 of that
+// scale; the column's logit scale carries 2^(e - 13)).
+template <bool IS_BF16, int D, int NT, bool FP8>
 __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int lane,
-                                       uint32_t (&qb)[NT][D / 16][2]) {
+                                       uint32_t (&qb)[NT][D / 16][2], LogitScale<NT, FP8>& ls) {
   const int gid = lane >> 2;
   const int tig = lane & 3;
   const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
@@ -268,7 +287,36 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int 
       qb[nt][kk][0] = live ? __ldg(q32 + ((row + d0) >> 1)) : 0u;
       qb[nt][kk][1] = live ? __ldg(q32 + ((row + d1) >> 1)) : 0u;
     }
+    if constexpr (FP8 && IS_BF16) {
+      float m = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 f = unpack2<true>(qb[nt][kk][i]);
+          m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const int e = max(static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127, -100);
+      const float p = __uint_as_float(static_cast<uint32_t>(127 + 13 - e) << 23);    // 2^(13-e)
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - 13 + e) << 23);  // 2^(e-13)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 f = unpack2<true>(qb[nt][kk][i]);
+          qb[nt][kk][i] = pack2<false>(f.x * p, f.y * p);
+        }
+      }
+      ls.s[nt][0] = a.scale_log2 * __shfl_sync(0xffffffffu, inv, tig * 8);
+      ls.s[nt][1] = a.scale_log2 * __shfl_sync(0xffffffffu, inv, tig * 8 + 4);
+    } else if constexpr (FP8) {
+      ls.s[nt][0] = ls.s[nt][1] = a.scale_log2;
+    }
   }
+  if constexpr (!FP8) ls.s[0][0] = a.scale_log2;
 }
 
 // Issues the TMA copies of one stage - tokens [t0, t0 + tt) of the sequence
@@ -360,7 +408,9 @@ template <bool IS_BF16, int D, int NT, bool SPLIT_P, bool FP8, class View>
 __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
                                               uint8_t* smem_base_ptr, uint32_t rowmask,
                                               const uint32_t (&qb)[NT][D / 16][2],
-                                              Acc<D, NT>& acc, float scale_log2, int lane) {
+                                              Acc<D, NT>& acc, const LogitScale<NT, FP8>& ls,
+                                              int lane) {
+  constexpr bool MB = IS_BF16 && !FP8;  // MMA operand type: E4M3 caches run in fp16
   constexpr int TS = kStageRows;
   constexpr int KD = D / 16;
   constexpr int HALVES = D / KvLayout<FP8>::kPieceElems;
@@ -384,18 +434,36 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
   if constexpr (FP8) {
-    // rows gid and gid + 8, dims 16kk + 4tig .. + 3: one 32-bit load per row
+    // ldmatrix over byte-pair rows: matrix j holds rows 8(j & 1) .. + 7 of
+    // 16-byte chunk kk + (j >> 1), and lane (gid, tig) receives bytes 4tig ..
+    // 4tig + 3 of its row: dims 16kk + 4tig .. + 3, the order load_q uses. Even
+    // and odd k-steps accumulate separately, two independent MMA chains.
+    const int i = lane >> 3;
+    const int row = ((i & 1) << 3) + (lane & 7);
+    float sodd[NT][4];
 #pragma unroll
-    for (int kk = 0; kk < KD; ++kk) {
-      const uint32_t col = ((((kk & 7) ^ (gid & 7)) << 4) + (tig << 2));
-      const uint32_t base = sv.k + (kk >> 3) * View::half_stride + col;
-      const uint32_t w0 = lds_u32(base + sv.row(gid));
-      const uint32_t w1 = lds_u32(base + sv.row(gid + 8));
-      uint32_t af[4];
-      e4m3x4_widen<IS_BF16>(w0, af[0], af[2]);
-      e4m3x4_widen<IS_BF16>(w1, af[1], af[3]);
+    for (int nt = 0; nt < NT; ++nt) sodd[nt][0] = sodd[nt][1] = sodd[nt][2] = sodd[nt][3] = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816<IS_BF16>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+    for (int kk = 0; kk < KD; kk += 2) {
+      const int chunk = (kk & 7) + (i >> 1);
+      uint32_t w[4];
+      ldsm_x4(sv.k + (kk >> 3) * View::half_stride + sv.row(row) + ((chunk ^ (row & 7)) << 4), w);
+      uint32_t a0[4];
+      uint32_t a1[4];
+      e4m3x4_to_f16(w[0], a0[0], a0[2]);
+      e4m3x4_to_f16(w[1], a0[1], a0[3]);
+      e4m3x4_to_f16(w[2], a1[0], a1[2]);
+      e4m3x4_to_f16(w[3], a1[1], a1[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816<MB>(sacc[nt], a0, qb[nt][kk][0], qb[nt][kk][1]);
+        mma16816<MB>(sodd[nt], a1, qb[nt][kk + 1][0], qb[nt][kk + 1][1]);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sacc[nt][r] += sodd[nt][r];
     }
   } else {
     const int i = lane >> 3;
@@ -406,27 +474,45 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
       uint32_t af[4];
       ldsm_x4(sv.k + (kk >> 2) * View::half_stride + sv.row(row) + ((chunk ^ (row & 7)) << 4), af);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816<IS_BF16>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+      for (int nt = 0; nt < NT; ++nt) mma16816<MB>(sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
     }
   }
 
-  // Online softmax update (log2 domain).
+  // Online softmax update (log2 domain). For E4M3 caches the running maximum
+  // is raised lazily: only when a logit exceeds it by more than 8 (a factor
+  // of 2^8), so most stages keep it and skip rescaling the output; p then
+  // stays below 2^8, and o / l is unchanged.
   const bool v0 = (rowmask >> gid) & 1u;
   const bool v1 = (rowmask >> (gid + 8)) & 1u;
   float p[NT][4];
+  float lazy_alpha[NT][2];
+  bool grew = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float x[4];
-    x[0] = v0 ? sacc[nt][0] * scale_log2 : -INFINITY;
-    x[1] = v0 ? sacc[nt][1] * scale_log2 : -INFINITY;
-    x[2] = v1 ? sacc[nt][2] * scale_log2 : -INFINITY;
-    x[3] = v1 ? sacc[nt][3] * scale_log2 : -INFINITY;
+    x[0] = v0 ? sacc[nt][0] * ls(nt, 0) : -INFINITY;
+    x[1] = v0 ? sacc[nt][1] * ls(nt, 1) : -INFINITY;
+    x[2] = v1 ? sacc[nt][2] * ls(nt, 0) : -INFINITY;
+    x[3] = v1 ? sacc[nt][3] * ls(nt, 1) : -INFINITY;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       float mx = fmaxf(x[c], x[c + 2]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if constexpr (FP8) {
+        const bool grow = mx > acc.m[nt][c] + 8.f;
+        const float m_new = grow ? mx : acc.m[nt][c];
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = grow ? exp2f(acc.m[nt][c] - m_use) : 1.f;
+        acc.m[nt][c] = m_new;
+        p[nt][c] = exp2f(x[c] - m_use);
+        p[nt][c + 2] = exp2f(x[c + 2] - m_use);
+        acc.l[nt][c] = acc.l[nt][c] * alpha + p[nt][c] + p[nt][c + 2];
+        lazy_alpha[nt][c] = alpha;
+        grew |= grow;
+        continue;
+      }
       const float m_new = fmaxf(acc.m[nt][c], mx);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = exp2f(acc.m[nt][c] - m_use);
@@ -441,51 +527,66 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
       }
     }
   }
+  if constexpr (FP8) {
+    if (__any_sync(0xffffffffu, grew)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int dm = 0; dm < KD; ++dm) {
+          acc.o[dm][nt][0] *= lazy_alpha[nt][0];
+          acc.o[dm][nt][1] *= lazy_alpha[nt][1];
+          acc.o[dm][nt][2] *= lazy_alpha[nt][0];
+          acc.o[dm][nt][3] *= lazy_alpha[nt][1];
+        }
+      }
+    }
+  }
 
   // P^T as the B operand (k = token, n = head): transpose the 8x8 halves.
   uint32_t bh[NT][2];
   uint32_t bl[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t h01 = pack2<IS_BF16>(p[nt][0], p[nt][1]);
-    const uint32_t h23 = pack2<IS_BF16>(p[nt][2], p[nt][3]);
+    const uint32_t h01 = pack2<MB>(p[nt][0], p[nt][1]);
+    const uint32_t h23 = pack2<MB>(p[nt][2], p[nt][3]);
     bh[nt][0] = movmatrix_trans(h01);
     bh[nt][1] = movmatrix_trans(h23);
     if constexpr (SPLIT_P) {
-      const float2 f01 = unpack2<IS_BF16>(h01);
-      const float2 f23 = unpack2<IS_BF16>(h23);
-      bl[nt][0] = movmatrix_trans(pack2<IS_BF16>(p[nt][0] - f01.x, p[nt][1] - f01.y));
-      bl[nt][1] = movmatrix_trans(pack2<IS_BF16>(p[nt][2] - f23.x, p[nt][3] - f23.y));
+      const float2 f01 = unpack2<MB>(h01);
+      const float2 f23 = unpack2<MB>(h23);
+      bl[nt][0] = movmatrix_trans(pack2<MB>(p[nt][0] - f01.x, p[nt][1] - f01.y));
+      bl[nt][1] = movmatrix_trans(pack2<MB>(p[nt][2] - f23.x, p[nt][3] - f23.y));
     }
   }
 
   // O^T += V^T P^T over the 16 tokens of the stage.
   if constexpr (FP8) {
-    // dims 32dp + 4gid .. + 3 of tokens 2tig, 2tig + 1, 2tig + 8, 2tig + 9; the
-    // byte pairs (token, token + 1) of each dim form the A operands of tiles
-    // 2dp (dims +0 / +1 in rows gid / gid + 8) and 2dp + 1 (dims +2 / +3).
-    const int t0 = tig * 2;
+    // ldmatrix.trans over byte-pair rows: matrix j holds tokens 8(j & 1) .. + 7
+    // of 16-byte chunk c + (j >> 1), and lane (gid, tig) receives dims 16c +
+    // 2gid, + 1 of tokens 2tig and 2tig + 1. A byte permute pairs the two
+    // tokens per dim: tile c of O^T holds dim 16c + 2gid in row gid and
+    // 16c + 2gid + 1 in row gid + 8 (acc_dim).
+    const int i = lane >> 3;
+    const int row = ((i & 1) << 3) + (lane & 7);
 #pragma unroll
-    for (int dp = 0; dp < D / 32; ++dp) {
-      const uint32_t chunk = static_cast<uint32_t>(((dp & 3) << 1) + (gid >> 2));
-      const uint32_t base = sv.v + (dp >> 2) * View::half_stride + ((gid & 3) << 2);
-      const uint32_t w0 = lds_u32(base + sv.row(t0) + ((chunk ^ (t0 & 7)) << 4));
-      const uint32_t w1 = lds_u32(base + sv.row(t0 + 1) + ((chunk ^ ((t0 + 1) & 7)) << 4));
-      const uint32_t w8 = lds_u32(base + sv.row(t0 + 8) + ((chunk ^ (t0 & 7)) << 4));
-      const uint32_t w9 = lds_u32(base + sv.row(t0 + 9) + ((chunk ^ ((t0 + 1) & 7)) << 4));
+    for (int dm = 0; dm < KD; dm += 2) {
+      const int chunk = (dm & 7) + (i >> 1);
+      uint32_t x[4];
+      ldsm_x4_trans(sv.v + (dm >> 3) * View::half_stride + sv.row(row) + ((chunk ^ (row & 7)) << 4),
+                    x);
       uint32_t fa[4];
       uint32_t fb[4];
-      e4m3x4_widen<IS_BF16>(prmt(w0, w1, 0x5140u), fa[0], fa[1]);
-      e4m3x4_widen<IS_BF16>(prmt(w8, w9, 0x5140u), fa[2], fa[3]);
-      e4m3x4_widen<IS_BF16>(prmt(w0, w1, 0x7362u), fb[0], fb[1]);
-      e4m3x4_widen<IS_BF16>(prmt(w8, w9, 0x7362u), fb[2], fb[3]);
+      e4m3x4_to_f16(prmt(x[0], x[0], 0x3120u), fa[0], fa[1]);
+      e4m3x4_to_f16(prmt(x[1], x[1], 0x3120u), fa[2], fa[3]);
+      e4m3x4_to_f16(prmt(x[2], x[2], 0x3120u), fb[0], fb[1]);
+      e4m3x4_to_f16(prmt(x[3], x[3], 0x3120u), fb[2], fb[3]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        mma16816<IS_BF16>(acc.o[2 * dp][nt], fa, bh[nt][0], bh[nt][1]);
-        mma16816<IS_BF16>(acc.o[2 * dp + 1][nt], fb, bh[nt][0], bh[nt][1]);
+        mma16816<MB>(acc.o[dm][nt], fa, bh[nt][0], bh[nt][1]);
+        mma16816<MB>(acc.o[dm + 1][nt], fb, bh[nt][0], bh[nt][1]);
         if constexpr (SPLIT_P) {
-          mma16816<IS_BF16>(acc.o[2 * dp][nt], fa, bl[nt][0], bl[nt][1]);
-          mma16816<IS_BF16>(acc.o[2 * dp + 1][nt], fb, bl[nt][0], bl[nt][1]);
+          mma16816<MB>(acc.o[dm][nt], fa, bl[nt][0], bl[nt][1]);
+          mma16816<MB>(acc.o[dm + 1][nt], fb, bl[nt][0], bl[nt][1]);
         }
       }
     }
@@ -500,8 +601,8 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
                     af);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        mma16816<IS_BF16>(acc.o[dm][nt], af, bh[nt][0], bh[nt][1]);
-        if constexpr (SPLIT_P) mma16816<IS_BF16>(acc.o[dm][nt], af, bl[nt][0], bl[nt][1]);
+        mma16816<MB>(acc.o[dm][nt], af, bh[nt][0], bh[nt][1]);
+        if constexpr (SPLIT_P) mma16816<MB>(acc.o[dm][nt], af, bl[nt][0], bl[nt][1]);
       }
     }
   }
@@ -544,7 +645,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int my_n = nst > warp ? (nst - warp - 1) / W + 1 : 0;
 
   uint32_t qb[NT][KD][2];
-  load_q<D, NT, FP8>(a, s, kvh, lane, qb);
+  LogitScale<NT, FP8> ls;
+  load_q<IS_BF16, D, NT, FP8>(a, s, kvh, lane, qb, ls);
 
   const uint32_t bar0 = sm_base + S::kBarOffset + warp * NS * 8;
   if (lane == 0) {
@@ -579,7 +681,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
     compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(
         warp_stage_view(ring + slot * S::kStageBytes, S::kHalves), ring + slot * S::kStageBytes,
-        ring_ptr + slot * S::kStageBytes, masks[slot], qb, acc, a.scale_log2, lane);
+        ring_ptr + slot * S::kStageBytes, masks[slot], qb, acc, ls, lane);
     fence_proxy_async_smem();  // our generic reads/writes of this slot precede the next TMA into it
     __syncwarp();
     if (it + NS < my_n) issue(it + NS);
@@ -911,7 +1013,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   for (int i = 0; i < pro; ++i) issue(i);
 
   uint32_t qb[NT][KD][2];
-  load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
+  LogitScale<NT, FP8> ls;
+  load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);
   Acc<D, NT> acc;
   acc.reset();
   bool aborted = false;
@@ -931,7 +1034,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (!aborted) {
       compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(
           warp_stage_view(ring + slot * S::kStageBytes, S::kHalves), ring, ring_ptr, masks[slot],
-          qb, acc, a.scale_log2, lane);
+          qb, acc, ls, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (it + NS < count) issue(it + NS);
@@ -950,7 +1053,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
-      load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
+      load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);
       acc.reset();
     }
   }

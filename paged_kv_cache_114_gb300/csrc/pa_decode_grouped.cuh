@@ -188,7 +188,8 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
 
   Cursor cc = cursor_at(a, pre, g0);
   uint32_t qb[NT][KD][2];
-  load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
+  LogitScale<NT, FP8> ls;
+  load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);
   Acc<D, NT> acc;
   acc.reset();
   bool aborted = false;
@@ -205,8 +206,8 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
     if (!aborted) {
       sv.k = sm_base + slot * stage_bytes;
       sv.v = sv.k + HALVES * half_bytes;
-      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(sv, sm_base, sm, masks[slot], qb, acc,
-                                                  a.scale_log2, lane);
+      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(sv, sm_base, sm, masks[slot], qb, acc, ls,
+                                                  lane);
       static_assert(GroupView<HG, TPO>::half_stride == S::half_bytes(HG), "layout");
       fence_proxy_async_smem();
       __syncwarp();
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
                              lane);
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
-      load_q<D, NT, FP8>(a, cc.s, kvh, lane, qb);
+      load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);
       acc.reset();
     }
   }

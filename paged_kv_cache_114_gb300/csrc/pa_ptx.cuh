@@ -153,13 +153,6 @@ __device__ __forceinline__ float2 unpack2(uint32_t x) {
   }
 }
 
-// 32-bit shared-memory load.
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
 // Byte permute: result byte i = byte sel_i of the 8-byte pair (hi:lo).
 __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
   uint32_t r;
@@ -167,24 +160,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
   return r;
 }
 
-// Widens the four E4M3 codes of a 32-bit word into two packed pairs of 16-bit
-// MMA operands: lo <- bytes 0 (low half), 1 (high half); hi <- bytes 2, 3.
-// Every E4M3 value is exact in fp16 and in bf16, so the widening is exact.
-template <bool IS_BF16>
-__device__ __forceinline__ void e4m3x4_widen(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu),
-                                                   __NV_E4M3);
-  const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16),
-                                                   __NV_E4M3);
-  if constexpr (IS_BF16) {
-    const float2 fa = __half22float2(__half2(a));
-    const float2 fb = __half22float2(__half2(b));
-    lo = pack2<true>(fa.x, fa.y);
-    hi = pack2<true>(fb.x, fb.y);
-  } else {
-    lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-    hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
-  }
+// Widens the four E4M3 codes of a 32-bit word to fp16, exactly (every E4M3
+// value is an fp16 value): lo <- bytes 0 (low half), 1 (high half); hi <- bytes
+// 2, 3. One conversion per 16-bit half, no unpacking.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Encodes two floats as E4M3 codes (x -> low byte, y -> high byte): nearest
