@@ -16,8 +16,12 @@ With --kv-dtype e4m3 the same workload shape runs on an FP8 (E4M3) pool: one
 byte per cached element, q and the new K/V rows fp16/bf16, codes quantised by
 the write and widened by decode.
 
+--prefill NAME times pa_prefill alone (multi-token causal attention) on a named
+workload instead: verify4_70b_bf16_b16 (speculative verification, HBM-bound),
+chunk512_gqa_bf16_b16 or prompt2k_mha_fp16_b16 (tensor-bound).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--kv-dtype e4m3]
-                       [--impl reference]
+                       [--impl reference] [--prefill NAME]
 """
 from __future__ import annotations
 
@@ -406,6 +410,113 @@ def run_e2e(run, K, W, world, dev, step_bytes):
                     "H2D copy, the 3 library calls, one D2H copy; stream synchronize per step"}
 
 
+# ----------------------------------------------------------------------------- prefill
+
+
+def prefill_keys(w):
+    """(query, key) pairs the causal mask admits, per query head: query i of
+    sequence s (n new of L) sees L - n + i + 1 keys."""
+    qn = np.diff(w.q_start).astype(np.int64)
+    L = w.seq_lens.astype(np.int64)
+    return int((qn * (L - qn) + qn * (qn + 1) // 2).sum())
+
+
+def prefill_flops(w):
+    """QK^T and PV: 2 * D multiply-adds each per admitted (query head, key)."""
+    return 4 * w.head_dim * w.num_q_heads * prefill_keys(w)
+
+
+def prefill_bytes(w, out_elem=4):
+    """Every cached K and V row of a sequence once per KV head, q, the output,
+    the table entries and q_start / lengths."""
+    L = w.seq_lens.astype(np.int64)
+    t = int(w.q_start[-1])
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    q = t * w.num_q_heads * w.head_dim * 2
+    out = t * w.num_q_heads * w.head_dim * out_elem
+    return kv + q + out + int((-(-L // w.block_size)).sum()) * 4 + 8 * w.num_seqs
+
+
+def run_prefill(args):
+    import torch
+
+    import paged_kv_cache_114_gb300 as pa
+    from workloads import make_prefill_config
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    w = make_prefill_config(args.prefill)
+    k = to_dev(w.k_cache, dev, w.dtype)
+    v = to_dev(w.v_cache, dev, w.dtype)
+    tables, lens = to_dev(w.block_tables, dev), to_dev(w.seq_lens, dev)
+    slots = pa.slot_mapping(tables, to_dev(w.seq_idx, dev), to_dev(w.positions, dev),
+                            w.block_size, w.num_blocks)
+    pa.write_kv(to_dev(w.key, dev, w.dtype), to_dev(w.value, dev, w.dtype), slots, k, v)
+    q = to_dev(w.q, dev, w.dtype)
+    q_start = to_dev(w.q_start, dev)
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
+    max_q = int(np.diff(w.q_start).max())
+
+    def call():
+        pa.prefill(q, k, v, tables, lens, q_start, w.scale, max_q_len=max_q, out=out)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error during warm-up")
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clocks:
+        for a, b in evs:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error in the timed region")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    flops, nbytes = prefill_flops(w), prefill_bytes(w)
+    tflops = flops / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    hbm, _ = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tc_peak, tc_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tc_peak, tc_kind = 1900.0, "fallback"
+    hbm_bound = args.prefill.startswith("verify")
+    roofline = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                 "frac": round(gbs / hbm, 4)} if hbm_bound else
+                {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak, "unit": "TFLOP/s",
+                 "frac": round(tflops / tc_peak, 4)})
+    roofline.update({"traffic": None, "kernel": "prefill_kernel", "mean_call_us": round(ms * 1e3, 2),
+                     "peak_source": f"{tc_kind if not hbm_bound else 'measured'} "
+                                    f"(MEASURED_PEAKS.json {'hbm_gbs' if hbm_bound else 'bf16_tflops'})"})
+    qn = np.diff(w.q_start)
+    line = {
+        "metric": "paged prefill attention throughput (multi-token causal, one layer)",
+        "value": round(gbs if hbm_bound else tflops, 2), "unit": "GB/s" if hbm_bound else "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name,
+                   "shape": f"{w.num_seqs} seqs, {w.num_q_heads} q heads / {w.num_kv_heads} kv heads, "
+                            f"head_dim {w.head_dim}, block {w.block_size}, seq_len "
+                            f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}, new tokens "
+                            f"{int(qn.min())}..{int(qn.max())}",
+                   "step": "pa_prefill (new K/V written before the timed region)",
+                   "flops_per_call": flops, "algorithmic_bytes_per_call": nbytes,
+                   "l2": "K/V pool larger than L2 for verify and prompt; chunk's 189 MB pool "
+                         "exceeds the 129 MB L2"},
+        "tflops": round(tflops, 2), "kv_gbs": round(gbs, 1), "roofline": roofline,
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 
@@ -565,6 +676,9 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--block-size", type=int, default=None, help="config 4 block size (8/16/32)")
     ap.add_argument("--partition", type=int, default=None, help="split-K partition tokens (default: library's)")
+    ap.add_argument("--prefill", default=None,
+                    choices=["verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16"],
+                    help="time pa_prefill on a named multi-token workload instead")
     ap.add_argument("--kv-dtype", choices=["native", "e4m3"], default="native",
                     help="pool element type: the config's fp16/bf16, or FP8 E4M3 codes (configs 2-5)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -578,6 +692,8 @@ def main(argv=None):
         return cpu_child(args)
     if args.impl == "reference":
         return run_reference(args)
+    if args.prefill:
+        return run_prefill(args)
     return run_gpu(args)
 
 
