@@ -33,6 +33,11 @@ Each function is the plain definition of one step, written from the pages:
 * the blockwise online-softmax recurrence and the partition-combine rule of
   ailinkdeeptech.com §3 (running max m, normaliser l, unnormalised o), used to
   pin the split-K reduction.
+* swap for preemption: a preempted sequence's blocks are copied, every layer,
+  K and V, to a pool in host memory and later back, possibly to other block
+  ids (pofe.ai §When memory runs out: swapping copies the evicted blocks to
+  CPU memory and back; learn.pranaymahendrakar.com §Preemption: copy blocks
+  to pinned host memory and back). A copy between two pools.
 * an FP8 cache: the same pool with one byte per element, which "halves the
   bytes per block; nothing else about paging changes" (pofe.ai §Fine-tuned
   models and adapters, quantised caches). The pages fix no format or scale, so
@@ -184,6 +189,21 @@ def copy_blocks(k_caches: Sequence[np.ndarray], v_caches: Sequence[np.ndarray],
         for k, v in zip(ks, vs):
             k[int(dst)] = k[int(src)]
             v[int(dst)] = v[int(src)]
+    return ks, vs
+
+
+def swap_blocks(src_k: Sequence[np.ndarray], src_v: Sequence[np.ndarray],
+                dst_k: Sequence[np.ndarray], dst_v: Sequence[np.ndarray],
+                pairs: Iterable[Tuple[int, int]]) -> Tuple[List[np.ndarray], List[np.ndarray]]:
+    """New destination pools where, for every (src, dst) pair and every layer,
+    block dst of the destination holds a copy of block src of the source (K and
+    V). The source pools are not changed; the two pools may differ in size."""
+    ks = [k.copy() for k in dst_k]
+    vs = [v.copy() for v in dst_v]
+    for src, dst in pairs:
+        for layer in range(len(ks)):
+            ks[layer][int(dst)] = src_k[layer][int(src)]
+            vs[layer][int(dst)] = src_v[layer][int(src)]
     return ks, vs
 
 
