@@ -20,8 +20,12 @@ the write and widened by decode.
 workload instead: verify4_70b_bf16_b16 (speculative verification, HBM-bound),
 chunk512_gqa_bf16_b16 or prompt2k_mha_fp16_b16 (tensor-bound).
 
+--swap times pa_swap_blocks: a preempted batch's blocks (every layer, K and V)
+out to a pinned host pool and back in, against a contiguous copy of the same
+bytes by the copy engine as the link's reference rate.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--kv-dtype e4m3]
-                       [--impl reference] [--prefill NAME]
+                       [--impl reference] [--prefill NAME] [--swap]
 """
 from __future__ import annotations
 
@@ -517,6 +521,103 @@ def run_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- swap
+
+
+SWAP_WORKLOAD = {"name": "swap16x4096_70b_bf16_b16_8layers", "layers": 8, "seqs": 16,
+                 "tokens": 4096, "block_size": 16, "kv_heads": 8, "head_dim": 128}
+
+
+def run_swap(args):
+    """Swap out 16 sequences of 4,096 tokens on the 70B head shape (8 layers of
+    the pool, K and V: 2.15 GB) to a pinned host pool and back in, each step one
+    pa_swap_blocks call per direction; blocks are scattered in both pools."""
+    import torch
+
+    import paged_kv_cache_114_gb300 as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    cfg = SWAP_WORKLOAD
+    rng = np.random.default_rng(3000)
+    b, h, d, L = cfg["block_size"], cfg["kv_heads"], cfg["head_dim"], cfg["layers"]
+    nblk = cfg["seqs"] * cfg["tokens"] // b
+    dev_blocks = int(nblk * 1.25)
+    pools = [(torch.randn(dev_blocks, b, h, d, dtype=torch.bfloat16, device=dev),
+              torch.randn(dev_blocks, b, h, d, dtype=torch.bfloat16, device=dev)) for _ in range(L)]
+    host = [(torch.empty(nblk, b, h, d, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(nblk, b, h, d, dtype=torch.bfloat16).pin_memory()) for _ in range(L)]
+    src_ids = rng.choice(dev_blocks, nblk, replace=False).astype(np.int64)
+    host_ids = rng.permutation(nblk).astype(np.int64)
+    out_pairs = torch.from_numpy(np.stack([src_ids, host_ids], 1)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([host_ids, src_ids], 1)).to(dev)
+    dk, dv = [p[0] for p in pools], [p[1] for p in pools]
+    hk, hv = [p[0] for p in host], [p[1] for p in host]
+    nbytes = 2 * L * nblk * b * h * d * 2
+
+    def timed(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        stream = torch.cuda.current_stream(dev)
+        for a, e in evs:
+            a.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(e) for a, e in evs)
+
+    swap_out = lambda: pa.swap_blocks(dk, dv, hk, hv, out_pairs)
+    swap_in = lambda: pa.swap_blocks(hk, hv, dk, dv, in_pairs)
+    for _ in range(args.warmup):
+        swap_out()
+        swap_in()
+    torch.cuda.synchronize()
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error during warm-up")
+    with ClockSampler(0) as clocks:
+        ms_out = timed(swap_out, args.steps)
+        ms_in = timed(swap_in, args.steps)
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error in the timed region")
+    # the link's reference: one contiguous copy-engine transfer of the same bytes
+    flat_d = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev)
+    flat_h = torch.empty(nbytes // 2, dtype=torch.bfloat16).pin_memory()
+    ms_ce_out = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), max(3, args.steps // 2))
+    ms_ce_in = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), max(3, args.steps // 2))
+    # the same pa_swap_blocks between two device pools (HBM read + write)
+    pools2 = [(torch.empty_like(p[0]), torch.empty_like(p[1])) for p in pools]
+    dd_pairs = torch.from_numpy(np.stack([src_ids, rng.permutation(dev_blocks)[:nblk]], 1)).to(dev)
+    ms_dd = timed(lambda: pa.swap_blocks(dk, dv, [p[0] for p in pools2], [p[1] for p in pools2],
+                                         dd_pairs), args.steps)
+    gbs = lambda ms: nbytes / (ms / 1e3) / 1e9
+    hbm, _ = measured_peaks()
+    line = {
+        "metric": "swap (preemption) block copy GB/s between the GPU pool and a pinned host pool",
+        "value": round(gbs(ms_out), 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_out, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg["name"],
+                   "shape": f"{cfg['seqs']} seqs x {cfg['tokens']} tokens, {L} layers, K and V, "
+                            f"{h} kv heads, head_dim {d}, block {b}: {nblk} blocks per layer, "
+                            f"scattered in a {dev_blocks}-block device pool",
+                   "bytes_per_call": nbytes},
+        "swap_out_gbs": round(gbs(ms_out), 1), "swap_in_gbs": round(gbs(ms_in), 1),
+        "swap_out_ms": round(ms_out, 4), "swap_in_ms": round(ms_in, 4),
+        "copy_engine_contiguous_gbs": {"out": round(gbs(ms_ce_out), 1), "in": round(gbs(ms_ce_in), 1)},
+        "device_to_device_gbs": round(gbs(ms_dd), 1),
+        "roofline": {"bound": "c2c", "achieved": round(gbs(ms_out), 1),
+                     "peak": round(gbs(ms_ce_out), 1), "unit": "GB/s",
+                     "frac": round(ms_ce_out / ms_out, 4), "traffic": None,
+                     "peak_source": "measured in this run: one contiguous pinned copy of the same "
+                                    "bytes by the copy engine (device to host)",
+                     "in": {"achieved": round(gbs(ms_in), 1), "peak": round(gbs(ms_ce_in), 1),
+                            "frac": round(ms_ce_in / ms_in, 4)},
+                     "device_to_device_frac_of_hbm": round(2 * gbs(ms_dd) / hbm, 4)},
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 
@@ -679,6 +780,8 @@ def main(argv=None):
     ap.add_argument("--prefill", default=None,
                     choices=["verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16"],
                     help="time pa_prefill on a named multi-token workload instead")
+    ap.add_argument("--swap", action="store_true",
+                    help="time pa_swap_blocks between the GPU pool and a pinned host pool instead")
     ap.add_argument("--kv-dtype", choices=["native", "e4m3"], default="native",
                     help="pool element type: the config's fp16/bf16, or FP8 E4M3 codes (configs 2-5)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -694,6 +797,8 @@ def main(argv=None):
         return run_reference(args)
     if args.prefill:
         return run_prefill(args)
+    if args.swap:
+        return run_swap(args)
     return run_gpu(args)
 
 

@@ -140,6 +140,32 @@ int pa_write_kv(const void* key, const void* value, const int64_t* slot_mapping,
 int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* src_dst_pairs,
                    int64_t num_pairs, void* stream);
 
+/*
+ * pa_swap_blocks - swap for preemption: for every (src, dst) pair and every
+ * layer, block dst of the destination pool becomes a copy of block src of the
+ * source pool, K and V. Swapping out copies a preempted sequence's blocks to
+ * host memory, swapping in copies them back, possibly to other block ids, after
+ * which the caller remaps the sequence's table ("PagedAttention: paging the KV
+ * cache", section "When memory runs out"; learn.pranaymahendrakar.com
+ * "PagedAttention", section "Preemption": copy blocks to pinned host memory and
+ * back). On GB300 the host pool is Grace memory that the kernel reads or
+ * writes directly over NVLink-C2C, so one launch moves any set of scattered
+ * blocks.
+ *   src, dst       host arrays of num_layers pa_cache; each k / v pointer is
+ *                  device memory of the current device, managed memory, or
+ *                  pinned host memory (cudaHostAlloc / cudaHostRegister).
+ *                  Every layer and both sides share dtype, block_size,
+ *                  num_kv_heads and head_dim; num_blocks may differ between
+ *                  the source and the destination. FP8 blocks move as codes.
+ *   src_dst_pairs  int64 [num_pairs][2] in device or pinned host memory
+ * Destinations must be distinct. When src and dst are the same pool, no
+ * destination may also be a source (as pa_copy_blocks). Pageable host memory
+ * returns PA_ERR_ARG before anything is launched. An id outside its pool skips
+ * the pair and sets PA_DEVERR_BLOCK_ID.
+ */
+int pa_swap_blocks(const pa_cache* src, const pa_cache* dst, int32_t num_layers,
+                   const int64_t* src_dst_pairs, int64_t num_pairs, void* stream);
+
 /* Host-side check of copy pairs: ids in range, distinct destinations, no
  * destination used as a source. Returns PA_OK or PA_ERR_PAIRS / PA_ERR_NULL. */
 int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t num_blocks);

@@ -318,6 +318,70 @@ int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* sr
   return PA_OK;
 }
 
+// A pointer the current device can read and write at the same address:
+// device memory of this device, managed memory, or pinned (registered) host
+// memory mapped into the unified address space.
+bool device_reachable(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // a failed query leaves its error behind: clear it
+    return false;
+  }
+  if (at.devicePointer != p) return false;
+  if (at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged) return true;
+  if (at.type != cudaMemoryTypeDevice) return false;
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && at.device == dev;
+}
+
+int pa_swap_blocks(const pa_cache* src, const pa_cache* dst, int32_t num_layers,
+                   const int64_t* src_dst_pairs, int64_t num_pairs, void* stream) {
+  if (num_layers <= 0 || num_pairs < 0) return PA_ERR_ARG;
+  if (src == nullptr || dst == nullptr) return PA_ERR_NULL;
+  for (int32_t l = 0; l < num_layers; ++l) {
+    for (const pa_cache* c : {&src[l], &dst[l]}) {
+      const int rc = check_cache(c);
+      if (rc != PA_OK) return rc;
+      if (c->dtype != src[0].dtype) return PA_ERR_DTYPE;
+      if (c->block_size != src[0].block_size || c->num_kv_heads != src[0].num_kv_heads ||
+          c->head_dim != src[0].head_dim)
+        return PA_ERR_SHAPE;
+    }
+    if (src[l].num_blocks != src[0].num_blocks || dst[l].num_blocks != dst[0].num_blocks)
+      return PA_ERR_SHAPE;
+  }
+  if (num_pairs == 0) return PA_OK;
+  if (src_dst_pairs == nullptr) return PA_ERR_NULL;
+  if (!aligned(src_dst_pairs, 8)) return PA_ERR_ALIGN;
+  const int64_t block_bytes = static_cast<int64_t>(src[0].block_size) * src[0].num_kv_heads *
+                              src[0].head_dim * static_cast<int64_t>(elem_bytes(src[0]));
+  if (num_pairs * ((block_bytes + 32767) / 32768) > 0x7fffffffLL) return PA_ERR_SHAPE;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  // every pool and the pairs must be reachable from this device: no pageable memory
+  if (!device_reachable(src_dst_pairs)) return PA_ERR_ARG;
+  for (int32_t l = 0; l < num_layers; ++l) {
+    if (!device_reachable(src[l].k) || !device_reachable(src[l].v) ||
+        !device_reachable(dst[l].k) || !device_reachable(dst[l].v))
+      return PA_ERR_ARG;
+  }
+  for (int32_t l0 = 0; l0 < num_layers; l0 += pa::kMaxCopyLayers) {
+    const int32_t n = (num_layers - l0) < pa::kMaxCopyLayers ? (num_layers - l0) : pa::kMaxCopyLayers;
+    pa::SwapLayers layers{};
+    for (int32_t i = 0; i < n; ++i) {
+      layers.src_k[i] = src[l0 + i].k;
+      layers.src_v[i] = src[l0 + i].v;
+      layers.dst_k[i] = dst[l0 + i].k;
+      layers.dst_v[i] = dst[l0 + i].v;
+    }
+    const cudaError_t e = pa::launch_swap_blocks(layers, n, src_dst_pairs, num_pairs,
+                                                 src[0].num_blocks, dst[0].num_blocks, block_bytes,
+                                                 di.err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;

@@ -142,7 +142,61 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// Swap for preemption: block src of one pool -> block dst of another, for
+// every pair, layer, K and V ("PagedAttention: paging the KV cache", When
+// memory runs out: swapping copies the evicted blocks to CPU memory and back).
+// On GB300 the host pool is Grace memory that the SMs read and write directly
+// over NVLink-C2C through the unified address space, so one launch gathers or
+// scatters any set of scattered blocks. A CTA moves a 32 KiB piece with 8
+// 16-byte vectors per thread in flight, enough to cover the link's latency.
+constexpr int kSwapUnroll = 8;
+constexpr int64_t kSwapPieceVecs = kCopyThreads * kSwapUnroll;  // 32 KiB per CTA
+
+// grid.x = pair * pieces + piece, grid.y = layer * 2 + (0: K, 1: V).
+__global__ void __launch_bounds__(kCopyThreads)
+    swap_blocks_kernel(const SwapLayers layers, const int64_t* __restrict__ pairs,
+                       int64_t src_blocks, int64_t dst_blocks, int64_t block_vecs, int64_t pieces,
+                       int* err) {
+  const int64_t pair = blockIdx.x / pieces;
+  const int64_t piece = blockIdx.x - pair * pieces;
+  const int64_t src = pairs[2 * pair];
+  const int64_t dst = pairs[2 * pair + 1];
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (threadIdx.x == 0 && piece == 0 && blockIdx.y == 0) atomicOr(err, PA_DEVERR_BLOCK_ID);
+    return;
+  }
+  const int layer = blockIdx.y >> 1;
+  const bool is_v = blockIdx.y & 1;
+  const uint4* from = static_cast<const uint4*>(is_v ? layers.src_v[layer] : layers.src_k[layer]) +
+                      src * block_vecs + piece * kSwapPieceVecs;
+  uint4* to = static_cast<uint4*>(is_v ? layers.dst_v[layer] : layers.dst_k[layer]) +
+              dst * block_vecs + piece * kSwapPieceVecs;
+  const int64_t n = min(kSwapPieceVecs, block_vecs - piece * kSwapPieceVecs);
+  uint4 buf[kSwapUnroll];
+#pragma unroll
+  for (int u = 0; u < kSwapUnroll; ++u) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(u) * kCopyThreads;
+    if (c < n) buf[u] = from[c];
+  }
+#pragma unroll
+  for (int u = 0; u < kSwapUnroll; ++u) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(u) * kCopyThreads;
+    if (c < n) to[c] = buf[u];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(const SwapLayers& layers, int32_t num_layers, const int64_t* pairs,
+                               int64_t num_pairs, int64_t src_blocks, int64_t dst_blocks,
+                               int64_t block_bytes, int* err, cudaStream_t st) {
+  const int64_t block_vecs = block_bytes / 16;
+  const int64_t pieces = (block_vecs + kSwapPieceVecs - 1) / kSwapPieceVecs;
+  dim3 grid(static_cast<unsigned>(num_pairs * pieces), static_cast<unsigned>(2 * num_layers));
+  swap_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(layers, pairs, src_blocks, dst_blocks,
+                                                    block_vecs, pieces, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
                                 const int32_t* seq_idx, const int32_t* positions, int64_t num_tokens,

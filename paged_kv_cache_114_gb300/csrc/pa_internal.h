@@ -131,4 +131,16 @@ cudaError_t launch_copy_blocks(const CopyLayers& layers, int32_t num_layers,
                                const int64_t* pairs, int64_t num_pairs, int64_t num_blocks,
                                int64_t block_bytes, int* err, cudaStream_t st);
 
+// Swap between two pools (either may be pinned host memory reached through
+// the unified address space).
+struct SwapLayers {
+  const void* src_k[kMaxCopyLayers];
+  const void* src_v[kMaxCopyLayers];
+  void* dst_k[kMaxCopyLayers];
+  void* dst_v[kMaxCopyLayers];
+};
+cudaError_t launch_swap_blocks(const SwapLayers& layers, int32_t num_layers, const int64_t* pairs,
+                               int64_t num_pairs, int64_t src_blocks, int64_t dst_blocks,
+                               int64_t block_bytes, int* err, cudaStream_t st);
+
 }  // namespace pa

@@ -136,6 +136,45 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
     _lib.check("pa_copy_blocks", st)
 
 
+def _pool(k_cache: torch.Tensor, v_cache: torch.Tensor) -> _lib.PaCache:
+    """pa_cache for a pool on the GPU or in pinned host memory (for swaps)."""
+    for t in (k_cache, v_cache):
+        _need(t.is_cuda or t.is_pinned(), "swap pools: CUDA tensors or pinned host tensors")
+        _need(t.is_contiguous(), "tensors must be contiguous")
+    _need(k_cache.dim() == 4 and k_cache.shape == v_cache.shape, "k/v caches: [NB, b, H_kv, D], same shape")
+    _need(k_cache.dtype == v_cache.dtype, "k and v share a dtype")
+    nb, b, hkv, d = k_cache.shape
+    if is_fp8_cache(k_cache):
+        return _lib.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, b, hkv, d,
+                            _lib.PA_FP8_E4M3, _lib.PA_F16, 1.0, 1.0)  # codes move as bytes
+    _need(k_cache.dtype in (torch.float16, torch.bfloat16), "caches: float16, bfloat16 or E4M3")
+    code = _DTYPES[k_cache.dtype]
+    return _lib.PaCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, b, hkv, d, code, code, 1.0, 1.0)
+
+
+def swap_blocks(src_k: Sequence[torch.Tensor], src_v: Sequence[torch.Tensor],
+                dst_k: Sequence[torch.Tensor], dst_v: Sequence[torch.Tensor],
+                pairs: torch.Tensor, device: Optional[torch.device] = None) -> None:
+    """For every (src, dst) pair and layer: block dst of the destination pools
+    <- block src of the source pools (K and V). Pools live on the GPU or in
+    pinned host memory (swap out: GPU -> host; swap in: host -> GPU). Runs on
+    the current stream of ``device`` (default: the pairs' device, else the
+    current one)."""
+    n = len(src_k)
+    _need(n > 0 and len(src_v) == n and len(dst_k) == n and len(dst_v) == n,
+          "one k and one v pool per layer on both sides")
+    _need(pairs.dtype == torch.int64 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs: int64 [P, 2]")
+    _need(pairs.is_contiguous() and (pairs.is_cuda or pairs.is_pinned()),
+          "pairs: contiguous, on the GPU or in pinned host memory")
+    if device is None:
+        device = pairs.device if pairs.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    srcs = (_lib.PaCache * n)(*[_pool(k, v) for k, v in zip(src_k, src_v)])
+    dsts = (_lib.PaCache * n)(*[_pool(k, v) for k, v in zip(dst_k, dst_v)])
+    with torch.cuda.device(device):
+        st = _lib.lib().pa_swap_blocks(srcs, dsts, n, _ptr(pairs), pairs.shape[0], _stream(device))
+    _lib.check("pa_swap_blocks", st)
+
+
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                            max_seq_len: int, partition_tokens: int) -> int:
     return int(_lib.lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,

@@ -103,6 +103,14 @@ def test_host_argument_errors_launch_nothing(lib):
     assert lib.pa_write_kv(vp(0), vp(0), vp(0), 1, None, vp(0)) == -1
     assert lib.pa_copy_blocks(None, 1, vp(0), 1, vp(0)) == -1
     assert lib.pa_copy_blocks(None, 0, vp(0), 1, vp(0)) == -6
+    assert lib.pa_swap_blocks(None, None, 1, vp(0), 1, vp(0)) == -1
+    assert lib.pa_swap_blocks(None, None, 0, vp(0), 1, vp(0)) == -6
+    sw_a = L.PaCache(4096, 8192, 64, 16, 8, 128, L.PA_F16, L.PA_F16, 1.0, 1.0)
+    sw_b = L.PaCache(4096, 8192, 64, 16, 8, 128, L.PA_BF16, L.PA_BF16, 1.0, 1.0)
+    sw_c = L.PaCache(4096, 8192, 64, 16, 4, 128, L.PA_F16, L.PA_F16, 1.0, 1.0)
+    assert lib.pa_swap_blocks(ctypes.byref(sw_a), ctypes.byref(sw_b), 1, vp(4096), 1, vp(0)) == -2
+    assert lib.pa_swap_blocks(ctypes.byref(sw_a), ctypes.byref(sw_c), 1, vp(4096), 1, vp(0)) == -3
+    assert lib.pa_swap_blocks(ctypes.byref(sw_a), ctypes.byref(sw_a), 1, vp(0), 0, vp(0)) == 0
     assert lib.pa_slot_mapping(vp(0), 1, 1, vp(0), vp(0), -1, 4, 8, vp(0), vp(0)) == -6
     assert lib.pa_slot_mapping(vp(0), 1, 1, vp(0), vp(0), 0, 4, 8, vp(0), vp(0)) == 0
     # cache checks: dtype, shape and alignment, all on the host
