@@ -38,6 +38,15 @@ Each function is the plain definition of one step, written from the pages:
   ids (pofe.ai §When memory runs out: swapping copies the evicted blocks to
   CPU memory and back; learn.pranaymahendrakar.com §Preemption: copy blocks
   to pinned host memory and back). A copy between two pools.
+* prefix-cache keys: every full block of a sequence gets a content key that
+  covers the whole block-aligned prefix ending with it, so a cache hit is an
+  unbroken chain of matching keys and the first differing token ends the
+  chain (firehose-demo "Paged Attention"; learn.pranaymahendrakar.com
+  §Prefix caching: hash each block-aligned prefix of token ids; only full
+  blocks are keyed, as in ailinkdeeptech.com's allocator). Reading taken:
+  key_j = SHA-256(key_{j-1} || the block's token ids as little-endian int32),
+  key_{-1} = a 32-byte root (zeros by default; a different root, e.g. one per
+  adapter, keeps caches apart, pofe.ai §Fine-tuned models and adapters).
 * an FP8 cache: the same pool with one byte per element, which "halves the
   bytes per block; nothing else about paging changes" (pofe.ai §Fine-tuned
   models and adapters, quantised caches). The pages fix no format or scale, so
@@ -55,6 +64,7 @@ invariants by the CPU tests).
 """
 from __future__ import annotations
 
+import hashlib
 import math
 from typing import Iterable, List, Optional, Sequence, Tuple
 
@@ -206,6 +216,25 @@ def swap_blocks(src_k: Sequence[np.ndarray], src_v: Sequence[np.ndarray],
             vs[layer][int(dst)] = src_v[layer][int(src)]
     return ks, vs
 
+
+
+# ----------------------------------------------------------------------------
+# prefix-cache keys (bytes)
+
+
+def prefix_block_keys(tokens: Sequence[int], block_size: int,
+                      root: Optional[bytes] = None) -> List[bytes]:
+    """Content keys of a sequence's full blocks: key_j = SHA-256(key_{j-1} ||
+    int32 little-endian token ids of block j), key_{-1} = ``root`` (32 zero
+    bytes by default). A trailing partial block gets no key."""
+    parent = bytes(32) if root is None else bytes(root)
+    assert len(parent) == 32
+    keys = []
+    for j in range(len(tokens) // block_size):
+        block = np.asarray(tokens[j * block_size:(j + 1) * block_size], dtype="<i4")
+        parent = hashlib.sha256(parent + block.tobytes()).digest()
+        keys.append(parent)
+    return keys
 
 # ----------------------------------------------------------------------------
 # decode attention (fp64)
