@@ -24,8 +24,11 @@ chunk512_gqa_bf16_b16 or prompt2k_mha_fp16_b16 (tensor-bound).
 out to a pinned host pool and back in, against a contiguous copy of the same
 bytes by the copy engine as the link's reference rate.
 
+--hash times pa_prefix_hash: SHA-256 chain keys of every full block of 4,096
+prompts of 2,048 token ids (b = 16).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--kv-dtype e4m3]
-                       [--impl reference] [--prefill NAME] [--swap]
+                       [--impl reference] [--prefill NAME] [--swap] [--hash]
 """
 from __future__ import annotations
 
@@ -618,6 +621,70 @@ def run_swap(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- prefix keys
+
+# 32-bit integer operations of one SHA-256 compression as FIPS 180-4 writes it:
+# 64 rounds of 26 (Sigma0 5, Sigma1 5, Ch 4, Maj 5, T1 4 adds, T2 1, e 1, a 1),
+# 48 schedule words of 13 (sigma0 5, sigma1 5, 3 adds), 8 final adds.
+SHA256_OPS_PER_COMPRESSION = 64 * 26 + 48 * 13 + 8
+# Integer peak: 152 SMs x 128 INT32 lanes x 2.07 GHz (Blackwell's unified
+# FP32/INT32 cores, every lane able to issue an integer op each clock).
+ALU_PEAK_TOPS = 152 * 128 * 2.07e9 / 1e12
+
+
+def run_hash(args):
+    import torch
+
+    import paged_kv_cache_114_gb300 as pa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    n_seq, n_tok, b = 4096, 2048, 16
+    rng = np.random.default_rng(4000)
+    toks = torch.from_numpy(rng.integers(0, 128000, size=n_seq * n_tok).astype(np.int32)).to(dev)
+    off = torch.arange(0, (n_seq + 1) * n_tok, n_tok, dtype=torch.int64, device=dev)
+    key_off = torch.arange(0, (n_seq + 1) * (n_tok // b), n_tok // b, dtype=torch.int64, device=dev)
+    keys = torch.empty((n_seq * n_tok // b, 32), dtype=torch.uint8, device=dev)
+    call = lambda: pa.prefix_hash(toks, off, b, key_offsets=key_off, out=keys)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for a, e in evs:
+            a.record(stream)
+            call()
+            e.record(stream)
+        torch.cuda.synchronize()
+    if pa.get_device_error(dev):
+        raise RuntimeError("device error in the timed region")
+    ms = statistics.mean(a.elapsed_time(e) for a, e in evs)
+    n_keys = n_seq * n_tok // b
+    words = 8 + b
+    chunks = n_keys * (((words + 3 + 15) // 16))
+    tops = chunks * SHA256_OPS_PER_COMPRESSION / (ms / 1e3) / 1e12
+    line = {
+        "metric": "prefix-cache keys per second (SHA-256 chain over full blocks)",
+        "value": round(n_keys / (ms / 1e3) / 1e6, 2), "unit": "Mkeys/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic",
+        "config": {"workload": "hash4096x2048_b16", "shape": f"{n_seq} prompts x {n_tok} token ids, "
+                   f"block {b}: {n_keys} keys, {chunks} SHA-256 compressions",
+                   "token_bytes": n_seq * n_tok * 4},
+        "token_gbs": round(n_seq * n_tok * 4 / (ms / 1e3) / 1e9, 1),
+        "roofline": {"bound": "alu", "achieved": round(tops, 2), "peak": round(ALU_PEAK_TOPS, 2),
+                     "unit": "Tops/s (32-bit integer)", "frac": round(tops / ALU_PEAK_TOPS, 4),
+                     "traffic": None, "kernel": "prefix_hash_kernel",
+                     "peak_source": "derived: 152 SMs x 128 INT32 lanes x 2.07 GHz",
+                     "ops_per_compression": SHA256_OPS_PER_COMPRESSION},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 
@@ -780,6 +847,8 @@ def main(argv=None):
     ap.add_argument("--prefill", default=None,
                     choices=["verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16"],
                     help="time pa_prefill on a named multi-token workload instead")
+    ap.add_argument("--hash", action="store_true",
+                    help="time pa_prefix_hash on 4,096 prompts of 2,048 token ids instead")
     ap.add_argument("--swap", action="store_true",
                     help="time pa_swap_blocks between the GPU pool and a pinned host pool instead")
     ap.add_argument("--kv-dtype", choices=["native", "e4m3"], default="native",
@@ -799,6 +868,8 @@ def main(argv=None):
         return run_prefill(args)
     if args.swap:
         return run_swap(args)
+    if args.hash:
+        return run_hash(args)
     return run_gpu(args)
 
 

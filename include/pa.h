@@ -166,6 +166,34 @@ int pa_copy_blocks(const pa_cache* caches, int32_t num_layers, const int64_t* sr
 int pa_swap_blocks(const pa_cache* src, const pa_cache* dst, int32_t num_layers,
                    const int64_t* src_dst_pairs, int64_t num_pairs, void* stream);
 
+/*
+ * pa_prefix_hash - prefix-cache keys of every full block of a batch of
+ * sequences, for automatic prefix caching: a cached block is found again by
+ * its key, a hit needs an unbroken chain of matching keys from position zero,
+ * and the first differing token ends the chain (firehose-demo "Paged
+ * Attention"; learn.pranaymahendrakar.com "PagedAttention", section "Prefix
+ * caching": hash each block-aligned prefix of token ids). The pages fix no
+ * function; this library computes
+ *   key_j = SHA-256(key_{j-1} || token ids of block j as int32 little-endian),
+ *   key_{-1} = root,
+ * SHA-256 as FIPS 180-4 defines it. A trailing partial block gets no key.
+ *   token_ids      device int32, the sequences' ids back to back
+ *   token_offsets  device int64 [num_seqs + 1]: sequence s owns ids
+ *                  token_offsets[s] .. token_offsets[s+1] - 1
+ *   key_offsets    device int64 [num_seqs + 1]: sequence s writes keys
+ *                  key_offsets[s] .. key_offsets[s+1] - 1, which must number
+ *                  floor(length_s / block_size)
+ *   root           host, 32 bytes, or NULL for 32 zero bytes (a distinct root,
+ *                  e.g. per adapter, keeps caches apart)
+ *   keys           device [key_offsets[num_seqs]][32] bytes (digest byte
+ *                  order), 16-byte aligned
+ * Errors (device): a negative length or a key range of the wrong size sets
+ * PA_DEVERR_SEQ_LEN and the sequence writes nothing.
+ */
+int pa_prefix_hash(const int32_t* token_ids, const int64_t* token_offsets,
+                   const int64_t* key_offsets, int32_t num_seqs, int32_t block_size,
+                   const uint8_t* root, uint8_t* keys, void* stream);
+
 /* Host-side check of copy pairs: ids in range, distinct destinations, no
  * destination used as a source. Returns PA_OK or PA_ERR_PAIRS / PA_ERR_NULL. */
 int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t num_blocks);

@@ -8,6 +8,7 @@ C ABI, declared in ``include/pa.h``); this package is its Python binding.
 * :func:`copy_blocks` - whole-block copies for copy-on-write;
 * :func:`swap_blocks` - block copies between the GPU pool and a pinned host
   pool, for preemption by swapping;
+* :func:`prefix_hash` - prefix-cache keys of full blocks (SHA-256 chain);
 * :func:`decode` - decode attention through block tables (single pass,
   split-K with a reduce, or a balanced split), GQA heads packed per KV head;
 * :class:`DecodeStep` - the three calls bound to fixed buffers for loops.
@@ -18,7 +19,7 @@ from ._lib import PA_PARTITION_BALANCED, STATIC_WORKSPACE_BYTES
 from .step import DecodeStep
 from .ops import (check_copy_pairs, copy_blocks, decode, decode_kernel_name, decode_static_workspace,
                   decode_workspace_bytes, default_partition, get_device_error, make_cache,
-                  new_workspace, prefill, slot_mapping, swap_blocks, write_kv)
+                  new_workspace, prefill, prefix_hash, slot_mapping, swap_blocks, write_kv)
 
 __all__ = [
     "DEVERR_BLOCK_ID", "DEVERR_POSITION", "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
@@ -26,5 +27,5 @@ __all__ = [
     "decode_workspace_bytes", "default_partition", "get_device_error", "make_cache",
     "slot_mapping", "write_kv", "decode_static_workspace", "STATIC_WORKSPACE_BYTES",
     "PA_PARTITION_BALANCED", "new_workspace", "DecodeStep", "decode_kernel_name",
-    "prefill", "swap_blocks",
+    "prefill", "swap_blocks", "prefix_hash",
 ]

@@ -27,7 +27,7 @@ EXPORTED = (
     "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_check_copy_pairs", "pa_decode",
     "pa_decode_workspace_bytes", "pa_decode_default_partition", "pa_get_device_error",
     "pa_status_string", "pa_abi_version", "pa_decode_static_workspace", "pa_decode_kernel_name",
-    "pa_prefill", "pa_swap_blocks",
+    "pa_prefill", "pa_swap_blocks", "pa_prefix_hash",
 )
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
@@ -67,6 +67,7 @@ def _declare(lib):
         "pa_write_kv": (ctypes.c_int, [vp, vp, vp, i64, cache_p, vp]),
         "pa_copy_blocks": (ctypes.c_int, [cache_p, i32, vp, i64, vp]),
         "pa_swap_blocks": (ctypes.c_int, [cache_p, cache_p, i32, vp, i64, vp]),
+        "pa_prefix_hash": (ctypes.c_int, [vp, vp, vp, i32, i32, ctypes.c_char_p, vp, vp]),
         "pa_check_copy_pairs": (ctypes.c_int, [vp, i64, i64]),
         "pa_decode": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32, ctypes.c_float, vp,
                                      ctypes.c_int, i32, vp, sz, vp]),

@@ -31,7 +31,8 @@ COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxa
 def _units():
     units = [("pa_api", "pa_api.cu", []), ("pa_cache_ops", "pa_cache_ops.cu", []),
              ("pa_decode_reduce", "pa_decode_reduce.cu", []),
-             ("pa_noalloc", "pa_noalloc.cu", []), ("pa_prefill", "pa_prefill.cu", [])]
+             ("pa_noalloc", "pa_noalloc.cu", []), ("pa_prefill", "pa_prefill.cu", []),
+             ("pa_prefix_hash", "pa_prefix_hash.cu", [])]
     for bf in (0, 1):
         for d in (64, 128, 256):
             tag = f"pa_decode_{'bf16' if bf else 'f16'}_{d}"

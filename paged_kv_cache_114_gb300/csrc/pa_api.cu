@@ -382,6 +382,30 @@ int pa_swap_blocks(const pa_cache* src, const pa_cache* dst, int32_t num_layers,
   return PA_OK;
 }
 
+int pa_prefix_hash(const int32_t* token_ids, const int64_t* token_offsets,
+                   const int64_t* key_offsets, int32_t num_seqs, int32_t block_size,
+                   const uint8_t* root, uint8_t* keys, void* stream) {
+  if (num_seqs < 0) return PA_ERR_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!token_ids || !token_offsets || !key_offsets || !keys) return PA_ERR_NULL;
+  if (block_size <= 0 || block_size > 4096) return PA_ERR_SHAPE;
+  if (!aligned(token_ids, 4) || !aligned(token_offsets, 8) || !aligned(key_offsets, 8) ||
+      !aligned(keys, 16))
+    return PA_ERR_ALIGN;
+  pa::Sha256Root r{};
+  for (int i = 0; i < 8; ++i) {  // the root's bytes, read as big-endian words
+    uint32_t w = 0;
+    for (int j = 0; j < 4; ++j) w = (w << 8) | (root ? root[4 * i + j] : 0u);
+    r.w[i] = w;
+  }
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  const cudaError_t e = pa::launch_prefix_hash(token_ids, token_offsets, key_offsets, num_seqs,
+                                               block_size, r, keys, di.err,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;

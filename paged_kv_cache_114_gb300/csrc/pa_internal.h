@@ -143,4 +143,19 @@ cudaError_t launch_swap_blocks(const SwapLayers& layers, int32_t num_layers, con
                                int64_t num_pairs, int64_t src_blocks, int64_t dst_blocks,
                                int64_t block_bytes, int* err, cudaStream_t st);
 
+// Prefix-cache keys (pa_prefix_hash.cu): SHA-256 constants of FIPS 180-4
+// (derived from the primes at first use) and a 32-byte root as 8 big-endian
+// words.
+struct Sha256Consts {
+  uint32_t k[64];
+  uint32_t h0[8];
+};
+struct Sha256Root {
+  uint32_t w[8];
+};
+const Sha256Consts& sha256_consts();
+cudaError_t launch_prefix_hash(const int32_t* tokens, const int64_t* tok_off, const int64_t* key_off,
+                               int32_t num_seqs, int32_t block_size, const Sha256Root& root,
+                               uint8_t* keys, int* err, cudaStream_t st);
+
 }  // namespace pa

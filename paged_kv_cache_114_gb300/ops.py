@@ -175,6 +175,39 @@ def swap_blocks(src_k: Sequence[torch.Tensor], src_v: Sequence[torch.Tensor],
     _lib.check("pa_swap_blocks", st)
 
 
+def prefix_hash(token_ids: torch.Tensor, token_offsets: torch.Tensor, block_size: int, *,
+                key_offsets: Optional[torch.Tensor] = None, root: Optional[bytes] = None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prefix-cache keys of every full block: key_j = SHA-256(key_{j-1} ||
+    int32 ids of block j), key_{-1} = ``root`` (32 bytes, zeros by default).
+    ``token_offsets`` (int64 [N + 1]) splits ``token_ids`` (int32) into
+    sequences; returns uint8 [sum_s floor(len_s / block_size), 32]. Without
+    ``key_offsets`` they are computed here from the lengths (one copy of the
+    offsets to the host)."""
+    dev = _cuda(token_ids, token_offsets)
+    _need(token_ids.dtype == torch.int32 and token_ids.dim() == 1, "token_ids: int32 [T]")
+    _need(token_offsets.dtype == torch.int64 and token_offsets.dim() == 1, "token_offsets: int64 [N + 1]")
+    n = token_offsets.shape[0] - 1
+    if key_offsets is None:
+        lens = torch.diff(token_offsets.cpu())
+        key_offsets = torch.cat([torch.zeros(1, dtype=torch.int64),
+                                 torch.cumsum(lens // block_size, 0)]).to(dev)
+    _cuda(key_offsets, token_ids)
+    _need(key_offsets.dtype == torch.int64 and key_offsets.shape == token_offsets.shape,
+          "key_offsets: int64 [N + 1]")
+    if out is None:
+        total = int(key_offsets[-1].item()) if n > 0 else 0
+        out = torch.empty((total, 32), dtype=torch.uint8, device=dev)
+    _cuda(out, token_ids)
+    _need(out.dtype == torch.uint8 and out.dim() == 2 and out.shape[1] == 32, "out: uint8 [K, 32]")
+    _need(root is None or len(root) == 32, "root: 32 bytes")
+    st = _lib.lib().pa_prefix_hash(_ptr(token_ids), _ptr(token_offsets), _ptr(key_offsets), n,
+                                   int(block_size), None if root is None else bytes(root),
+                                   _ptr(out), _stream(dev))
+    _lib.check("pa_prefix_hash", st)
+    return out
+
+
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                            max_seq_len: int, partition_tokens: int) -> int:
     return int(_lib.lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
