@@ -32,7 +32,8 @@ def _units():
     units = [("pa_api", "pa_api.cu", []), ("pa_cache_ops", "pa_cache_ops.cu", []),
              ("pa_decode_reduce", "pa_decode_reduce.cu", []),
              ("pa_noalloc", "pa_noalloc.cu", []), ("pa_prefill", "pa_prefill.cu", []),
-             ("pa_prefix_hash", "pa_prefix_hash.cu", [])]
+             ("pa_prefix_hash", "pa_prefix_hash.cu", []),
+             ("pa_prefill_tc", "pa_prefill_tc.cu", [])]
     for bf in (0, 1):
         for d in (64, 128, 256):
             tag = f"pa_decode_{'bf16' if bf else 'f16'}_{d}"

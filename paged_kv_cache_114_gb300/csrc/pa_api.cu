@@ -511,10 +511,23 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
       !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
     return PA_ERR_CUDA;
-  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
-                  static_cast<unsigned>(num_seqs));
-  const cudaError_t e = pa::launch_prefill(tk, tv, a, D, cache->dtype == PA_BF16, grid,
-                                           static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
+      aligned(out, 16)) {
+    // 5th-generation tensor cores: 256 (query, head) rows per CTA, S and O in
+    // TMEM. Batches of fewer rows per KV head (speculative verification of a few
+    // drafts) stay on the 64-row kernel, whose tiles they fill.
+    const int64_t tiles256 = (static_cast<int64_t>(max_q_len) * g + 255) / 256;
+    const dim3 grid(static_cast<unsigned>(tiles256), static_cast<unsigned>(hkv),
+                    static_cast<unsigned>(num_seqs));
+    e = pa::launch_prefill_tc(tk, tv, a, cache->dtype == PA_BF16, grid,
+                              static_cast<cudaStream_t>(stream));
+  } else {
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
+                    static_cast<unsigned>(num_seqs));
+    e = pa::launch_prefill(tk, tv, a, D, cache->dtype == PA_BF16, grid,
+                           static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
