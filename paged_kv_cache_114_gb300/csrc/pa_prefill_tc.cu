@@ -16,8 +16,10 @@
 //   P_t  = exp2(S_t * scale*log2e - m)   online softmax, one row per thread
 //   O   += P_t V_t     tcgen05.mma M=128 N=128 K=64, V MN-major
 // TMEM: row tile q uses columns 256q .. 256q+255 - S double-buffered in the
-// first 128, O in the last 128. P goes through shared memory in the MMA's
-// 128-byte swizzled layout. Warps 0-3 run the softmax of tile A and warps 4-7
+// first 128, O in the last 128. P never leaves tensor memory: the softmax
+// writes P_t over its own S buffer (bf16/fp16 pairs, 32 columns per part) and
+// the PV MMA takes its A operand from there; S_{t+2} reuses the buffer only
+// after PV_t, in the MMA warp's issue order. Warps 0-3 run the softmax of tile A and warps 4-7
 // that of tile B (warp w owns TMEM lanes 32 (w % 4) ..), so every SM
 // sub-partition alternates two independent softmax warps; warp 8 issues the
 // TMA copies of K/V tiles (one box of 64 head-dim elements x block piece per
@@ -26,8 +28,8 @@
 // computes the next scores while the softmax works.
 //
 // The running maximum rises only when a row's maximum exceeds it by more than
-// 8 (log2 units); then the softmax warp rescales its rows of O in TMEM after
-// the previous O update. p stays below 2^8. A bf16 P carries only 8
+// 8 (log2 units); then the softmax warp waits for the previous O update and
+// rescales its rows of O in TMEM. p stays below 2^8. A bf16 P carries only 8
 // significant bits, so for bf16 inputs P is split into a high and a low bf16
 // part, O += P_hi V + P_lo V, keeping about 16 bits of each weight; an fp16 P
 // (11 bits) is used whole.
@@ -50,7 +52,7 @@ constexpr int kD = 128;            // head dim
 constexpr int kRowsTc = 128;       // query rows per row tile (TMEM lanes)
 constexpr int kQTiles = 2;         // row tiles per CTA
 constexpr int kBn = 64;            // tokens per K/V tile
-constexpr int kStagesTc = 3;       // K/V tiles in flight
+constexpr int kStagesTc = 4;       // K/V tiles in flight
 constexpr int kSoftmaxWarps = 4 * kQTiles;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
@@ -64,12 +66,13 @@ struct TcSmem {
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kStage = 4 * kHalf;                 // K halves, then V halves
   static constexpr uint32_t kStages = kQ + kQTiles * kQTile;
-  // P: per row tile, (high, low) parts of 128 rows x 128 B
-  static constexpr uint32_t kPBytes = kRowsTc * 128;
-  static constexpr uint32_t kP = kStages + kStagesTc * kStage;
-  static constexpr uint32_t kBar = kP + kQTiles * 2 * kPBytes;
-  // kv_full[NS], kv_empty[NS], s_full[2 tiles][2], p_full[2], o_done[2], final
-  static constexpr uint32_t kNumBars = 2 * kStagesTc + 4 + 2 + 2 + 1;
+  static constexpr uint32_t kBar = kStages + kStagesTc * kStage;
+  // kv_full[NS], kv_empty[NS], s_full[2 tiles][2], p_full[2 tiles][2],
+  // o_done[2 tiles][2], final. p_full and o_done alternate by tile parity: a
+  // softmax warp may publish P_{t+1} before the MMA warp waits for P_t, and
+  // waits on o_done only now and then, so a single barrier could run two
+  // phases ahead of its waiter, where parity waits alias.
+  static constexpr uint32_t kNumBars = 2 * kStagesTc + 4 + 4 + 4 + 1;
   static constexpr uint32_t kMask = kBar + kNumBars * 8;        // uint64 per stage
   static constexpr uint32_t kMisc = kMask + kStagesTc * 8;      // tmem base, abort flag
   static constexpr uint32_t kTotal = kMisc + 16 + 1024;         // + base-alignment slack
@@ -101,6 +104,16 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// The same with the A operand in tensor memory (row m in lane m, 16-bit pairs
+// per 32-bit column).
+__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -165,6 +178,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 32 packed 32-bit words into consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -184,12 +209,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while
+// the phase is incomplete, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait that also gives up once another role of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile uint32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (*abort != 0u || globaltimer_ns() - t0 > kLimitTcNs) return false;
   }
   return true;
@@ -240,9 +280,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   auto kv_full = [&](int k) { return bar + 8u * k; };
   auto kv_empty = [&](int k) { return bar + 8u * (kStagesTc + k); };
   auto s_full = [&](int q, int b) { return bar + 8u * (2 * kStagesTc + 2 * q + b); };
-  auto p_full = [&](int q) { return bar + 8u * (2 * kStagesTc + 4 + q); };
-  auto o_done = [&](int q) { return bar + 8u * (2 * kStagesTc + 6 + q); };
-  const uint32_t fin = bar + 8u * (2 * kStagesTc + 8);
+  auto p_full = [&](int q, int b) { return bar + 8u * (2 * kStagesTc + 4 + 2 * q + b); };
+  auto o_done = [&](int q, int b) { return bar + 8u * (2 * kStagesTc + 8 + 2 * q + b); };
+  const uint32_t fin = bar + 8u * (2 * kStagesTc + 12);
   uint64_t* masks = reinterpret_cast<uint64_t*>(sm + S::kMask);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kMisc);
   volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(sm + S::kMisc + 4);
@@ -255,8 +295,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int q = 0; q < kQTiles; ++q) {
       mbar_init(s_full(q, 0), 1);
       mbar_init(s_full(q, 1), 1);
-      mbar_init(p_full(q), 4);
-      mbar_init(o_done(q), 1);
+      mbar_init(p_full(q, 0), 4);
+      mbar_init(p_full(q, 1), 4);
+      mbar_init(o_done(q, 0), 1);
+      mbar_init(o_done(q, 1), 1);
     }
     mbar_init(fin, 1);
     *abort = 0u;
@@ -359,19 +401,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       umma_commit(s_full(q, t & 1));
     };
-    auto issue_pv = [&](int q, int t) {  // O += P_t V_t of row tile q
+    auto issue_pv = [&](int q, int t) {  // O += P_t V_t of row tile q, P_t read from TMEM
       const uint32_t v_addr = base + S::kStages + (t % kStagesTc) * S::kStage + 2 * S::kHalf;
+      const uint32_t p_col = tmem + q * 256u + (t & 1) * kBn;
 #pragma unroll
       for (int part = 0; part < (IS_BF16 ? 2 : 1); ++part) {
-        const uint32_t p_addr = base + S::kP + (q * 2 + part) * S::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kBn / 16; ++kk) {
-          umma(tmem + q * 256u + 2 * kBn, umma_desc(p_addr + kk * 32u, 16, 1024),
-               umma_desc(v_addr + kk * 16u * 128u, S::kHalf, 1024), id_o,
-               (t > 0 || part > 0 || kk > 0) ? 1u : 0u);
+          umma_tmem_a(tmem + q * 256u + 2 * kBn, p_col + part * (kBn / 2) + kk * 8u,
+                      umma_desc(v_addr + kk * 16u * 128u, S::kHalf, 1024), id_o,
+                      (t > 0 || part > 0 || kk > 0) ? 1u : 0u);
         }
       }
-      umma_commit(o_done(q));
+      umma_commit(o_done(q, t & 1));
     };
     bool ok = true;
     if (lane == 0) {
@@ -392,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         for (int q = 0; ok && q < kQTiles; ++q) {
           if (t >= nt[q]) continue;
-          ok = wait_or_abort(p_full(q), t & 1, abort);
+          ok = wait_or_abort(p_full(q, t & 1), (t >> 1) & 1, abort);
           if (!ok) break;
           tc_fence_after();
           issue_pv(q, t);
@@ -464,10 +506,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const float m_new = grow ? mx : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = grow ? exp2f(m - m_use) : 1.f;
-      // the previous O update of this tile must be complete before its P
-      // buffer is rewritten and before O is rescaled
-      if (t > 0 && !wait_or_abort(o_done(q), (t - 1) & 1, abort)) { ok = false; break; }
+      // O is rescaled only after the previous O update of this tile completed
       if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) {
+        if (!wait_or_abort(o_done(q, (t - 1) & 1), ((t - 1) >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kD; c += 32) {
@@ -499,15 +540,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int c = 0; c < w; ++c) ps[c] += ps[c + w];
       }
       l = l * alpha + ps[0];
-      const uint32_t prow = S::kP + q * 2 * S::kPBytes + r * 128u;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4*>(sm + prow + (((c ^ (r & 7))) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        if constexpr (IS_BF16)
-          *reinterpret_cast<uint4*>(sm + prow + S::kPBytes + (((c ^ (r & 7))) << 4)) =
-              make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
-      }
+      // P over this tile's S buffer: high part in its first 32 columns, low part next
+      tmem_st32u(s_col + (t & 1) * kBn, pk);
+      if constexpr (IS_BF16) tmem_st32u(s_col + (t & 1) * kBn + kBn / 2, pl);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       // tokens without valid data: zero their V rows so 0 * garbage never
       // enters O (each row tile's warps zero the rows; the writes are equal)
       if (vmask != ~0ull) {
@@ -523,13 +559,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(q));
+      if (lane == 0) mbar_arrive(p_full(q, t & 1));
     }
     if (!ok) {
       if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
     } else if (my_tiles > 0) {
       // ---- epilogue: O / l once the last P V has completed
-      if (wait_or_abort(o_done(q), (my_tiles - 1) & 1, abort)) {
+      if (wait_or_abort(o_done(q, (my_tiles - 1) & 1), ((my_tiles - 1) >> 1) & 1, abort)) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t ob = row_ok ? ((static_cast<int64_t>(q0) + i) * a.num_q_heads +
