@@ -52,7 +52,7 @@ SPEC_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 KERNEL_SOURCES = ["pa_decode.cuh", "pa_decode_grouped.cuh", "pa_ptx.cuh", "pa_decode_reduce.cu",
-                  "pa_decode_inst.cu", "pa_internal.h"]
+                  "pa_decode_inst.cu"]
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -116,10 +116,18 @@ def measured_peaks():
 
 
 def kernel_hash():
+    """Hash of what the decode kernels are built from: their sources and the
+    DecodeArgs struct they take (other declarations in the shared internal
+    header do not change them)."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_114_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_114_gb300", "csrc", name), "rb") as f:
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(csrc, "pa_internal.h")) as f:
+        text = f.read()
+    start = text.index("struct DecodeArgs")
+    h.update(text[start:text.index("};", start)].encode())
     return h.hexdigest()[:16]
 
 
