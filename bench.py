@@ -446,7 +446,7 @@ def prefill_bytes(w, out_elem=4):
     the table entries and q_start / lengths."""
     L = w.seq_lens.astype(np.int64)
     t = int(w.q_start[-1])
-    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * 2 * kv_elem(w)
     q = t * w.num_q_heads * w.head_dim * 2
     out = t * w.num_q_heads * w.head_dim * out_elem
     return kv + q + out + int((-(-L // w.block_size)).sum()) * 4 + 8 * w.num_seqs
@@ -460,20 +460,22 @@ def run_prefill(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     pa.lib()
-    w = make_prefill_config(args.prefill)
-    k = to_dev(w.k_cache, dev, w.dtype)
-    v = to_dev(w.v_cache, dev, w.dtype)
+    w = make_prefill_config(args.prefill, kv_dtype="e4m3" if args.kv_dtype == "e4m3" else None)
+    fp8 = w.kv_dtype == "e4m3"
+    k = to_dev(w.k_cache, dev, None if fp8 else w.dtype)
+    v = to_dev(w.v_cache, dev, None if fp8 else w.dtype)
+    sc = {"k_scale": w.k_scale, "v_scale": w.v_scale} if fp8 else {}
     tables, lens = to_dev(w.block_tables, dev), to_dev(w.seq_lens, dev)
     slots = pa.slot_mapping(tables, to_dev(w.seq_idx, dev), to_dev(w.positions, dev),
                             w.block_size, w.num_blocks)
-    pa.write_kv(to_dev(w.key, dev, w.dtype), to_dev(w.value, dev, w.dtype), slots, k, v)
+    pa.write_kv(to_dev(w.key, dev, w.dtype), to_dev(w.value, dev, w.dtype), slots, k, v, **sc)
     q = to_dev(w.q, dev, w.dtype)
     q_start = to_dev(w.q_start, dev)
     out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
     max_q = int(np.diff(w.q_start).max())
 
     def call():
-        pa.prefill(q, k, v, tables, lens, q_start, w.scale, max_q_len=max_q, out=out)
+        pa.prefill(q, k, v, tables, lens, q_start, w.scale, max_q_len=max_q, out=out, **sc)
 
     for _ in range(args.warmup):
         call()
@@ -503,11 +505,14 @@ def run_prefill(args):
     except Exception:
         tc_peak, tc_kind = 1900.0, "fallback"
     hbm_bound = args.prefill.startswith("verify")
+    kernel = ("prefill_tc_kernel" if (not fp8 and w.head_dim == 128 and
+                                      int(np.diff(w.q_start).max()) * w.group >= 128)
+              else "prefill_kernel")
     roofline = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                  "frac": round(gbs / hbm, 4)} if hbm_bound else
                 {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak, "unit": "TFLOP/s",
                  "frac": round(tflops / tc_peak, 4)})
-    roofline.update({"traffic": None, "kernel": "prefill_kernel", "mean_call_us": round(ms * 1e3, 2),
+    roofline.update({"traffic": None, "kernel": kernel, "mean_call_us": round(ms * 1e3, 2),
                      "peak_source": f"{tc_kind if not hbm_bound else 'measured'} "
                                     f"(MEASURED_PEAKS.json {'hbm_gbs' if hbm_bound else 'bf16_tflops'})"})
     qn = np.diff(w.q_start)
@@ -515,9 +520,9 @@ def run_prefill(args):
         "metric": "paged prefill attention throughput (multi-token causal, one layer)",
         "value": round(gbs if hbm_bound else tflops, 2), "unit": "GB/s" if hbm_bound else "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic",
-        "config": {"workload": w.name,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.kv_dtype or w.dtype, "data": "synthetic",
+        "config": {"workload": w.name + ("_e4m3" if fp8 else ""), "kv_dtype": w.cache_dtype,
                    "shape": f"{w.num_seqs} seqs, {w.num_q_heads} q heads / {w.num_kv_heads} kv heads, "
                             f"head_dim {w.head_dim}, block {w.block_size}, seq_len "
                             f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}, new tokens "

@@ -260,10 +260,12 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
  * The K/V of all L_s positions, the new ones included, must already be in
  * the cache (pa_slot_mapping + pa_write_kv first). Decode is the case n_s = 1.
  *   q            device [q_start[num_seqs]][num_q_heads][head_dim], cache dtype
+ *                (act_dtype for FP8 caches)
  *   q_start      device int32 [num_seqs + 1], non-decreasing, q_start[0] = 0
  *   max_q_len    host upper bound of every n_s (sizes the launch)
- *   cache        host pointer to one pa_cache (fp16 or bf16; an FP8 cache
- *                returns PA_ERR_DTYPE); head_dim 64, 128 or 256;
+ *   cache        host pointer to one pa_cache; head_dim 64, 128 or 256 (128
+ *                or 256 for FP8 caches, whose q is act_dtype and whose K/V
+ *                rows are the codes' values times k_scale / v_scale);
  *                block_size >= 8 and a divisor or a multiple of 64
  *   block_tables device int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens     device int32 [num_seqs]

@@ -468,7 +468,7 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
                pa_dtype out_dtype, void* stream) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
-  if (is_fp8(*cache)) return PA_ERR_DTYPE;
+  const bool fp8 = is_fp8(*cache);
   if (num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
   if (num_seqs == 0 || max_q_len == 0) return PA_OK;
@@ -478,6 +478,7 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   const int b = cache->block_size;
   const int hkv = cache->num_kv_heads;
   if (D != 64 && D != 128 && D != 256) return PA_ERR_SHAPE;
+  if (fp8 && D == 64) return PA_ERR_SHAPE;
   if (b < 8 || !(64 % b == 0 || b % 64 == 0)) return PA_ERR_SHAPE;
   if (num_q_heads % hkv != 0) return PA_ERR_SHAPE;
   if (num_seqs > 65535 || hkv > 65535) return PA_ERR_SHAPE;
@@ -503,7 +504,11 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   a.tok_per_op = b < 64 ? b : 64;
   a.ops_per_stage = 64 / a.tok_per_op;
   a.out_dtype = out_dtype;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // E4M3: the logit of code row c is scale * k_scale * (q . value(c))
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) *
+                                    (fp8 ? static_cast<double>(cache->k_scale) : 1.0) *
+                                    1.4426950408889634);
+  a.v_scale = fp8 ? cache->v_scale : 1.f;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   a.err = di.err;
@@ -512,7 +517,8 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
       !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
     return PA_ERR_CUDA;
   cudaError_t e;
-  if (D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
+  const bool act_bf16 = (fp8 ? cache->act_dtype : cache->dtype) == PA_BF16;
+  if (!fp8 && D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
       aligned(out, 16)) {
     // 5th-generation tensor cores: 256 (query, head) rows per CTA, S and O in
     // TMEM. Batches of fewer rows per KV head (speculative verification of a few
@@ -520,13 +526,11 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
     const int64_t tiles256 = (static_cast<int64_t>(max_q_len) * g + 255) / 256;
     const dim3 grid(static_cast<unsigned>(tiles256), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));
-    e = pa::launch_prefill_tc(tk, tv, a, cache->dtype == PA_BF16, grid,
-                              static_cast<cudaStream_t>(stream));
+    e = pa::launch_prefill_tc(tk, tv, a, act_bf16, grid, static_cast<cudaStream_t>(stream));
   } else {
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));
-    e = pa::launch_prefill(tk, tv, a, D, cache->dtype == PA_BF16, grid,
-                           static_cast<cudaStream_t>(stream));
+    e = pa::launch_prefill(tk, tv, a, D, act_bf16, fp8, grid, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -98,11 +98,13 @@ struct PrefillArgs {
   int32_t tok_per_op;            // tokens one TMA box covers: min(block_size, 64)
   int32_t ops_per_stage;         // boxes per 64-token stage
   int32_t out_dtype;             // pa_dtype
-  float scale_log2;              // scale * log2(e)
+  float scale_log2;              // scale * log2(e) (times k_scale for E4M3 caches)
+  float v_scale;                 // E4M3 caches: V code c stands for value(c) * v_scale
 };
-// Grid: (ceil(max_q_len * g / 64), H_kv, N).
+// Grid: (ceil(max_q_len * g / 64), H_kv, N). bf16: q/out MMA type (the act
+// dtype for E4M3 caches); fp8: E4M3 cache (head_dim 128 or 256).
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                           int head_dim, bool bf16, dim3 grid, cudaStream_t st);
+                           int head_dim, bool bf16, bool fp8, dim3 grid, cudaStream_t st);
 // tcgen05/TMEM kernel for head_dim 128 (pa_prefill_tc.cu). Grid: (ceil(max_q_len * g / 256),
 // H_kv, N); needs out 16-byte aligned.
 cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,

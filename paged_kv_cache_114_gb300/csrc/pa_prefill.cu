@@ -26,6 +26,17 @@
 // Rows of a stage that hold no valid token (past the CTA's last position, or
 // of a block whose id is out of range) have their V rows zeroed before PV, so
 // stale or NaN bytes never reach the output.
+//
+// FP8 (E4M3) caches: a stage row is D bytes, one 128-byte swizzled line per
+// 128 head-dim codes. ldmatrix treats byte pairs as its 16-bit elements: for
+// S = Q K^T each lane gets four consecutive codes of a token, so the MMA's
+// reduction index runs over head-dim elements four at a time (q is loaded in
+// that order); for O = P V the transposing ldmatrix gives two dims of two
+// tokens, and one byte permute pairs the tokens per dim, the two dims landing
+// in two n-tiles of O. Codes widen exactly to fp16 (cvt.rn.f16x2.e4m3x2) and
+// every MMA runs in fp16; a bf16 query row becomes fp16 times a power of two
+// that keeps its largest element below 2^14, undone in the row's logit scale.
+// k_scale folds into the logit scale, v_scale multiplies the output.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,9 +56,9 @@ constexpr int prefill_stages() {
   return D == 64 ? 4 : (D == 128 ? 3 : 2);
 }
 
-template <int D, int NS>
+template <int D, int NS, bool FP8>
 struct PrefillSmem {
-  static constexpr int kHalves = D / 64;
+  static constexpr int kHalves = D / (FP8 ? 128 : 64);
   static constexpr uint32_t kPlane = kTok * 128;               // 64 rows of one column half
   static constexpr uint32_t kStage = 2 * kHalves * kPlane;     // K planes then V planes
   static constexpr uint32_t kBar = NS * kStage;                // full[NS], empty[NS]
@@ -74,12 +85,13 @@ __device__ __forceinline__ uint32_t swz(uint32_t planes, int t, int c8) {
 // Warp-wide issue of stage `it` (tokens it*64 ..) into ring slot `slot`: lane
 // j < ops_per_stage copies block piece j if it starts at or before max_pos.
 // Lane 0 records the stage's valid-row mask and arms the full barrier.
-template <int D, int NS>
+template <int D, int NS, bool FP8>
 __device__ __forceinline__ void issue_prefill_stage(const PrefillArgs& a, const CUtensorMap* tmk,
                                                     const CUtensorMap* tmv, int64_t table_row,
                                                     int kvh, int it, int max_pos, uint32_t base,
                                                     uint32_t full0, uint64_t* masks, int lane) {
-  using S = PrefillSmem<D, NS>;
+  using S = PrefillSmem<D, NS, FP8>;
+  constexpr int PE = FP8 ? 128 : 64;  // head-dim elements per 128-byte line
   const int slot = it % NS;
   const int tpo = a.tok_per_op;
   const int t0 = it * kTok;
@@ -105,7 +117,8 @@ __device__ __forceinline__ void issue_prefill_stage(const PrefillArgs& a, const 
     const int last = max_pos - t0;  // rows 0 .. last are at or before max_pos
     if (last < kTok - 1) m &= (1ull << (last + 1)) - 1ull;
     masks[slot] = m;
-    mbar_arrive_expect_tx(full0 + 8 * slot, static_cast<uint32_t>(__popc(okmask)) * tpo * D * 4u);
+    mbar_arrive_expect_tx(full0 + 8 * slot,
+                          static_cast<uint32_t>(__popc(okmask)) * tpo * D * (FP8 ? 2u : 4u));
   }
   __syncwarp();
   if (ok) {
@@ -113,17 +126,18 @@ __device__ __forceinline__ void issue_prefill_stage(const PrefillArgs& a, const 
     const uint32_t dv = dk + S::kHalves * S::kPlane;
 #pragma unroll
     for (int c = 0; c < S::kHalves; ++c) {
-      tma_load_4d(dk + c * S::kPlane, tmk, full0 + 8 * slot, c * 64, kvh, off, blk);
-      tma_load_4d(dv + c * S::kPlane, tmv, full0 + 8 * slot, c * 64, kvh, off, blk);
+      tma_load_4d(dk + c * S::kPlane, tmk, full0 + 8 * slot, c * PE, kvh, off, blk);
+      tma_load_4d(dv + c * S::kPlane, tmv, full0 + 8 * slot, c * PE, kvh, off, blk);
     }
   }
 }
 
-template <bool IS_BF16, int D, int NS>
+template <bool IS_BF16, int D, int NS, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const PrefillArgs a) {
-  using S = PrefillSmem<D, NS>;
+  using S = PrefillSmem<D, NS, FP8>;
+  constexpr bool MB = IS_BF16 && !FP8;  // MMA operand type: E4M3 caches run in fp16
   constexpr int KD = D / 16;   // k-steps of QK^T
   constexpr int ND = D / 8;    // n-tiles of O
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -173,8 +187,8 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
   int issued = 0;  // stages warp 0 has issued
   if (warp == 0) {
     for (; issued < NS && issued < n_stages; ++issued)
-      issue_prefill_stage<D, NS>(a, &tmk, &tmv, table_row, kvh, issued, max_pos, base, full0,
-                                 masks, lane);
+      issue_prefill_stage<D, NS, FP8>(a, &tmk, &tmv, table_row, kvh, issued, max_pos, base, full0,
+                                      masks, lane);
   }
 
   // -------------------------------------------------------------- consumers
@@ -197,11 +211,50 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
 #pragma unroll
     for (int kk = 0; kk < KD; ++kk) {
       const int d = kk * 16 + tig * 2;
-      qa[kk][0] = v0 ? __ldg(q32 + ((b0 + d) >> 1)) : 0u;
-      qa[kk][1] = v1 ? __ldg(q32 + ((b1 + d) >> 1)) : 0u;
-      qa[kk][2] = v0 ? __ldg(q32 + ((b0 + d + 8) >> 1)) : 0u;
-      qa[kk][3] = v1 ? __ldg(q32 + ((b1 + d + 8) >> 1)) : 0u;
+      // E4M3: lane quad t takes dims 16kk + 4t .. + 3, the order the codes arrive in
+      const int da = FP8 ? kk * 16 + tig * 4 : d;
+      const int db = FP8 ? da + 2 : d + 8;
+      qa[kk][0] = v0 ? __ldg(q32 + ((b0 + da) >> 1)) : 0u;
+      qa[kk][1] = v1 ? __ldg(q32 + ((b1 + da) >> 1)) : 0u;
+      qa[kk][2] = v0 ? __ldg(q32 + ((b0 + db) >> 1)) : 0u;
+      qa[kk][3] = v1 ? __ldg(q32 + ((b1 + db) >> 1)) : 0u;
     }
+  }
+  // logit scale per row (log2 units); E4M3 with bf16 q: q rows become fp16
+  // times 2^(13 - e), e the exponent of the row's largest magnitude
+  float sl0 = a.scale_log2, sl1 = a.scale_log2;
+  if constexpr (FP8 && IS_BF16) {
+    float mx0 = 0.f, mx1 = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk) {
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const float2 f0 = unpack2<true>(qa[kk][i]);
+        const float2 f1 = unpack2<true>(qa[kk][i + 1]);
+        mx0 = fmaxf(mx0, fmaxf(fabsf(f0.x), fabsf(f0.y)));
+        mx1 = fmaxf(mx1, fmaxf(fabsf(f1.x), fabsf(f1.y)));
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const int e0 = max(static_cast<int>((__float_as_uint(mx0) >> 23) & 0xFFu) - 127, -100);
+    const int e1 = max(static_cast<int>((__float_as_uint(mx1) >> 23) & 0xFFu) - 127, -100);
+    const float p0 = __uint_as_float(static_cast<uint32_t>(127 + 13 - e0) << 23);
+    const float p1 = __uint_as_float(static_cast<uint32_t>(127 + 13 - e1) << 23);
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk) {
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const float2 f0 = unpack2<true>(qa[kk][i]);
+        const float2 f1 = unpack2<true>(qa[kk][i + 1]);
+        qa[kk][i] = pack2<false>(f0.x * p0, f0.y * p0);
+        qa[kk][i + 1] = pack2<false>(f1.x * p1, f1.y * p1);
+      }
+    }
+    sl0 *= __uint_as_float(static_cast<uint32_t>(127 - 13 + e0) << 23);
+    sl1 *= __uint_as_float(static_cast<uint32_t>(127 - 13 + e1) << 23);
   }
 
   float o[ND][4];
@@ -242,16 +295,38 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
       float sc[8][4];
 #pragma unroll
       for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+      if constexpr (FP8) {
+        // matrix j: tokens 16p + 8(j & 1) .. + 7 of 16-byte chunk kk + (j >> 1);
+        // lane (gid, tig) gets codes 4tig .. 4tig + 3 of its token
 #pragma unroll
-      for (int kk = 0; kk < KD; ++kk) {
+        for (int kk = 0; kk < KD; kk += 2) {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {  // tokens 16p .. 16p + 15
-          const int mi = lane >> 3;
-          const int t = p * 16 + ((mi >> 1) << 3) + (lane & 7);
-          uint32_t r[4];
-          ldsm_x4(swz(kp, t, kk * 2 + (mi & 1)), r);
-          mma16816<IS_BF16>(sc[2 * p], qa[kk], r[0], r[1]);
-          mma16816<IS_BF16>(sc[2 * p + 1], qa[kk], r[2], r[3]);
+          for (int p = 0; p < 4; ++p) {
+            const int mi = lane >> 3;
+            const int t = p * 16 + ((mi & 1) << 3) + (lane & 7);
+            uint32_t r[4];
+            ldsm_x4(swz(kp, t, kk + (mi >> 1)), r);
+            uint32_t b[4][2];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) e4m3x4_to_f16(r[j], b[j][0], b[j][1]);
+            mma16816<false>(sc[2 * p], qa[kk], b[0][0], b[0][1]);
+            mma16816<false>(sc[2 * p + 1], qa[kk], b[1][0], b[1][1]);
+            mma16816<false>(sc[2 * p], qa[kk + 1], b[2][0], b[2][1]);
+            mma16816<false>(sc[2 * p + 1], qa[kk + 1], b[3][0], b[3][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < KD; ++kk) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {  // tokens 16p .. 16p + 15
+            const int mi = lane >> 3;
+            const int t = p * 16 + ((mi >> 1) << 3) + (lane & 7);
+            uint32_t r[4];
+            ldsm_x4(swz(kp, t, kk * 2 + (mi & 1)), r);
+            mma16816<IS_BF16>(sc[2 * p], qa[kk], r[0], r[1]);
+            mma16816<IS_BF16>(sc[2 * p + 1], qa[kk], r[2], r[3]);
+          }
         }
       }
       // ---- scale, mask, online softmax (log2 domain)
@@ -263,8 +338,8 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
         for (int c = 0; c < 2; ++c) {
           const int tl = n * 8 + tig * 2 + c;
           const int t = t0 + tl;
-          float x0 = sc[n][c] * a.scale_log2;
-          float x1 = sc[n][2 + c] * a.scale_log2;
+          float x0 = sc[n][c] * sl0;
+          float x1 = sc[n][2 + c] * sl1;
           if (need_mask) {
             const bool ok = (vmask >> tl) & 1ull;
             x0 = (ok && t <= pos0) ? x0 : -INFINITY;
@@ -316,20 +391,44 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
         const float pv[4][2] = {{pa[0], pa[1]}, {pa[2], pa[3]}, {pb[0], pb[1]}, {pb[2], pb[3]}};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          hi[i] = pack2<IS_BF16>(pv[i][0], pv[i][1]);
-          const float2 h = unpack2<IS_BF16>(hi[i]);
-          lo[i] = pack2<IS_BF16>(pv[i][0] - h.x, pv[i][1] - h.y);
+          hi[i] = pack2<MB>(pv[i][0], pv[i][1]);
+          const float2 h = unpack2<MB>(hi[i]);
+          lo[i] = pack2<MB>(pv[i][0] - h.x, pv[i][1] - h.y);
         }
+        if constexpr (FP8) {
+          // matrix j: tokens 16k2 + 8(j & 1) .. + 7 of 16-byte chunk c + (j >> 1);
+          // lane (gid, tig) gets dims 16c + 2gid, + 1 of tokens 2tig, 2tig + 1
 #pragma unroll
-        for (int dn = 0; dn < D / 16; ++dn) {  // head-dim columns 16dn .. 16dn + 15
-          const int mi = lane >> 3;
-          const int t = k2 * 16 + ((mi & 1) << 3) + (lane & 7);
-          uint32_t r[4];
-          ldsm_x4_trans(swz(vp, t, dn * 2 + (mi >> 1)), r);
-          mma16816<IS_BF16>(o[2 * dn], hi, r[0], r[1]);
-          mma16816<IS_BF16>(o[2 * dn], lo, r[0], r[1]);
-          mma16816<IS_BF16>(o[2 * dn + 1], hi, r[2], r[3]);
-          mma16816<IS_BF16>(o[2 * dn + 1], lo, r[2], r[3]);
+          for (int c = 0; c < D / 16; c += 2) {
+            const int mi = lane >> 3;
+            const int t = k2 * 16 + ((mi & 1) << 3) + (lane & 7);
+            uint32_t r[4];
+            ldsm_x4_trans(swz(vp, t, c + (mi >> 1)), r);
+            uint32_t b[4][2];  // [matrix][dim + 0 / dim + 1]
+#pragma unroll
+            for (int j = 0; j < 4; ++j) e4m3x4_to_f16(prmt(r[j], r[j], 0x3120u), b[j][0], b[j][1]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // chunk c + h
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {  // n-tile of dims 16(c + h) + 2n + e
+                auto& acc = o[2 * (c + h) + e];
+                mma16816<false>(acc, hi, b[2 * h][e], b[2 * h + 1][e]);
+                mma16816<false>(acc, lo, b[2 * h][e], b[2 * h + 1][e]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int dn = 0; dn < D / 16; ++dn) {  // head-dim columns 16dn .. 16dn + 15
+            const int mi = lane >> 3;
+            const int t = k2 * 16 + ((mi & 1) << 3) + (lane & 7);
+            uint32_t r[4];
+            ldsm_x4_trans(swz(vp, t, dn * 2 + (mi >> 1)), r);
+            mma16816<IS_BF16>(o[2 * dn], hi, r[0], r[1]);
+            mma16816<IS_BF16>(o[2 * dn], lo, r[0], r[1]);
+            mma16816<IS_BF16>(o[2 * dn + 1], hi, r[2], r[3]);
+            mma16816<IS_BF16>(o[2 * dn + 1], lo, r[2], r[3]);
+          }
         }
       }
     }
@@ -345,8 +444,8 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
         aborted = true;
         break;
       }
-      issue_prefill_stage<D, NS>(a, &tmk, &tmv, table_row, kvh, it + NS, max_pos, base, full0,
-                                 masks, lane);
+      issue_prefill_stage<D, NS, FP8>(a, &tmk, &tmv, table_row, kvh, it + NS, max_pos, base, full0,
+                                      masks, lane);
       ++issued;
     }
   }
@@ -362,30 +461,35 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const float vs = FP8 ? a.v_scale : 1.f;
+  const float inv0 = l0 > 0.f ? vs / l0 : 0.f;
+  const float inv1 = l1 > 0.f ? vs / l1 : 0.f;
   const int64_t ob0 = ((static_cast<int64_t>(q0) + r0 / g) * a.num_q_heads + kvh * g + r0 % g) * D;
   const int64_t ob1 = ((static_cast<int64_t>(q0) + r1 / g) * a.num_q_heads + kvh * g + r1 % g) * D;
 #pragma unroll
   for (int n = 0; n < ND; ++n) {
-    const int d = n * 8 + tig * 2;
+    // 16-bit: columns 2tig, 2tig + 1 of n-tile n are dims 8n + 2tig, + 1; E4M3:
+    // n-tile 2c + e holds dim 16c + 2col + e, so its columns are dims
+    // 16c + 4tig + e and 16c + 4tig + 2 + e
+    const int d = FP8 ? (n >> 1) * 16 + tig * 4 + (n & 1) : n * 8 + tig * 2;
+    const int dd = FP8 ? 2 : 1;
     if (v0) {
       store_val(a, ob0 + d, o[n][0] * inv0);
-      store_val(a, ob0 + d + 1, o[n][1] * inv0);
+      store_val(a, ob0 + d + dd, o[n][1] * inv0);
     }
     if (v1) {
       store_val(a, ob1 + d, o[n][2] * inv1);
-      store_val(a, ob1 + d + 1, o[n][3] * inv1);
+      store_val(a, ob1 + d + dd, o[n][3] * inv1);
     }
   }
 }
 
-template <bool IS_BF16, int D>
+template <bool IS_BF16, int D, bool FP8 = false>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a, dim3 grid,
                    cudaStream_t st) {
-  constexpr int NS = prefill_stages<D>();
-  auto kern = prefill_kernel<IS_BF16, D, NS>;
-  const int smem = static_cast<int>(PrefillSmem<D, NS>::kTotal);
+  constexpr int NS = prefill_stages<D>() * (FP8 ? 2 : 1);  // the same bytes in flight
+  auto kern = prefill_kernel<IS_BF16, D, NS, FP8>;
+  const int smem = static_cast<int>(PrefillSmem<D, NS, FP8>::kTotal);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kWarps * 32, smem, st>>>(tk, tv, a);
@@ -395,7 +499,14 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillAr
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                           int head_dim, bool bf16, dim3 grid, cudaStream_t st) {
+                           int head_dim, bool bf16, bool fp8, dim3 grid, cudaStream_t st) {
+  if (fp8) {  // E4M3 caches: head_dim 128 or 256
+    if (head_dim == 128) return bf16 ? launch<true, 128, true>(tk, tv, a, grid, st)
+                                     : launch<false, 128, true>(tk, tv, a, grid, st);
+    if (head_dim == 256) return bf16 ? launch<true, 256, true>(tk, tv, a, grid, st)
+                                     : launch<false, 256, true>(tk, tv, a, grid, st);
+    return cudaErrorInvalidValue;
+  }
   if (bf16) {
     return head_dim == 64 ? launch<true, 64>(tk, tv, a, grid, st)
            : head_dim == 128 ? launch<true, 128>(tk, tv, a, grid, st)

@@ -287,17 +287,18 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
 
 def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
             seq_lens: torch.Tensor, q_start: torch.Tensor, scale: float, *, max_q_len: int,
-            out: Optional[torch.Tensor] = None,
-            out_dtype: Optional[torch.dtype] = None) -> torch.Tensor:
+            out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+            k_scale: Optional[float] = None, v_scale: Optional[float] = None) -> torch.Tensor:
     """Causal attention for several new tokens per sequence (chunked prefill,
     speculative verification): query row t of sequence s (rows q_start[s] ..
     q_start[s+1]) sits at position seq_lens[s] - n_s + (t - q_start[s]) and
     attends to positions 0 .. that position. The new tokens' K/V must already
     be in the cache. ``max_q_len`` bounds every n_s (it sizes the launch).
+    E4M3 caches take the layer's ``k_scale`` and ``v_scale``.
     """
     dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens, q_start)
     _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [T, Hq, D] with the cache's D")
-    _need(q.dtype == k_cache.dtype, "q dtype must match the cache (float16 or bfloat16 caches)")
+    _check_act(q, k_cache, "q")
     n = block_tables.shape[0]
     _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2, "block_tables: int32 [N, maxB]")
     _need(seq_lens.dtype == torch.int32 and seq_lens.shape == (n,), "seq_lens: int32 [N]")
@@ -307,7 +308,7 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
         out = torch.empty((t_all, hq, d), dtype=out_dtype or q.dtype, device=dev)
     _cuda(out, q)
     _need(out.shape == q.shape and out.dtype in _DTYPES, "out: [T, Hq, D] of float16/bfloat16/float32")
-    cache = make_cache(k_cache, v_cache)
+    cache = make_cache(k_cache, v_cache, act_dtype=q.dtype, k_scale=k_scale, v_scale=v_scale)
     st = _lib.lib().pa_prefill(_ptr(q), n, _ptr(q_start), int(max_q_len), hq, ctypes.byref(cache),
                                _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
                                float(scale), _ptr(out), _DTYPES[out.dtype], _stream(dev))

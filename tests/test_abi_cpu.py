@@ -155,8 +155,8 @@ def test_host_argument_errors_launch_nothing(lib):
     assert dec(fp8(d=64)) == -3
     assert dec(fp8(d=120)) == -3
     assert lib.pa_write_kv(vp(4096), vp(4096), vp(4096), 1, ctypes.byref(fp8(vs=-1.0)), vp(0)) == -6
-    assert lib.pa_prefill(vp(4096), 1, vp(4096), 1, 8, ctypes.byref(fp8()), vp(4096), 1, vp(4096),
-                          1.0, vp(4096), 0, vp(0)) == -2
+    assert lib.pa_prefill(vp(4096), 1, vp(4096), 1, 8, ctypes.byref(fp8(d=64)), vp(4096), 1,
+                          vp(4096), 1.0, vp(4096), 0, vp(0)) == -3
     # zero sequences is a no-op
     assert lib.pa_decode(vp(0), 0, 8, ctypes.byref(good), vp(0), 1, vp(0), 1, 1.0,
                          vp(0), 0, 0, vp(0), 0, vp(0)) == 0

@@ -420,7 +420,7 @@ def _config5(rng: np.random.Generator, kv_dtype: Optional[str] = None) -> Worklo
 PREFILL_NAMES = ("verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16")
 
 
-def make_prefill_config(name: str) -> Workload:
+def make_prefill_config(name: str, kv_dtype: Optional[str] = None) -> Workload:
     """Named multi-token workloads (seeded like the decode configs):
 
     * ``verify4_70b_bf16_b16``: speculative verification of 4 draft tokens per
@@ -430,6 +430,8 @@ def make_prefill_config(name: str) -> Workload:
       4096 cached tokens for 8 sequences (32 / 8 heads, d 128, bf16, b 16).
     * ``prompt2k_mha_fp16_b16``: whole 2048-token prompts of 16 sequences on
       the 7B/13B head shape (32 / 32 heads, d 128, fp16, b 16).
+
+    ``kv_dtype="e4m3"`` gives the same shapes an FP8 pool.
     """
     seed = 2000 + PREFILL_NAMES.index(name)
     rng = np.random.default_rng(seed)
@@ -437,15 +439,15 @@ def make_prefill_config(name: str) -> Workload:
         lens = rng.integers(512, 8192, size=128, endpoint=True)
         return make_prefill_case(seed, num_seqs=128, num_q_heads=64, num_kv_heads=8, head_dim=128,
                                  block_size=16, seq_lens=lens, q_lens=[4] * 128, dtype="bf16",
-                                 name=name)
+                                 name=name, kv_dtype=kv_dtype)
     if name == "chunk512_gqa_bf16_b16":
         return make_prefill_case(seed, num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
                                  block_size=16, seq_lens=[4096 + 512] * 8, q_lens=[512] * 8,
-                                 dtype="bf16", name=name)
+                                 dtype="bf16", name=name, kv_dtype=kv_dtype)
     if name == "prompt2k_mha_fp16_b16":
         return make_prefill_case(seed, num_seqs=16, num_q_heads=32, num_kv_heads=32, head_dim=128,
                                  block_size=16, seq_lens=[2048] * 16, q_lens=[2048] * 16,
-                                 dtype="f16", name=name)
+                                 dtype="f16", name=name, kv_dtype=kv_dtype)
     raise ValueError(f"unknown prefill workload {name!r}")
 
 
