@@ -505,7 +505,7 @@ def run_prefill(args):
     except Exception:
         tc_peak, tc_kind = 1900.0, "fallback"
     hbm_bound = args.prefill.startswith("verify")
-    kernel = ("prefill_tc_kernel" if (not fp8 and w.head_dim == 128 and
+    kernel = ("prefill_tc_kernel" if (w.head_dim == 128 and
                                       int(np.diff(w.q_start).max()) * w.group >= 128)
               else "prefill_kernel")
     roofline = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",

@@ -518,7 +518,7 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
     return PA_ERR_CUDA;
   cudaError_t e;
   const bool act_bf16 = (fp8 ? cache->act_dtype : cache->dtype) == PA_BF16;
-  if (!fp8 && D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
+  if (D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
       aligned(out, 16)) {
     // 5th-generation tensor cores: 256 (query, head) rows per CTA, S and O in
     // TMEM. Batches of fewer rows per KV head (speculative verification of a few
@@ -526,7 +526,7 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
     const int64_t tiles256 = (static_cast<int64_t>(max_q_len) * g + 255) / 256;
     const dim3 grid(static_cast<unsigned>(tiles256), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));
-    e = pa::launch_prefill_tc(tk, tv, a, act_bf16, grid, static_cast<cudaStream_t>(stream));
+    e = pa::launch_prefill_tc(tk, tv, a, act_bf16, fp8, grid, static_cast<cudaStream_t>(stream));
   } else {
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));

@@ -34,6 +34,14 @@
 // part, O += P_hi V + P_lo V, keeping about 16 bits of each weight; an fp16 P
 // (11 bits) is used whole.
 //
+// FP8 (E4M3) caches: the TMA ring holds the codes (one 128-byte line per token
+// for K and for V); two converter warps widen each tile exactly to fp16 into a
+// ring of four tiles in the 16-bit layout the MMAs read (one warp K, one V, zeroing
+// V rows without valid data), and every MMA runs in fp16. A bf16 query row is
+// stored as fp16 times a power of two that keeps its largest element below
+// 2^14, undone in that row's logit scale; P is then fp16 and used whole. k_scale
+// folds into the logit scale, v_scale multiplies the output.
+//
 // Masking: keys past a row's position get p = 0; V rows of tokens that hold no
 // valid data (past the sequence's length, or of a block with an id out of
 // range) are zeroed in shared memory before O += P V reads them. Every wait is
@@ -52,32 +60,48 @@ constexpr int kD = 128;            // head dim
 constexpr int kRowsTc = 128;       // query rows per row tile (TMEM lanes)
 constexpr int kQTiles = 2;         // row tiles per CTA
 constexpr int kBn = 64;            // tokens per K/V tile
-constexpr int kStagesTc = 4;       // K/V tiles in flight
+constexpr int kStagesTc = 4;       // tiles in flight in the TMA ring
 constexpr int kSoftmaxWarps = 4 * kQTiles;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreadsTc = (kSoftmaxWarps + 2) * 32;
+constexpr int kConvWarp = kSoftmaxWarps + 2;  // FP8: warps kConvWarp (K) and kConvWarp + 1 (V)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kLimitTcNs = 2000000000ull;
 
+template <bool FP8>
+constexpr int tc_threads() {
+  return (kSoftmaxWarps + 2 + (FP8 ? 2 : 0)) * 32;
+}
+
+// Shared memory. 16-bit caches: the TMA ring holds the K/V tiles the MMAs
+// read (kStagesTc of kStage). FP8: the TMA ring holds code tiles (kLoadStages
+// of kCodeTile) and the MMAs read a ring of kMmaTiles widened tiles.
+template <bool FP8>
 struct TcSmem {
   static constexpr uint32_t kHalf = kBn * 128;                  // 64 token rows of 128 bytes
   static constexpr uint32_t kQTile = 2 * kRowsTc * 128;         // 2 halves x 128 rows x 128 B
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kStage = 4 * kHalf;                 // K halves, then V halves
-  static constexpr uint32_t kStages = kQ + kQTiles * kQTile;
-  static constexpr uint32_t kBar = kStages + kStagesTc * kStage;
+  static constexpr uint32_t kStages = kQ + kQTiles * kQTile;    // tiles the MMAs read
+  static constexpr int kLoadStages = FP8 ? 2 : kStagesTc;   // TMA ring
+  static constexpr int kMmaTiles = FP8 ? 4 : kStagesTc;
+  static constexpr uint32_t kCodeTile = 2 * kHalf;              // K codes, then V codes
+  static constexpr uint32_t kCodes = kStages + kMmaTiles * kStage;
+  static constexpr uint32_t kBar = kCodes + (FP8 ? kLoadStages * kCodeTile : 0);
   // kv_full[NS], kv_empty[NS], s_full[2 tiles][2], p_full[2 tiles][2],
-  // o_done[2 tiles][2], final. p_full and o_done alternate by tile parity: a
-  // softmax warp may publish P_{t+1} before the MMA warp waits for P_t, and
-  // waits on o_done only now and then, so a single barrier could run two
-  // phases ahead of its waiter, where parity waits alias.
-  static constexpr uint32_t kNumBars = 2 * kStagesTc + 4 + 4 + 4 + 1;
-  static constexpr uint32_t kMask = kBar + kNumBars * 8;        // uint64 per stage
-  static constexpr uint32_t kMisc = kMask + kStagesTc * 8;      // tmem base, abort flag
+  // o_done[2 tiles][2], final, and for FP8 conv_full[4], conv_empty[4].
+  // p_full and o_done alternate by tile parity: a softmax warp may publish
+  // P_{t+1} before the MMA warp waits for P_t, and waits on o_done only now and
+  // then, so a single barrier could run two phases ahead of its waiter, where
+  // parity waits alias.
+  static constexpr uint32_t kNumBars = 2 * kStagesTc + 4 + 4 + 4 + 1 + 8;
+  static constexpr uint32_t kMask = kBar + kNumBars * 8;        // uint64 per ring stage
+  static constexpr uint32_t kConvMask = kMask + kStagesTc * 8;  // FP8: uint64 per widened tile
+  static constexpr uint32_t kMisc = kConvMask + 4 * 8;          // tmem base, abort flag
   static constexpr uint32_t kTotal = kMisc + 16 + 1024;         // + base-alignment slack
 };
-static_assert(TcSmem::kTotal <= 232448, "shared memory budget");
+static_assert(TcSmem<false>::kTotal <= 232448 && TcSmem<true>::kTotal <= 232448,
+              "shared memory budget");
 
 // ------------------------------------------------------------------ tcgen05
 
@@ -237,11 +261,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 
 // Grid: (row-pair tiles, H_kv, N); x is taken in reverse so the tiles with the
 // largest positions (most K/V) start first.
-template <bool IS_BF16>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+template <bool IS_BF16, bool FP8>
+__global__ void __launch_bounds__(tc_threads<FP8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using S = TcSmem;
+  using S = TcSmem<FP8>;
+  constexpr bool MB = IS_BF16 && !FP8;  // MMA operand type: E4M3 caches run in fp16
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t base = smem_u32(sm);
@@ -283,14 +308,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   auto p_full = [&](int q, int b) { return bar + 8u * (2 * kStagesTc + 4 + 2 * q + b); };
   auto o_done = [&](int q, int b) { return bar + 8u * (2 * kStagesTc + 8 + 2 * q + b); };
   const uint32_t fin = bar + 8u * (2 * kStagesTc + 12);
+  auto conv_full = [&](int b) { return bar + 8u * (2 * kStagesTc + 13 + b); };
+  auto conv_empty = [&](int b) { return bar + 8u * (2 * kStagesTc + 17 + b); };
+  constexpr int LS = S::kLoadStages;  // TMA ring stages
+  constexpr int NB = S::kMmaTiles;  // FP8: widened tiles, tile t in buffer t % NB
   uint64_t* masks = reinterpret_cast<uint64_t*>(sm + S::kMask);
+  uint64_t* conv_masks = reinterpret_cast<uint64_t*>(sm + S::kConvMask);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kMisc);
   volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(sm + S::kMisc + 4);
 
   if (threadIdx.x == 0) {
     for (int k = 0; k < kStagesTc; ++k) {
       mbar_init(kv_full(k), 1);
-      mbar_init(kv_empty(k), 1);
+      mbar_init(kv_empty(k), FP8 ? 2 : 1);  // FP8: released by both converter warps
+    }
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(conv_full(b), 2);
+      mbar_init(conv_empty(b), 1);
     }
     for (int q = 0; q < kQTiles; ++q) {
       mbar_init(s_full(q, 0), 1);
@@ -311,7 +345,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  // ---- Q rows into shared memory (K-major, 128-byte swizzle), one row per thread
+  // ---- Q rows into shared memory (K-major, 128-byte swizzle), one row per thread.
+  // FP8 with bf16 q: the row becomes fp16 times 2^(13 - e), e the exponent of
+  // its largest magnitude; q_scale is the factor the row's logits undo.
+  float q_scale = 1.f;
   if (warp < kSoftmaxWarps) {
     const int q = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
@@ -322,12 +359,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
                                            ((static_cast<int64_t>(q0) + i) * a.num_q_heads +
                                             static_cast<int64_t>(kvh) * g + R % g) * kD);
+    uint4 row[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) row[c] = src != nullptr ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (FP8 && IS_BF16) {
+      float mx = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t w[4] = {row[c].x, row[c].y, row[c].z, row[c].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f = unpack2<true>(w[h]);
+          mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+      const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -100);
+      const float p = __uint_as_float(static_cast<uint32_t>(127 + 13 - e) << 23);  // 2^(13-e)
+      q_scale = __uint_as_float(static_cast<uint32_t>(127 - 13 + e) << 23);        // 2^(e-13)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t w[4] = {row[c].x, row[c].y, row[c].z, row[c].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f = unpack2<true>(w[h]);
+          w[h] = pack2<false>(f.x * p, f.y * p);
+        }
+        row[c] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint4 v = src != nullptr ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
       const uint32_t off = S::kQ + q * S::kQTile + (c >> 3) * (kRowsTc * 128u) + r * 128u +
                            (((c & 7) ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(sm + off) = v;
+      *reinterpret_cast<uint4*>(sm + off) = row[c];
     }
   }
   fence_proxy_async_smem();
@@ -342,9 +406,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int tpo = a.tok_per_op;
     int issued = 0;
     for (; issued < ntiles; ++issued) {
-      const int slot = issued % kStagesTc;
-      if (issued >= kStagesTc &&
-          !wait_or_abort(kv_empty(slot), ((issued / kStagesTc) - 1) & 1, abort)) {
+      const int slot = issued % LS;
+      if (issued >= LS &&
+          !wait_or_abort(kv_empty(slot), ((issued / LS) - 1) & 1, abort)) {
         if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
         break;
       }
@@ -369,29 +433,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int last = L - 1 - t0;  // tokens past the length hold no valid data
         if (last < kBn - 1) m &= (1ull << (last + 1)) - 1ull;
         masks[slot] = m;
-        mbar_arrive_expect_tx(kv_full(slot), static_cast<uint32_t>(__popc(okmask)) * tpo * kD * 4u);
+        mbar_arrive_expect_tx(kv_full(slot),
+                              static_cast<uint32_t>(__popc(okmask)) * tpo * kD * (FP8 ? 2u : 4u));
       }
       __syncwarp();
       if (ok) {
-        const uint32_t dk = base + S::kStages + slot * S::kStage + lane * tpo * 128u;
-        const uint32_t dv = dk + 2 * S::kHalf;
+        if constexpr (FP8) {  // one 128-byte line of codes per token for K and for V
+          const uint32_t dk = base + S::kCodes + slot * S::kCodeTile + lane * tpo * 128u;
+          tma_load_4d(dk, &tmk, kv_full(slot), 0, kvh, off, blk);
+          tma_load_4d(dk + S::kHalf, &tmv, kv_full(slot), 0, kvh, off, blk);
+        } else {
+          const uint32_t dk = base + S::kStages + slot * S::kStage + lane * tpo * 128u;
+          const uint32_t dv = dk + 2 * S::kHalf;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tma_load_4d(dk + c * S::kHalf, &tmk, kv_full(slot), c * 64, kvh, off, blk);
-          tma_load_4d(dv + c * S::kHalf, &tmv, kv_full(slot), c * 64, kvh, off, blk);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_4d(dk + c * S::kHalf, &tmk, kv_full(slot), c * 64, kvh, off, blk);
+            tma_load_4d(dv + c * S::kHalf, &tmv, kv_full(slot), c * 64, kvh, off, blk);
+          }
         }
       }
     }
     // copies in flight complete before the CTA frees its shared memory
-    for (int j = (issued > kStagesTc ? issued - kStagesTc : 0); j < issued; ++j)
-      mbar_wait_bounded(kv_full(j % kStagesTc), (j / kStagesTc) & 1, kLimitTcNs);
+    for (int j = (issued > LS ? issued - LS : 0); j < issued; ++j)
+      mbar_wait_bounded(kv_full(j % LS), (j / LS) & 1, kLimitTcNs);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t id_s = umma_idesc(IS_BF16, kRowsTc, kBn, false);
-    constexpr uint32_t id_o = umma_idesc(IS_BF16, kRowsTc, kD, true);
+    constexpr uint32_t id_s = umma_idesc(MB, kRowsTc, kBn, false);
+    constexpr uint32_t id_o = umma_idesc(MB, kRowsTc, kD, true);
+    // the tile the MMAs read: the ring stage itself, or (FP8) the widened buffer
+    auto mma_tile = [&](int t) { return t % NB; };
+    // wait until tile t is readable by the MMAs
+    auto tile_ready = [&](int t) {
+      return FP8 ? wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort)
+                 : wait_or_abort(kv_full(t % LS), (t / LS) & 1, abort);
+    };
     auto issue_s = [&](int q, int t) {  // S_t of row tile q into its TMEM columns 64 * (t % 2)
       const uint32_t q_addr = base + S::kQ + q * S::kQTile;
-      const uint32_t k_addr = base + S::kStages + (t % kStagesTc) * S::kStage;
+      const uint32_t k_addr = base + S::kStages + mma_tile(t) * S::kStage;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (kRowsTc * 128u) + (kk & 3) * 32u;
@@ -402,10 +480,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       umma_commit(s_full(q, t & 1));
     };
     auto issue_pv = [&](int q, int t) {  // O += P_t V_t of row tile q, P_t read from TMEM
-      const uint32_t v_addr = base + S::kStages + (t % kStagesTc) * S::kStage + 2 * S::kHalf;
+      const uint32_t v_addr = base + S::kStages + mma_tile(t) * S::kStage + 2 * S::kHalf;
       const uint32_t p_col = tmem + q * 256u + (t & 1) * kBn;
 #pragma unroll
-      for (int part = 0; part < (IS_BF16 ? 2 : 1); ++part) {
+      for (int part = 0; part < (MB ? 2 : 1); ++part) {
 #pragma unroll
         for (int kk = 0; kk < kBn / 16; ++kk) {
           umma_tmem_a(tmem + q * 256u + 2 * kBn, p_col + part * (kBn / 2) + kk * 8u,
@@ -417,7 +495,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     };
     bool ok = true;
     if (lane == 0) {
-      ok = wait_or_abort(kv_full(0), 0, abort);
+      ok = tile_ready(0);
       if (ok) {
         tc_fence_after();
         for (int q = 0; q < kQTiles; ++q)
@@ -425,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       for (int t = 0; ok && t < ntiles; ++t) {
         if (t + 1 < ntiles) {
-          ok = wait_or_abort(kv_full((t + 1) % kStagesTc), ((t + 1) / kStagesTc) & 1, abort);
+          ok = tile_ready(t + 1);
           if (!ok) break;
           tc_fence_after();
           // S buffer (t+1) % 2 of a tile was released with its P_{t-1}
@@ -439,13 +517,61 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc_fence_after();
           issue_pv(q, t);
         }
-        if (ok) umma_commit(kv_empty(t % kStagesTc));
+        if (ok) umma_commit(FP8 ? conv_empty(t % NB) : kv_empty(t % LS));
       }
       if (!ok) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
       umma_commit(fin);  // arrives once every MMA issued above has completed
       mbar_wait_bounded(fin, 0, kLimitTcNs);
     }
     __syncwarp();
+  } else if (FP8 && warp >= kConvWarp) {
+    // ------------------------------------------------------------ converters (FP8)
+    // warp kConvWarp widens K, kConvWarp + 1 widens V (rows without valid data
+    // become zeros). A code line of token t holds 8 chunks of 16 codes, chunk c
+    // at (c ^ (t & 7)) * 16; its 32 fp16 bytes go to half c / 4, chunks
+    // 2 (c % 4) and 2 (c % 4) + 1 of that token's line, swizzled the same way.
+    const int which = warp - kConvWarp;  // 0: K, 1: V
+    for (int t = 0; t < ntiles; ++t) {
+      const int slot = t % LS;
+      const int b = t % NB;
+      if (!wait_or_abort(kv_full(slot), (t / LS) & 1, abort)) {
+        if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
+        break;
+      }
+      if (t >= NB && !wait_or_abort(conv_empty(b), ((t / NB) - 1) & 1, abort)) {
+        if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
+        break;
+      }
+      const uint64_t vmask = masks[slot];
+      const uint32_t src = S::kCodes + slot * S::kCodeTile + which * S::kHalf;
+      const uint32_t dst = S::kStages + b * S::kStage + which * 2 * S::kHalf;
+#pragma unroll 4
+      for (int idx = lane; idx < kBn * 8; idx += 32) {
+        const int tok = idx >> 3;
+        const int c = idx & 7;
+        uint4 lo, hi;
+        if (which == 1 && !((vmask >> tok) & 1ull)) {
+          lo = hi = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          const uint4 w = *reinterpret_cast<const uint4*>(sm + src + tok * 128u + ((c ^ (tok & 7)) << 4));
+          e4m3x4_to_f16(w.x, lo.x, lo.y);
+          e4m3x4_to_f16(w.y, lo.z, lo.w);
+          e4m3x4_to_f16(w.z, hi.x, hi.y);
+          e4m3x4_to_f16(w.w, hi.z, hi.w);
+        }
+        const uint32_t line = dst + (c >> 2) * S::kHalf + tok * 128u;
+        const int c2 = (c & 3) * 2;
+        *reinterpret_cast<uint4*>(sm + line + ((c2 ^ (tok & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(sm + line + (((c2 + 1) ^ (tok & 7)) << 4)) = hi;
+      }
+      if (which == 0 && lane == 0) conv_masks[b] = vmask;
+      fence_proxy_async_smem();  // the MMAs read the widened tile through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(kv_empty(slot));  // the codes are no longer needed
+        mbar_arrive(conv_full(b));
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int q = warp >> 2;
@@ -457,21 +583,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t lane_base = tmem + q * 256u + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base;            // S buffers: + 64 * (t % 2)
     const uint32_t o_col = lane_base + 2 * kBn;  // O
-    const float sl = a.scale_log2;
+    const float sl = a.scale_log2 * q_scale;
     const bool pos_scale = sl > 0.f;
     float m = -INFINITY;  // running max, log2 units
     float l = 0.f;
     bool ok = true;
     const int my_tiles = nt[q];
     for (int t = 0; t < my_tiles; ++t) {
-      const int slot = t % kStagesTc;
+      const int slot = t % LS;
       if (!wait_or_abort(s_full(q, t & 1), (t >> 1) & 1, abort)) { ok = false; break; }
       tc_fence_after();
       float x[kBn];
       tmem_ld64(s_col + (t & 1) * kBn, x);
       // the tile's valid-token mask: the producer wrote it before arming kv_full
-      if (!wait_or_abort(kv_full(slot), (t / kStagesTc) & 1, abort)) { ok = false; break; }
-      const uint64_t vmask = masks[slot];
+      // (FP8: the K converter copied it before arming conv_full)
+      uint64_t vmask;
+      if constexpr (FP8) {
+        if (!wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort)) { ok = false; break; }
+        vmask = conv_masks[t % NB];
+      } else {
+        if (!wait_or_abort(kv_full(slot), (t / LS) & 1, abort)) { ok = false; break; }
+        vmask = masks[slot];
+      }
       const int k0 = t * kBn;
       // logits in log2 units are x * sl; with sl > 0 the max commutes with the
       // scaling and the scaling folds into the exponent's FMA
@@ -521,14 +654,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       m = m_new;
       uint32_t pk[kBn / 2];
-      uint32_t pl[IS_BF16 ? kBn / 2 : 1];
+      uint32_t pl[MB ? kBn / 2 : 1];
       float ps[kBn / 2];
 #pragma unroll
       for (int c = 0; c < kBn; c += 2) {
         const float p0 = fast_exp2(fmaf(x[c], fs, -m_use));
         const float p1 = fast_exp2(fmaf(x[c + 1], fs, -m_use));
-        pk[c >> 1] = pack2<IS_BF16>(p0, p1);
-        if constexpr (IS_BF16) {
+        pk[c >> 1] = pack2<MB>(p0, p1);
+        if constexpr (MB) {
           const float2 hi = unpack2<true>(pk[c >> 1]);
           pl[c >> 1] = pack2<true>(p0 - hi.x, p1 - hi.y);
         }
@@ -542,11 +675,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       l = l * alpha + ps[0];
       // P over this tile's S buffer: high part in its first 32 columns, low part next
       tmem_st32u(s_col + (t & 1) * kBn, pk);
-      if constexpr (IS_BF16) tmem_st32u(s_col + (t & 1) * kBn + kBn / 2, pl);
+      if constexpr (MB) tmem_st32u(s_col + (t & 1) * kBn + kBn / 2, pl);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       // tokens without valid data: zero their V rows so 0 * garbage never
-      // enters O (each row tile's warps zero the rows; the writes are equal)
-      if (vmask != ~0ull) {
+      // enters O (each row tile's warps zero the rows; the writes are equal).
+      // FP8: the V converter wrote those rows as zeros.
+      if (!FP8 && vmask != ~0ull) {
         const uint32_t vbase = S::kStages + slot * S::kStage + 2 * S::kHalf;
         for (int idx = r; idx < kBn * 16; idx += kRowsTc) {
           const int tok = idx >> 4;
@@ -567,7 +701,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // ---- epilogue: O / l once the last P V has completed
       if (wait_or_abort(o_done(q, (my_tiles - 1) & 1), ((my_tiles - 1) >> 1) & 1, abort)) {
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? (FP8 ? a.v_scale : 1.f) / l : 0.f;
         const int64_t ob = row_ok ? ((static_cast<int64_t>(q0) + i) * a.num_q_heads +
                                      static_cast<int64_t>(kvh) * g + R % g) * kD
                                   : 0;
@@ -614,22 +748,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 }
 
-template <bool IS_BF16>
+template <bool IS_BF16, bool FP8>
 cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a, dim3 grid,
                       cudaStream_t st) {
-  auto kern = prefill_tc_kernel<IS_BF16>;
-  const int smem = static_cast<int>(TcSmem::kTotal);
+  auto kern = prefill_tc_kernel<IS_BF16, FP8>;
+  const int smem = static_cast<int>(TcSmem<FP8>::kTotal);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreadsTc, smem, st>>>(tk, tv, a);
+  kern<<<grid, tc_threads<FP8>(), smem, st>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                              bool bf16, dim3 grid, cudaStream_t st) {
-  return bf16 ? launch_tc<true>(tk, tv, a, grid, st) : launch_tc<false>(tk, tv, a, grid, st);
+                              bool bf16, bool fp8, dim3 grid, cudaStream_t st) {
+  if (fp8) return bf16 ? launch_tc<true, true>(tk, tv, a, grid, st) : launch_tc<false, true>(tk, tv, a, grid, st);
+  return bf16 ? launch_tc<true, false>(tk, tv, a, grid, st) : launch_tc<false, false>(tk, tv, a, grid, st);
 }
 
 }  // namespace pa
