@@ -545,24 +545,38 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       const uint64_t vmask = masks[slot];
       const uint32_t src = S::kCodes + slot * S::kCodeTile + which * S::kHalf;
       const uint32_t dst = S::kStages + b * S::kStage + which * 2 * S::kHalf;
-#pragma unroll 4
-      for (int idx = lane; idx < kBn * 8; idx += 32) {
-        const int tok = idx >> 3;
-        const int c = idx & 7;
-        uint4 lo, hi;
-        if (which == 1 && !((vmask >> tok) & 1ull)) {
-          lo = hi = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-          const uint4 w = *reinterpret_cast<const uint4*>(sm + src + tok * 128u + ((c ^ (tok & 7)) << 4));
-          e4m3x4_to_f16(w.x, lo.x, lo.y);
-          e4m3x4_to_f16(w.y, lo.z, lo.w);
-          e4m3x4_to_f16(w.z, hi.x, hi.y);
-          e4m3x4_to_f16(w.w, hi.z, hi.w);
+      // all of a batch's loads issue before its first store: the stores go to the
+      // same shared array, so the compiler could not move a later load above them
+      constexpr int kBatch = 8;
+#pragma unroll
+      for (int b0 = 0; b0 < kBn * 8 / 32; b0 += kBatch) {
+        uint4 w[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = (b0 + u) * 32 + lane;
+          const int tok = idx >> 3;
+          const int c = idx & 7;
+          w[u] = *reinterpret_cast<const uint4*>(sm + src + tok * 128u + ((c ^ (tok & 7)) << 4));
         }
-        const uint32_t line = dst + (c >> 2) * S::kHalf + tok * 128u;
-        const int c2 = (c & 3) * 2;
-        *reinterpret_cast<uint4*>(sm + line + ((c2 ^ (tok & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4*>(sm + line + (((c2 + 1) ^ (tok & 7)) << 4)) = hi;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = (b0 + u) * 32 + lane;
+          const int tok = idx >> 3;
+          const int c = idx & 7;
+          uint4 lo, hi;
+          if (which == 1 && !((vmask >> tok) & 1ull)) {
+            lo = hi = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            e4m3x4_to_f16(w[u].x, lo.x, lo.y);
+            e4m3x4_to_f16(w[u].y, lo.z, lo.w);
+            e4m3x4_to_f16(w[u].z, hi.x, hi.y);
+            e4m3x4_to_f16(w[u].w, hi.z, hi.w);
+          }
+          const uint32_t line = dst + (c >> 2) * S::kHalf + tok * 128u;
+          const int c2 = (c & 3) * 2;
+          *reinterpret_cast<uint4*>(sm + line + ((c2 ^ (tok & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(sm + line + (((c2 + 1) ^ (tok & 7)) << 4)) = hi;
+        }
       }
       if (which == 0 && lane == 0) conv_masks[b] = vmask;
       fence_proxy_async_smem();  // the MMAs read the widened tile through the async proxy
