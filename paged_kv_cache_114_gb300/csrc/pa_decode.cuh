@@ -319,6 +319,19 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int 
   if constexpr (!FP8) ls.s[0][0] = a.scale_log2;
 }
 
+// Pulls the q rows that load_q(s, kvh) will read (g contiguous rows of D
+// 16-bit elements) into L1 ahead of time, one 128-byte line per lane. The
+// streamed pool evicts q from L2, so without this a warp that starts a new
+// piece waits a DRAM round trip for its q.
+template <int D>
+__device__ __forceinline__ void prefetch_q(const DecodeArgs& a, int s, int kvh, int lane) {
+  const char* base = static_cast<const char*>(a.q) +
+                     (static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group) * D * 2;
+  const int lines = (a.group * D * 2 + 127) / 128;
+  for (int i = lane; i < lines; i += 32)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(base + static_cast<int64_t>(i) * 128));
+}
+
 // Issues the TMA copies of one stage - tokens [t0, t0 + tt) of the sequence
 // whose table row starts at `table_row`, KV head kvh, clipped at tok_end -
 // into the stage at shared address `stage`, completing on mbarrier `bar`.

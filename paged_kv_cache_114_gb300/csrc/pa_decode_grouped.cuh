@@ -187,9 +187,17 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   sv.head_off = static_cast<uint32_t>(warp * TPO * 128);
 
   Cursor cc = cursor_at(a, pre, g0);
+  // q of the piece after c, when that piece starts inside this range
+  auto prefetch_next = [&](const Cursor& c) {
+    if (c.ps + c.n >= g1) return;
+    int s2 = c.s + 1;
+    while (s2 < N && pre[s2 + 1] == pre[s2]) ++s2;  // empty sequences have no piece
+    if (s2 < N) prefetch_q<D>(a, s2, kvh, lane);
+  };
   uint32_t qb[NT][KD][2];
   LogitScale<NT, FP8> ls;
   load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);
+  prefetch_next(cc);
   Acc<D, NT> acc;
   acc.reset();
   bool aborted = false;
@@ -225,6 +233,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
       load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);
+      prefetch_next(cc);
       acc.reset();
     }
   }
