@@ -202,6 +202,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (sm_100 and later): one instruction rounds each half
+// exactly as its scalar form would.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (sm_100 and later)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 32 packed 32-bit words into consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -638,16 +672,16 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
         }
       }
       float mx;
-      {
-        float t32[32];
+      {  // 64 -> 22 -> 8 -> 3 -> 1 with three-input maxima
+        float t22[22];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) t32[c] = fmaxf(x[c], x[c + 32]);
+        for (int c = 0; c < 21; ++c) t22[c] = max3(x[c], x[c + 21], x[c + 42]);
+        t22[21] = x[63];
+        float t8[8];
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {
-#pragma unroll
-          for (int c = 0; c < w; ++c) t32[c] = fmaxf(t32[c], t32[c + w]);
-        }
-        mx = t32[0] * fs;
+        for (int c = 0; c < 7; ++c) t8[c] = max3(t22[c], t22[c + 7], t22[c + 14]);
+        t8[7] = t22[21];
+        mx = max3(max3(t8[0], t8[1], t8[2]), max3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7])) * fs;
       }
       const bool grow = mx > m + 8.f;
       const float m_new = grow ? mx : m;
@@ -669,24 +703,31 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       m = m_new;
       uint32_t pk[kBn / 2];
       uint32_t pl[MB ? kBn / 2 : 1];
-      float ps[kBn / 2];
+      uint64_t ps[kBn / 4];  // pair sums of p
+      const uint64_t fs2 = f2(fs, fs);
+      const uint64_t nm2 = f2(-m_use, -m_use);
 #pragma unroll
       for (int c = 0; c < kBn; c += 2) {
-        const float p0 = fast_exp2(fmaf(x[c], fs, -m_use));
-        const float p1 = fast_exp2(fmaf(x[c + 1], fs, -m_use));
+        const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
+        const float p0 = fast_exp2(e.x);
+        const float p1 = fast_exp2(e.y);
+        const uint64_t pp = f2(p0, p1);
         pk[c >> 1] = pack2<MB>(p0, p1);
         if constexpr (MB) {
           const float2 hi = unpack2<true>(pk[c >> 1]);
-          pl[c >> 1] = pack2<true>(p0 - hi.x, p1 - hi.y);
+          const float2 lo = f2_split(sub_f2(pp, f2(hi.x, hi.y)));
+          pl[c >> 1] = pack2<true>(lo.x, lo.y);
         }
-        ps[c >> 1] = p0 + p1;
+        if ((c & 2) == 0) ps[c >> 2] = pp;
+        else ps[c >> 2] = add_f2(ps[c >> 2], pp);
       }
 #pragma unroll
-      for (int w = 16; w >= 1; w >>= 1) {
+      for (int w = kBn / 8; w >= 1; w >>= 1) {
 #pragma unroll
-        for (int c = 0; c < w; ++c) ps[c] += ps[c + w];
+        for (int c = 0; c < w; ++c) ps[c] = add_f2(ps[c], ps[c + w]);
       }
-      l = l * alpha + ps[0];
+      const float2 psum = f2_split(ps[0]);
+      l = l * alpha + (psum.x + psum.y);
       // P over this tile's S buffer: high part in its first 32 columns, low part next
       tmem_st32u(s_col + (t & 1) * kBn, pk);
       if constexpr (MB) tmem_st32u(s_col + (t & 1) * kBn + kBn / 2, pl);
