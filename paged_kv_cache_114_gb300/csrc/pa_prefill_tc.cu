@@ -501,27 +501,32 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       return FP8 ? wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort)
                  : wait_or_abort(kv_full(t % LS), (t / LS) & 1, abort);
     };
+    // A descriptor's start address is its low 14 bits in 16-byte units and
+    // shared memory stays below 256 KB, so an offset is a plain add: one
+    // descriptor per operand and tile, then an add per MMA.
+    const uint64_t dq0 = umma_desc(base + S::kQ, 16, 1024);
     auto issue_s = [&](int q, int t) {  // S_t of row tile q into its TMEM columns 64 * (t % 2)
-      const uint32_t q_addr = base + S::kQ + q * S::kQTile;
-      const uint32_t k_addr = base + S::kStages + mma_tile(t) * S::kStage;
+      const uint64_t dq = dq0 + ((q * S::kQTile) >> 4);
+      const uint64_t dk = umma_desc(base + S::kStages + mma_tile(t) * S::kStage, 16, 1024);
+      const uint32_t d = tmem + q * 256u + (t & 1) * kBn;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (kRowsTc * 128u) + (kk & 3) * 32u;
         const uint32_t ko = (kk >> 2) * S::kHalf + (kk & 3) * 32u;
-        umma(tmem + q * 256u + (t & 1) * kBn, umma_desc(q_addr + qo, 16, 1024),
-             umma_desc(k_addr + ko, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        umma(d, dq + (qo >> 4), dk + (ko >> 4), id_s, kk > 0 ? 1u : 0u);
       }
       umma_commit(s_full(q, t & 1));
     };
     auto issue_pv = [&](int q, int t) {  // O += P_t V_t of row tile q, P_t read from TMEM
-      const uint32_t v_addr = base + S::kStages + mma_tile(t) * S::kStage + 2 * S::kHalf;
+      const uint64_t dv = umma_desc(base + S::kStages + mma_tile(t) * S::kStage + 2 * S::kHalf,
+                                    S::kHalf, 1024);
       const uint32_t p_col = tmem + q * 256u + (t & 1) * kBn;
+      const uint32_t d = tmem + q * 256u + 2 * kBn;
 #pragma unroll
       for (int part = 0; part < (MB ? 2 : 1); ++part) {
 #pragma unroll
         for (int kk = 0; kk < kBn / 16; ++kk) {
-          umma_tmem_a(tmem + q * 256u + 2 * kBn, p_col + part * (kBn / 2) + kk * 8u,
-                      umma_desc(v_addr + kk * 16u * 128u, S::kHalf, 1024), id_o,
+          umma_tmem_a(d, p_col + part * (kBn / 2) + kk * 8u, dv + ((kk * 16u * 128u) >> 4), id_o,
                       (t > 0 || part > 0 || kk > 0) ? 1u : 0u);
         }
       }
