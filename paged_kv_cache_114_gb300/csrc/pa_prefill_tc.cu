@@ -83,6 +83,11 @@ struct TcSmem {
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kStage = 4 * kHalf;                 // K halves, then V halves
   static constexpr uint32_t kStages = kQ + kQTiles * kQTile;    // tiles the MMAs read
+  // The K and V tiles the MMAs read sit as [column half][stage][64 rows][128 B],
+  // so consecutive stages are adjacent rows of one operand.
+  static constexpr uint32_t kHalfStride = kStagesTc * kHalf;    // between column halves
+  static constexpr uint32_t kKRing = kStages;
+  static constexpr uint32_t kVRing = kStages + 2 * kHalfStride;
   static constexpr int kLoadStages = FP8 ? 2 : kStagesTc;   // TMA ring
   static constexpr int kMmaTiles = FP8 ? 4 : kStagesTc;
   static constexpr uint32_t kCodeTile = 2 * kHalf;              // K codes, then V codes
@@ -477,12 +482,12 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
           tma_load_4d(dk, &tmk, kv_full(slot), 0, kvh, off, blk);
           tma_load_4d(dk + S::kHalf, &tmv, kv_full(slot), 0, kvh, off, blk);
         } else {
-          const uint32_t dk = base + S::kStages + slot * S::kStage + lane * tpo * 128u;
-          const uint32_t dv = dk + 2 * S::kHalf;
+          const uint32_t dk = base + S::kKRing + slot * S::kHalf + lane * tpo * 128u;
+          const uint32_t dv = base + S::kVRing + slot * S::kHalf + lane * tpo * 128u;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            tma_load_4d(dk + c * S::kHalf, &tmk, kv_full(slot), c * 64, kvh, off, blk);
-            tma_load_4d(dv + c * S::kHalf, &tmv, kv_full(slot), c * 64, kvh, off, blk);
+            tma_load_4d(dk + c * S::kHalfStride, &tmk, kv_full(slot), c * 64, kvh, off, blk);
+            tma_load_4d(dv + c * S::kHalfStride, &tmv, kv_full(slot), c * 64, kvh, off, blk);
           }
         }
       }
@@ -507,19 +512,18 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
     const uint64_t dq0 = umma_desc(base + S::kQ, 16, 1024);
     auto issue_s = [&](int q, int t) {  // S_t of row tile q into its TMEM columns 64 * (t % 2)
       const uint64_t dq = dq0 + ((q * S::kQTile) >> 4);
-      const uint64_t dk = umma_desc(base + S::kStages + mma_tile(t) * S::kStage, 16, 1024);
+      const uint64_t dk = umma_desc(base + S::kKRing + mma_tile(t) * S::kHalf, 16, 1024);
       const uint32_t d = tmem + q * 256u + (t & 1) * kBn;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t qo = (kk >> 2) * (kRowsTc * 128u) + (kk & 3) * 32u;
-        const uint32_t ko = (kk >> 2) * S::kHalf + (kk & 3) * 32u;
+        const uint32_t ko = (kk >> 2) * S::kHalfStride + (kk & 3) * 32u;
         umma(d, dq + (qo >> 4), dk + (ko >> 4), id_s, kk > 0 ? 1u : 0u);
       }
       umma_commit(s_full(q, t & 1));
     };
     auto issue_pv = [&](int q, int t) {  // O += P_t V_t of row tile q, P_t read from TMEM
-      const uint64_t dv = umma_desc(base + S::kStages + mma_tile(t) * S::kStage + 2 * S::kHalf,
-                                    S::kHalf, 1024);
+      const uint64_t dv = umma_desc(base + S::kVRing + mma_tile(t) * S::kHalf, S::kHalfStride, 1024);
       const uint32_t p_col = tmem + q * 256u + (t & 1) * kBn;
       const uint32_t d = tmem + q * 256u + 2 * kBn;
 #pragma unroll
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       }
       const uint64_t vmask = masks[slot];
       const uint32_t src = S::kCodes + slot * S::kCodeTile + which * S::kHalf;
-      const uint32_t dst = S::kStages + b * S::kStage + which * 2 * S::kHalf;
+      const uint32_t dst = (which ? S::kVRing : S::kKRing) + b * S::kHalf;
       // all of a batch's loads issue before its first store: the stores go to the
       // same shared array, so the compiler could not move a later load above them
       constexpr int kBatch = 8;
@@ -611,7 +615,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
             e4m3x4_to_f16(w[u].z, hi.x, hi.y);
             e4m3x4_to_f16(w[u].w, hi.z, hi.w);
           }
-          const uint32_t line = dst + (c >> 2) * S::kHalf + tok * 128u;
+          const uint32_t line = dst + (c >> 2) * S::kHalfStride + tok * 128u;
           const int c2 = (c & 3) * 2;
           *reinterpret_cast<uint4*>(sm + line + ((c2 ^ (tok & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(sm + line + (((c2 + 1) ^ (tok & 7)) << 4)) = hi;
@@ -741,12 +745,12 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       // enters O (each row tile's warps zero the rows; the writes are equal).
       // FP8: the V converter wrote those rows as zeros.
       if (!FP8 && vmask != ~0ull) {
-        const uint32_t vbase = S::kStages + slot * S::kStage + 2 * S::kHalf;
+        const uint32_t vbase = S::kVRing + slot * S::kHalf;
         for (int idx = r; idx < kBn * 16; idx += kRowsTc) {
           const int tok = idx >> 4;
           const int rem = idx & 15;
           if (!((vmask >> tok) & 1ull))
-            *reinterpret_cast<uint4*>(sm + vbase + (rem >> 3) * S::kHalf + tok * 128u + ((rem & 7) << 4)) =
+            *reinterpret_cast<uint4*>(sm + vbase + (rem >> 3) * S::kHalfStride + tok * 128u + ((rem & 7) << 4)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
       }
