@@ -192,8 +192,17 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int wrow = row_base + warp * 16;      // this warp's first row
-  const bool active = wrow < row_end;
+  // A warp computes 16 rows. With fewer than 64 rows (e.g. verifying a few
+  // draft tokens), the warps left over split each stage's tokens instead:
+  // warp w takes row group w % row_warps and token part w / row_warps of every
+  // stage, and the parts' softmax states are merged at the end.
+  const int row_warps = (row_end - row_base + 15) / 16;
+  const int split = row_warps == 1 ? 4 : (row_warps == 2 ? 2 : 1);
+  const int pcount = 4 / split;               // 16-token groups per stage and warp
+  const int tpart = warp / row_warps;         // token part of this warp
+  const int pg0 = tpart * pcount;             // its first 16-token group
+  const int wrow = row_base + (warp % row_warps) * 16;  // this warp's first row
+  const bool active = tpart < split;
   const int r0 = wrow + gid;                   // the lane's two rows
   const int r1 = r0 + 8;
   const bool v0 = r0 < row_end;
@@ -302,8 +311,9 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
         for (int kk = 0; kk < KD; kk += 2) {
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
+            if (p >= pcount) break;
             const int mi = lane >> 3;
-            const int t = p * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int t = (pg0 + p) * 16 + ((mi & 1) << 3) + (lane & 7);
             uint32_t r[4];
             ldsm_x4(swz(kp, t, kk + (mi >> 1)), r);
             uint32_t b[4][2];
@@ -319,9 +329,10 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
 #pragma unroll
         for (int kk = 0; kk < KD; ++kk) {
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {  // tokens 16p .. 16p + 15
+          for (int p = 0; p < 4; ++p) {  // tokens 16(pg0 + p) .. + 15
+            if (p >= pcount) break;
             const int mi = lane >> 3;
-            const int t = p * 16 + ((mi >> 1) << 3) + (lane & 7);
+            const int t = (pg0 + p) * 16 + ((mi >> 1) << 3) + (lane & 7);
             uint32_t r[4];
             ldsm_x4(swz(kp, t, kk * 2 + (mi & 1)), r);
             mma16816<IS_BF16>(sc[2 * p], qa[kk], r[0], r[1]);
@@ -336,11 +347,14 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
       for (int n = 0; n < 8; ++n) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int tl = n * 8 + tig * 2 + c;
+          const int tl = pg0 * 16 + n * 8 + tig * 2 + c;
           const int t = t0 + tl;
           float x0 = sc[n][c] * sl0;
           float x1 = sc[n][2 + c] * sl1;
-          if (need_mask) {
+          if (n >= 2 * pcount) {  // not this warp's tokens
+            x0 = -INFINITY;
+            x1 = -INFINITY;
+          } else if (need_mask) {
             const bool ok = (vmask >> tl) & 1ull;
             x0 = (ok && t <= pos0) ? x0 : -INFINITY;
             x1 = (ok && t <= pos1) ? x1 : -INFINITY;
@@ -385,6 +399,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
       // ---- O += P V, 16 tokens per k-step, P split into high and low parts
 #pragma unroll
       for (int k2 = 0; k2 < 4; ++k2) {
+        if (k2 >= pcount) break;
         uint32_t hi[4], lo[4];
         const float* pa = sc[2 * k2];
         const float* pb = sc[2 * k2 + 1];
@@ -401,7 +416,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
 #pragma unroll
           for (int c = 0; c < D / 16; c += 2) {
             const int mi = lane >> 3;
-            const int t = k2 * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int t = (pg0 + k2) * 16 + ((mi & 1) << 3) + (lane & 7);
             uint32_t r[4];
             ldsm_x4_trans(swz(vp, t, c + (mi >> 1)), r);
             uint32_t b[4][2];  // [matrix][dim + 0 / dim + 1]
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
 #pragma unroll
           for (int dn = 0; dn < D / 16; ++dn) {  // head-dim columns 16dn .. 16dn + 15
             const int mi = lane >> 3;
-            const int t = k2 * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int t = (pg0 + k2) * 16 + ((mi & 1) << 3) + (lane & 7);
             uint32_t r[4];
             ldsm_x4_trans(swz(vp, t, dn * 2 + (mi >> 1)), r);
             mma16816<IS_BF16>(o[2 * dn], hi, r[0], r[1]);
@@ -454,7 +469,51 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
     for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
       mbar_wait_bounded(full0 + 8 * (j % NS), (j / NS) & 1, kLimitNs);
   }
-  if (!active || aborted) return;
+  // ---- merge the token parts of a split row group (uniform across the CTA,
+  // so every thread takes both barriers). The ring is free by now: the other
+  // parts park (m, l, O) there, lane-major, and part 0 folds them in.
+  if (split > 1) {
+    constexpr int kF = 4 + ND * 4;  // floats of state per lane
+    static_assert(kWarps * kF * 32 * 4 <= S::kBar, "the parked states fit in the ring");
+    float* park = reinterpret_cast<float*>(sm);
+    __syncthreads();  // every copy has landed and every warp is done with the ring
+    if (tpart > 0) {
+      float* my = park + warp * kF * 32 + lane;
+      my[0] = m0;
+      my[32] = m1;
+      my[64] = l0;
+      my[96] = l1;
+#pragma unroll
+      for (int n = 0; n < ND; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) my[(4 + n * 4 + e) * 32] = o[n][e];
+      }
+    }
+    __syncthreads();
+    if (tpart == 0) {
+      for (int pt = 1; pt < split; ++pt) {
+        const float* ot = park + (warp + pt * row_warps) * kF * 32 + lane;
+        const float om0 = ot[0], om1 = ot[32];
+        const float nm0 = fmaxf(m0, om0), nm1 = fmaxf(m1, om1);
+        const float u0 = nm0 == -INFINITY ? 0.f : nm0;
+        const float u1 = nm1 == -INFINITY ? 0.f : nm1;
+        const float a0 = exp2f(m0 - u0), b0 = exp2f(om0 - u0);
+        const float a1 = exp2f(m1 - u1), b1 = exp2f(om1 - u1);
+        l0 = l0 * a0 + ot[64] * b0;
+        l1 = l1 * a1 + ot[96] * b1;
+#pragma unroll
+        for (int n = 0; n < ND; ++n) {
+          o[n][0] = o[n][0] * a0 + ot[(4 + n * 4 + 0) * 32] * b0;
+          o[n][1] = o[n][1] * a0 + ot[(4 + n * 4 + 1) * 32] * b0;
+          o[n][2] = o[n][2] * a1 + ot[(4 + n * 4 + 2) * 32] * b1;
+          o[n][3] = o[n][3] * a1 + ot[(4 + n * 4 + 3) * 32] * b1;
+        }
+        m0 = nm0;
+        m1 = nm1;
+      }
+    }
+  }
+  if (!active || tpart > 0 || aborted) return;
 
   // ---- normalise and store
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
