@@ -62,6 +62,9 @@ CASES = [
     ("f16", 16, 2, 128, 128, [513, 300], [129, 300]),                # b = 128: two boxes per block
     ("bf16", 12, 2, 64, 16, [95, 160, 33], [31, 160, 9]),            # g = 6: heads of a query split across warps
     ("f16", 8, 1, 128, 8, [1, 2, 3, 4, 5], [1, 2, 1, 4, 3]),         # tiny sequences, MQA
+    # drafts only: 32, 32, 48 and 8 rows per KV head, so the 64-row kernel's
+    # warps split each stage's tokens two ways, not at all, and four ways
+    ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 6, 1]),
 ]
 
 

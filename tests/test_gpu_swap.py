@@ -140,3 +140,34 @@ def test_preemption_round_trip(dev, kv):
                       partition_tokens=-1, **kw)
     assert pa.get_device_error(dev) == 0
     assert torch.equal(before, after)
+
+
+@pytest.mark.parametrize("op", ["swap gpu->host", "copy"])
+def test_more_layers_than_one_launch(dev, op):
+    """70 layers: the library moves at most 64 per launch, so this takes two
+    launches; every layer must match the oracle byte for byte."""
+    import paged_kv_cache_114_gb300 as pa
+    rng = np.random.default_rng(70 + len(op))
+    layers, shape = 70, (16, 1, 64)
+    sk, sv = _np_pools(rng, 12, layers, shape, np.uint16)
+    if op == "copy":
+        pairs = [(0, 5), (3, 6), (7, 1), (11, 10)]
+        want_k, want_v = oracle.copy_blocks(sk, sv, pairs)
+        tk = [_torch(a, "gpu", dev, "f16") for a in sk]
+        tv = [_torch(a, "gpu", dev, "f16") for a in sv]
+        pa.copy_blocks(tk, tv, to_dev(np.array(pairs, dtype=np.int64), dev))
+        got_k, got_v = tk, tv
+    else:
+        dk, dv = _np_pools(rng, 9, layers, shape, np.uint16)
+        pairs = [(2, 8), (9, 0), (4, 4)]
+        want_k, want_v = oracle.swap_blocks(sk, sv, dk, dv, pairs)
+        tk = [_torch(a, "gpu", dev, "f16") for a in sk]
+        tv = [_torch(a, "gpu", dev, "f16") for a in sv]
+        got_k = [_torch(a, "host", dev, "f16") for a in dk]
+        got_v = [_torch(a, "host", dev, "f16") for a in dv]
+        pa.swap_blocks(tk, tv, got_k, got_v, to_dev(np.array(pairs, dtype=np.int64), dev))
+    torch.cuda.synchronize()
+    assert pa.get_device_error(dev) == 0
+    for i in range(layers):
+        assert np.array_equal(bits_of(got_k[i]), want_k[i]), f"K of layer {i}"
+        assert np.array_equal(bits_of(got_v[i]), want_v[i]), f"V of layer {i}"
