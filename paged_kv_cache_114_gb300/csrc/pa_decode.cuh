@@ -428,7 +428,6 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
   constexpr int KD = D / 16;
   constexpr int HALVES = D / KvLayout<FP8>::kPieceElems;
   const int gid = lane >> 2;
-  const int tig = lane & 3;
 
   if (rowmask != (1u << TS) - 1u) {  // zero V rows that must not contribute
     for (int idx = lane; idx < TS * HALVES * 8; idx += 32) {
