@@ -49,6 +49,7 @@ namespace {
 constexpr int kRows = 64;        // query rows per CTA
 constexpr int kTok = 64;         // tokens per stage
 constexpr int kWarps = 4;        // consumer warps
+constexpr int kOrderMax = 256;   // batches up to this size run longest sequence first
 constexpr uint64_t kLimitNs = 2000000000ull;  // 2 s per bounded wait
 
 template <int D>
@@ -146,7 +147,28 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2;
   const int tig = lane & 3;
-  const int s = blockIdx.z;
+  // CTA z takes the sequence of rank z by length, longest first (ties by
+  // index), so the long sequences start in the first wave and the short ones
+  // fill the tail. The ranks of all lengths are a permutation of 0 .. N-1.
+  int s = blockIdx.z;
+  if (a.num_seqs <= kOrderMax && static_cast<int>(gridDim.z) == a.num_seqs) {
+    __shared__ int lens_sm[kOrderMax];
+    __shared__ int pick;
+    const int N = a.num_seqs;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) lens_sm[i] = __ldg(a.seq_lens + i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+      const int li = lens_sm[i];
+      int rank = 0;
+      for (int u = 0; u < N; ++u) {
+        const int lu = lens_sm[u];
+        rank += (lu > li || (lu == li && u < i)) ? 1 : 0;
+      }
+      if (rank == static_cast<int>(blockIdx.z)) pick = i;
+    }
+    __syncthreads();
+    s = pick;
+  }
   const int kvh = blockIdx.y;
   const int g = a.group;
 
