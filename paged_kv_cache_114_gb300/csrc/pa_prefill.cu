@@ -27,6 +27,12 @@
 // of a block whose id is out of range) have their V rows zeroed before PV, so
 // stale or NaN bytes never reach the output.
 //
+// Few rows (verifying a few drafts: g * n rows per KV head, often 32 or less):
+// the warps without rows of their own take a share of each stage's tokens,
+// keep their own softmax state, and fold it into the first part through the
+// freed ring at the end, so all four warps compute. Batches of up to 256
+// sequences run longest first (CTA z takes the sequence of rank z by length).
+//
 // FP8 (E4M3) caches: a stage row is D bytes, one 128-byte swizzled line per
 // 128 head-dim codes. ldmatrix treats byte pairs as its 16-bit elements: for
 // S = Q K^T each lane gets four consecutive codes of a token, so the MMA's
