@@ -56,6 +56,7 @@ constexpr int kRows = 64;        // query rows per CTA
 constexpr int kTok = 64;         // tokens per stage
 constexpr int kWarps = 4;        // consumer warps
 constexpr int kOrderMax = 256;   // batches up to this size run longest sequence first
+constexpr int kIdsCap = 512;     // block ids staged in shared memory per CTA
 constexpr uint64_t kLimitNs = 2000000000ull;  // 2 s per bounded wait
 
 template <int D>
@@ -70,7 +71,8 @@ struct PrefillSmem {
   static constexpr uint32_t kStage = 2 * kHalves * kPlane;     // K planes then V planes
   static constexpr uint32_t kBar = NS * kStage;                // full[NS], empty[NS]
   static constexpr uint32_t kMask = kBar + 2 * NS * 8;         // uint64 valid-row mask per stage
-  static constexpr uint32_t kTotal = kMask + NS * 8 + 1024;    // + base-alignment slack
+  static constexpr uint32_t kIds = kMask + NS * 8;             // the sequence's first block ids
+  static constexpr uint32_t kTotal = kIds + kIdsCap * 4 + 1024; // + base-alignment slack
 };
 
 __device__ __forceinline__ void store_val(const PrefillArgs& a, int64_t idx, float v) {
@@ -96,7 +98,8 @@ template <int D, int NS, bool FP8>
 __device__ __forceinline__ void issue_prefill_stage(const PrefillArgs& a, const CUtensorMap* tmk,
                                                     const CUtensorMap* tmv, int64_t table_row,
                                                     int kvh, int it, int max_pos, uint32_t base,
-                                                    uint32_t full0, uint64_t* masks, int lane) {
+                                                    uint32_t full0, uint64_t* masks,
+                                                    const int32_t* ids, int lane) {
   using S = PrefillSmem<D, NS, FP8>;
   constexpr int PE = FP8 ? 128 : 64;  // head-dim elements per 128-byte line
   const int slot = it % NS;
@@ -110,7 +113,7 @@ __device__ __forceinline__ void issue_prefill_stage(const PrefillArgs& a, const 
     if (t <= max_pos) {
       const int j = t / a.block_size;
       off = t - j * a.block_size;
-      blk = __ldg(a.block_tables + table_row + j);
+      blk = j < kIdsCap ? ids[j] : __ldg(a.block_tables + table_row + j);
       ok = blk >= 0 && blk < a.num_blocks;
       if (!ok) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
     }
@@ -201,6 +204,8 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
   const uint32_t full0 = base + S::kBar;
   const uint32_t empty0 = full0 + NS * 8;
   uint64_t* masks = reinterpret_cast<uint64_t*>(sm + S::kMask);
+  int32_t* ids = reinterpret_cast<int32_t*>(sm + S::kIds);
+  const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -209,14 +214,17 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
     }
     fence_mbar_init();
   }
+  // the block ids up to the CTA's last position, read once by every thread
+  // together, so refilling a stage never waits on the table
+  const int n_ids = min(max_pos / a.block_size + 1, kIdsCap);
+  for (int j = threadIdx.x; j < n_ids; j += blockDim.x) ids[j] = __ldg(a.block_tables + table_row + j);
   __syncthreads();
 
-  const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
   int issued = 0;  // stages warp 0 has issued
   if (warp == 0) {
     for (; issued < NS && issued < n_stages; ++issued)
       issue_prefill_stage<D, NS, FP8>(a, &tmk, &tmv, table_row, kvh, issued, max_pos, base, full0,
-                                      masks, lane);
+                                      masks, ids, lane);
   }
 
   // -------------------------------------------------------------- consumers
@@ -488,7 +496,7 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
         break;
       }
       issue_prefill_stage<D, NS, FP8>(a, &tmk, &tmv, table_row, kvh, it + NS, max_pos, base, full0,
-                                      masks, lane);
+                                      masks, ids, lane);
       ++issued;
     }
   }
