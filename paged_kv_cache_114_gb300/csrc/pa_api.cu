@@ -530,7 +530,9 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   } else {
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));
-    e = pa::launch_prefill(tk, tv, a, D, act_bf16, fp8, grid, static_cast<cudaStream_t>(stream));
+    const bool thin = D == 128 && static_cast<int64_t>(max_q_len) * g <= 32;
+    e = pa::launch_prefill(tk, tv, a, D, act_bf16, fp8, thin, grid,
+                           static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

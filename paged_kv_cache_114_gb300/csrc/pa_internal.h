@@ -102,9 +102,11 @@ struct PrefillArgs {
   float v_scale;                 // E4M3 caches: V code c stands for value(c) * v_scale
 };
 // Grid: (ceil(max_q_len * g / 64), H_kv, N). bf16: q/out MMA type (the act
-// dtype for E4M3 caches); fp8: E4M3 cache (head_dim 128 or 256).
+// dtype for E4M3 caches); fp8: E4M3 cache (head_dim 128 or 256); thin: head
+// dim 128 with at most 32 rows per CTA (three CTAs per SM, a two-stage ring).
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                           int head_dim, bool bf16, bool fp8, dim3 grid, cudaStream_t st);
+                           int head_dim, bool bf16, bool fp8, bool thin, dim3 grid,
+                           cudaStream_t st);
 // tcgen05/TMEM kernel for head_dim 128 (pa_prefill_tc.cu). Grid: (ceil(max_q_len * g / 256),
 // H_kv, N); needs q and out 16-byte aligned. fp8: E4M3 cache (q / out type bf16 or fp16).
 cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,

@@ -142,8 +142,10 @@ __device__ __forceinline__ void issue_prefill_stage(const PrefillArgs& a, const 
   }
 }
 
-template <bool IS_BF16, int D, int NS, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
+// MINB: CTAs per SM the register budget is cut for (2 for D <= 128, 1 for
+// 256; 3 for the thin launch of CTAs with few rows, with a shorter ring).
+template <bool IS_BF16, int D, int NS, bool FP8, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const PrefillArgs a) {
   using S = PrefillSmem<D, NS, FP8>;
@@ -579,11 +581,15 @@ __global__ void __launch_bounds__(kWarps * 32, D <= 128 ? 2 : 1)
   }
 }
 
-template <bool IS_BF16, int D, bool FP8 = false>
+// THIN (head_dim 128, at most 32 rows per CTA): two stages instead of three
+// and three CTAs per SM, the same bytes in flight per SM with half again as
+// many warps to hide the latency.
+template <bool IS_BF16, int D, bool FP8 = false, bool THIN = false>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a, dim3 grid,
                    cudaStream_t st) {
-  constexpr int NS = prefill_stages<D>() * (FP8 ? 2 : 1);  // the same bytes in flight
-  auto kern = prefill_kernel<IS_BF16, D, NS, FP8>;
+  constexpr int NS = (THIN ? 2 : prefill_stages<D>()) * (FP8 ? 2 : 1);  // same bytes per stage
+  constexpr int MINB = THIN ? 3 : (D <= 128 ? 2 : 1);
+  auto kern = prefill_kernel<IS_BF16, D, NS, FP8, MINB>;
   const int smem = static_cast<int>(PrefillSmem<D, NS, FP8>::kTotal);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -594,7 +600,14 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillAr
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                           int head_dim, bool bf16, bool fp8, dim3 grid, cudaStream_t st) {
+                           int head_dim, bool bf16, bool fp8, bool thin, dim3 grid,
+                           cudaStream_t st) {
+  if (thin && head_dim == 128) {
+    if (fp8) return bf16 ? launch<true, 128, true, true>(tk, tv, a, grid, st)
+                         : launch<false, 128, true, true>(tk, tv, a, grid, st);
+    return bf16 ? launch<true, 128, false, true>(tk, tv, a, grid, st)
+                : launch<false, 128, false, true>(tk, tv, a, grid, st);
+  }
   if (fp8) {  // E4M3 caches: head_dim 128 or 256
     if (head_dim == 128) return bf16 ? launch<true, 128, true>(tk, tv, a, grid, st)
                                      : launch<false, 128, true>(tk, tv, a, grid, st);

@@ -65,6 +65,8 @@ CASES = [
     # drafts only: 32, 32, 48 and 8 rows per KV head, so the 64-row kernel's
     # warps split each stage's tokens two ways, not at all, and four ways
     ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 6, 1]),
+    # at most 32 rows per KV head: the thin launch (two-stage ring, 3 CTAs per SM)
+    ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 3, 1]),
 ]
 
 

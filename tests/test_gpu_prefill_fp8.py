@@ -60,6 +60,7 @@ CASES = [
     ("bf16", 12, 2, 128, 16, [95, 160, 33], [31, 160, 9]),            # g = 6
     ("f16", 8, 1, 128, 8, [1, 2, 3, 4, 5], [1, 2, 1, 4, 3]),          # tiny sequences, MQA
     ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 6, 1]),      # drafts only: 32/32/48/8 rows
+    ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 3, 1]),      # at most 32 rows: thin launch
 ]
 
 
