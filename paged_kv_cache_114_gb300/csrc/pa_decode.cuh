@@ -178,9 +178,11 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, int n, SlotFn sl
       }
       const int nch = n - c0 < 32 ? n - c0 : 32;
       // Branch-free so the unrolled loads of several partials are in flight
-      // together: a contributor or row without a partial reads partial 0 of
-      // row 0 (always in bounds) and its weight 0 selects the value away.
-#pragma unroll 4
+      // together (eight contributors' rows per round: a merge is a few L2
+      // round trips even while other SMs stream): a contributor or row without
+      // a partial reads partial 0 of row 0 (always in bounds) and its weight 0
+      // selects the value away.
+#pragma unroll 8
       for (int c = 0; c < nch; ++c) {
         const int sc = __shfl_sync(0xffffffffu, sid, c);
 #pragma unroll
