@@ -880,7 +880,17 @@ __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& ac
   acc.reduce_l();
   const int64_t row0 = static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group;
   if (ps >= g0 && pe <= g1) {
-    // whole piece: normalise and write
+    // whole piece: normalise and write, one reciprocal per column (v_scale
+    // folded in for E4M3) rather than a division per element
+    float inv[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float l = acc.l[nt][c];
+        inv[nt][c] = l > 0.f ? (FP8 ? a.v_scale : 1.f) / l : 0.f;
+      }
+    }
 #pragma unroll
     for (int dm = 0; dm < KD; ++dm) {
 #pragma unroll
@@ -888,12 +898,8 @@ __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& ac
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int col = nt * 8 + tig * 2 + (r & 1);
-          if (col < a.group) {
-            const int d = acc_dim<FP8>(dm, gid, r);
-            const float l = acc.l[nt][r & 1];
-            const float o = FP8 ? acc.o[dm][nt][r] * a.v_scale : acc.o[dm][nt][r];
-            store_out(a, (row0 + col) * D + d, l > 0.f ? o / l : 0.f);
-          }
+          if (col < a.group)
+            store_out(a, (row0 + col) * D + acc_dim<FP8>(dm, gid, r), acc.o[dm][nt][r] * inv[nt][r & 1]);
         }
       }
     }
