@@ -473,9 +473,12 @@ def run_prefill(args):
     q_start = to_dev(w.q_start, dev)
     out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
     max_q = int(np.diff(w.q_start).max())
+    ws = None if args.no_workspace else pa.new_prefill_workspace(
+        w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, max_q, dev)
 
     def call():
-        pa.prefill(q, k, v, tables, lens, q_start, w.scale, max_q_len=max_q, out=out, **sc)
+        pa.prefill(q, k, v, tables, lens, q_start, w.scale, max_q_len=max_q, out=out, workspace=ws,
+                   **sc)
 
     for _ in range(args.warmup):
         call()
@@ -505,9 +508,8 @@ def run_prefill(args):
     except Exception:
         tc_peak, tc_kind = 1900.0, "fallback"
     hbm_bound = args.prefill.startswith("verify")
-    kernel = ("prefill_tc_kernel" if (w.head_dim == 128 and
-                                      int(np.diff(w.q_start).max()) * w.group >= 128)
-              else "prefill_kernel")
+    kernel = pa.prefill_kernel_name(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                    w.block_size, max_q, ws is not None)
     roofline = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                  "frac": round(gbs / hbm, 4)} if hbm_bound else
                 {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak, "unit": "TFLOP/s",
@@ -858,8 +860,12 @@ def main(argv=None):
     ap.add_argument("--block-size", type=int, default=None, help="config 4 block size (8/16/32)")
     ap.add_argument("--partition", type=int, default=None, help="split-K partition tokens (default: library's)")
     ap.add_argument("--prefill", default=None,
-                    choices=["verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16"],
+                    choices=["verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16",
+                             "verify4_long_bf16_b16"],
                     help="time pa_prefill on a named multi-token workload instead")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="with --prefill: no workspace, so few-token batches run one CTA per "
+                         "(sequence, KV head, 64 rows) instead of the balanced kernel")
     ap.add_argument("--hash", action="store_true",
                     help="time pa_prefix_hash on 4,096 prompts of 2,048 token ids instead")
     ap.add_argument("--swap", action="store_true",

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 2
+#define PA_ABI_VERSION 3
 
 typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
@@ -270,7 +270,20 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
  *   block_tables device int32 [num_seqs][max_blocks_per_seq]
  *   seq_lens     device int32 [num_seqs]
  *   out          device [q_start[num_seqs]][num_q_heads][head_dim] of out_dtype
- * No workspace. num_seqs <= 65535 and num_kv_heads <= 65535.
+ *   workspace    device, pa_prefill_workspace_bytes() bytes or more, 256-byte
+ *                aligned, owned by the caller and not used by another call
+ *                in flight; or NULL with workspace_bytes 0. Batches of a few
+ *                new tokens per sequence (at most 32 (query, head) rows per KV
+ *                head, head_dim 128, blocks of 16 or more tokens, at most 2048
+ *                sequences; over 16 rows only while the batch has fewer than
+ *                6 (sequence, KV head) pairs per SM) use it to run on the
+ *                balanced head-grouped kernel, whose per-SM ranges of the
+ *                cache need partials and arrival counters (cleared by each
+ *                call); without one they run one CTA per (sequence, KV head,
+ *                64 rows). Other shapes never use it.
+ * num_seqs <= 65535 and num_kv_heads <= 65535.
+ * Errors (host): a workspace of workspace_bytes > 0 but fewer bytes than the
+ * shape needs, or NULL, returns PA_ERR_WORKSPACE; misaligned, PA_ERR_ALIGN.
  * Errors (device): n_s > L_s, L_s above the table's capacity or n_s above
  * max_q_len set PA_DEVERR_SEQ_LEN and the sequence's rows (or those past
  * max_q_len) are not written; a table entry out of range sets
@@ -279,7 +292,21 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
 int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t max_q_len,
                int32_t num_q_heads, const pa_cache* cache, const int32_t* block_tables,
                int32_t max_blocks_per_seq, const int32_t* seq_lens, float scale, void* out,
-               pa_dtype out_dtype, void* stream);
+               pa_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes pa_prefill can use for these sizes on the current device
+ * (0 when the shape runs on a kernel that needs none). */
+size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int32_t max_q_len);
+
+/* Name of the kernel pa_prefill launches for this shape, given a workspace
+ * (with_workspace != 0) or not, for 16-byte aligned q and out, on a device of
+ * num_sms SMs (0: the current device): "multi_grouped_kernel",
+ * "prefill_tc_kernel" or "prefill_kernel"; NULL for sizes it rejects (or
+ * num_sms 0 without a device). */
+const char* pa_prefill_kernel_name(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t max_q_len,
+                                   int32_t with_workspace, int32_t num_sms);
 
 /* Workspace bytes pa_decode needs for these sizes (0 when one partition covers
  * max_seq_len or partition_tokens == 0). The balanced mode's size depends on

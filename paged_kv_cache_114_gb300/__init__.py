@@ -19,7 +19,8 @@ from ._lib import PA_PARTITION_BALANCED, STATIC_WORKSPACE_BYTES
 from .step import DecodeStep
 from .ops import (check_copy_pairs, copy_blocks, decode, decode_kernel_name, decode_static_workspace,
                   decode_workspace_bytes, default_partition, get_device_error, make_cache,
-                  new_workspace, prefill, prefix_hash, slot_mapping, swap_blocks, write_kv)
+                  new_prefill_workspace, new_workspace, prefill, prefill_kernel_name,
+                  prefill_workspace_bytes, prefix_hash, slot_mapping, swap_blocks, write_kv)
 
 __all__ = [
     "DEVERR_BLOCK_ID", "DEVERR_POSITION", "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
@@ -27,5 +28,6 @@ __all__ = [
     "decode_workspace_bytes", "default_partition", "get_device_error", "make_cache",
     "slot_mapping", "write_kv", "decode_static_workspace", "STATIC_WORKSPACE_BYTES",
     "PA_PARTITION_BALANCED", "new_workspace", "DecodeStep", "decode_kernel_name",
-    "prefill", "swap_blocks", "prefix_hash",
+    "prefill", "prefill_workspace_bytes", "new_prefill_workspace", "prefill_kernel_name",
+    "swap_blocks", "prefix_hash",
 ]

@@ -1,7 +1,8 @@
 """Builds libpagedkv.so in-tree with nvcc for sm_103a (GB300).
 
 Each translation unit compiles in its own nvcc process, in parallel; the decode
-kernel is compiled once per (cache type, dtype, head_dim). The library links the CUDA
+kernel is compiled once per (cache type, dtype, head_dim) and the multi-token
+balanced kernel once per (cache type, dtype). The library links the CUDA
 runtime statically and needs no libcuda at link time (the tensor-map encoder
 is fetched through the runtime's driver entry-point query).
 
@@ -42,6 +43,9 @@ def _units():
             tag = f"pa_decode_e4m3_{'bf16' if bf else 'f16'}_{d}"
             units.append((tag, "pa_decode_inst.cu", [f"-DPA_INST_BF16={bf}", f"-DPA_INST_D={d}",
                                                      "-DPA_INST_FP8=1"]))
+        for fp8 in (0, 1):  # few new tokens per sequence on the grouped balanced kernel
+            tag = f"pa_verify_{'e4m3_' if fp8 else ''}{'bf16' if bf else 'f16'}"
+            units.append((tag, "pa_verify_inst.cu", [f"-DPA_INST_BF16={bf}", f"-DPA_INST_FP8={fp8}"]))
     return units
 
 

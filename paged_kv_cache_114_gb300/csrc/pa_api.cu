@@ -188,6 +188,59 @@ bool encode_grouped_map(CUtensorMap* m, const void* base, const pa_cache& c, int
   return r == CUDA_SUCCESS;
 }
 
+// pa_prefill on the grouped balanced kernel (few new tokens per sequence):
+// head_dim 128, blocks of 16 or more tokens, at most 32 (query, head) rows
+// per KV head, at most kMaxBalancedSeqs sequences. Eight warps per CTA: HG
+// KV heads x R tiles of 8 * NT rows, one CTA per SM. It is chosen over the
+// per-sequence kernel (3 CTAs of (sequence, KV head) per SM at these sizes)
+// for up to 16 rows per KV head, and for more when that kernel's grid is
+// under two waves: then its longest sequence, streamed by one CTA, bounds the
+// call. Measured on GB300 with 64 / 8 heads, 4 drafts, lengths U[512, 8192]:
+// 16 sequences 118 vs 357 us, 48 sequences 265 vs 392 us, 128 sequences 634
+// vs 535 us; with 2 drafts and 128 sequences 368 vs 477 us.
+struct MultiPlan {
+  bool ok;
+  int nt, row_tiles, head_group;
+  unsigned ctas;
+};
+
+MultiPlan multi_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t block_size, int32_t max_q_len, int sms) {
+  MultiPlan p{false, 0, 0, 0, 0};
+  if (head_dim != 128 || block_size < pa::kStageRows || block_size % pa::kStageRows != 0) return p;
+  if (num_seqs <= 0 || num_seqs > pa::kMaxBalancedSeqs || num_kv_heads <= 0 ||
+      num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return p;
+  const int64_t rows = static_cast<int64_t>(max_q_len) * (num_q_heads / num_kv_heads);
+  if (rows <= 0 || rows > 32) return p;
+  if (rows <= 8) {
+    p.nt = 1; p.row_tiles = 1; p.head_group = 8;
+  } else if (rows <= 16) {
+    p.nt = 2; p.row_tiles = 1; p.head_group = 8;
+  } else {
+    p.nt = 2; p.row_tiles = 2; p.head_group = 4;
+  }
+  if (num_kv_heads % p.head_group != 0 || num_kv_heads / p.head_group > sms) return p;
+  if (rows > 16 && static_cast<int64_t>(num_seqs) * num_kv_heads >= 6LL * sms) return p;
+  p.ctas = static_cast<unsigned>(sms);
+  p.ok = true;
+  return p;
+}
+
+// Its workspace: arrival counters [N][H_kv * R], then kBalancedSlotsPerSm * SMs
+// partial slots of 8 * NT rows ((m, l), then o).
+BalancedLayout multi_layout(int32_t num_seqs, int32_t num_kv_heads, const MultiPlan& p, int sms) {
+  BalancedLayout l{};
+  const int64_t cols = 8LL * p.nt;
+  const int64_t slots = static_cast<int64_t>(pa::kBalancedSlotsPerSm) * sms;
+  const size_t counters =
+      static_cast<size_t>(num_seqs) * num_kv_heads * p.row_tiles * sizeof(unsigned int);
+  l.ml_offset = (counters + 255) / 256 * 256;
+  l.o_offset = l.ml_offset + static_cast<size_t>(slots * cols * 2) * sizeof(float);
+  l.total = l.o_offset + static_cast<size_t>(slots * cols * 128) * sizeof(float);
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
@@ -462,10 +515,37 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
   return pt >= max_seq_len ? 0 : static_cast<int32_t>(pt);
 }
 
+size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int32_t max_q_len) {
+  DeviceInfo di;
+  if (!device_info(&di)) return 0;
+  const MultiPlan p = multi_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_q_len, di.sms);
+  return p.ok ? multi_layout(num_seqs, num_kv_heads, p, di.sms).total : 0;
+}
+
+const char* pa_prefill_kernel_name(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t max_q_len,
+                                   int32_t with_workspace, int32_t num_sms) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_q_len <= 0 ||
+      num_q_heads % num_kv_heads != 0 || num_sms < 0)
+    return nullptr;
+  if (num_sms == 0) {
+    DeviceInfo di;
+    if (!device_info(&di)) return nullptr;
+    num_sms = di.sms;
+  }
+  if (with_workspace &&
+      multi_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_q_len, num_sms).ok)
+    return "multi_grouped_kernel";
+  const int64_t rows = static_cast<int64_t>(max_q_len) * (num_q_heads / num_kv_heads);
+  return head_dim == 128 && rows >= 128 ? "prefill_tc_kernel" : "prefill_kernel";
+}
+
 int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t max_q_len,
                int32_t num_q_heads, const pa_cache* cache, const int32_t* block_tables,
                int32_t max_blocks_per_seq, const int32_t* seq_lens, float scale, void* out,
-               pa_dtype out_dtype, void* stream) {
+               pa_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_cache(cache);
   if (rc != PA_OK) return rc;
   const bool fp8 = is_fp8(*cache);
@@ -512,12 +592,71 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   a.err = di.err;
+  cudaError_t e;
+  const bool act_bf16 = (fp8 ? cache->act_dtype : cache->dtype) == PA_BF16;
+  const MultiPlan mp = multi_plan(num_seqs, num_q_heads, hkv, D, b, max_q_len, di.sms);
+  // the stage line's per-sequence offsets are int32 in the kernel
+  const int64_t line_cap = static_cast<int64_t>(num_seqs) *
+                           ((static_cast<int64_t>(max_blocks_per_seq) * b + pa::kStageRows - 1) /
+                            pa::kStageRows);
+  if (mp.ok && workspace_bytes > 0 && line_cap <= 0x7fffffffLL) {
+    // A few new tokens per sequence: the balanced, head-grouped stream with
+    // (query, head) rows as the MMA columns.
+    const BalancedLayout lay = multi_layout(num_seqs, hkv, mp, di.sms);
+    if (workspace == nullptr || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
+    if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(q_start, 4))
+      return PA_ERR_ALIGN;
+    pa::DecodeArgs d{};
+    d.q = q;
+    d.out = out;
+    d.block_tables = block_tables;
+    d.seq_lens = seq_lens;
+    d.err = di.err;
+    d.num_blocks = cache->num_blocks;
+    d.num_seqs = num_seqs;
+    d.num_q_heads = num_q_heads;
+    d.num_kv_heads = hkv;
+    d.group = g;
+    d.block_size = b;
+    d.max_blocks = max_blocks_per_seq;
+    d.max_seq_len = 0x7fffffff;
+    d.max_parts = 1;
+    d.tok_per_op = pa::kStageRows;
+    d.slot_rows = pa::kStageRows;
+    d.ops_per_stage = 1;
+    d.out_dtype = out_dtype;
+    d.scale_log2 = a.scale_log2;
+    d.v_scale = a.v_scale;
+    d.q_start = q_start;
+    d.max_q = max_q_len;
+    char* ws = static_cast<char*>(workspace);
+    d.counters = reinterpret_cast<unsigned int*>(ws);
+    d.part_ml = reinterpret_cast<float*>(ws + lay.ml_offset);
+    d.part_o = reinterpret_cast<float*>(ws + lay.o_offset);
+    CUtensorMap gk, gv;
+    if (!encode_grouped_map(&gk, cache->k, *cache, pa::kStageRows, mp.head_group) ||
+        !encode_grouped_map(&gv, cache->v, *cache, pa::kStageRows, mp.head_group))
+      return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // arrival counters start each call at zero, whatever the workspace held
+    e = cudaMemsetAsync(d.counters, 0,
+                        static_cast<size_t>(num_seqs) * hkv * mp.row_tiles * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    const dim3 grid(mp.ctas, 1, 1);
+    if (fp8) {
+      e = act_bf16 ? pa::launch_multi_e4m3_bf16(gk, gv, d, mp.nt, mp.row_tiles, mp.head_group, grid, st)
+                   : pa::launch_multi_e4m3_f16(gk, gv, d, mp.nt, mp.row_tiles, mp.head_group, grid, st);
+    } else {
+      e = act_bf16 ? pa::launch_multi_bf16(gk, gv, d, mp.nt, mp.row_tiles, mp.head_group, grid, st)
+                   : pa::launch_multi_f16(gk, gv, d, mp.nt, mp.row_tiles, mp.head_group, grid, st);
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   CUtensorMap tk, tv;
   if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
       !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
     return PA_ERR_CUDA;
-  cudaError_t e;
-  const bool act_bf16 = (fp8 ? cache->act_dtype : cache->dtype) == PA_BF16;
   if (D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
       aligned(out, 16)) {
     // 5th-generation tensor cores: 256 (query, head) rows per CTA, S and O in

@@ -90,6 +90,28 @@ __device__ __forceinline__ int decode_seq_len(const DecodeArgs& a, int s, bool r
   return raw;
 }
 
+// Tokens a sequence puts on the balanced kernels' stage line. Decode: its
+// checked length. Multi-token rows (MULTI): L_s when the sequence has new
+// rows that can be placed; 0 when it has none, and 0, flagged, when n_s > L_s
+// or L_s exceeds its block table. n_s > max_q is flagged too; the rows past
+// max_q are then skipped, the others computed.
+template <bool MULTI>
+__device__ __forceinline__ int line_len(const DecodeArgs& a, int s, bool report) {
+  if constexpr (!MULTI) {
+    return decode_seq_len(a, s, report);
+  } else {
+    const int n = __ldg(a.q_start + s + 1) - __ldg(a.q_start + s);
+    const int L = __ldg(a.seq_lens + s);
+    if (n <= 0) return 0;
+    if (n > L || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.block_size) {
+      if (report) atomicOr(a.err, PA_DEVERR_SEQ_LEN);
+      return 0;
+    }
+    if (n > a.max_q && report) atomicOr(a.err, PA_DEVERR_SEQ_LEN);
+    return L;
+  }
+}
+
 __device__ __forceinline__ void store_out(const DecodeArgs& a, int64_t idx, float v) {
   if (a.out_dtype == PA_F32) {
     static_cast<float*>(a.out)[idx] = v;
@@ -263,25 +285,25 @@ struct Acc {
   }
 };
 
-// q of the group of KV head kvh as the B operand of S^T = K Q^T
-// (k = head-dim index, n = head within the tile); heads past g are zero, and
-// the column logit scales. For FP8 caches, lane quad t takes dims 16kk + 4t ..
-// + 3 of k-step kk, the order in which compute_stage reads the codes, and a
-// bf16 query row is stored as fp16 times 2^(13 - e), e the exponent of its
-// largest magnitude (exact for every element at or above 2^-14 of that
-// scale; the column's logit scale carries 2^(e - 13)).
-template <bool IS_BF16, int D, int NT, bool FP8>
-__device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int lane,
-                                       uint32_t (&qb)[NT][D / 16][2], LogitScale<NT, FP8>& ls) {
-  const int gid = lane >> 2;
+// q rows as the B operand of S^T = K Q^T (k = head-dim index, n = column of
+// the tile): column gid of n-tile nt holds q row qrow(nt) (in rows of D
+// elements), or zeros when that is negative; plus the column logit scales.
+// For FP8 caches, lane quad t takes dims 16kk + 4t .. + 3 of k-step kk, the
+// order in which compute_stage reads the codes, and a bf16 query row is
+// stored as fp16 times 2^(13 - e), e the exponent of its largest magnitude
+// (exact for every element at or above 2^-14 of that scale; the column's
+// logit scale carries 2^(e - 13)).
+template <bool IS_BF16, int D, int NT, bool FP8, class RowFn>
+__device__ __forceinline__ void load_q_rows(const DecodeArgs& a, RowFn qrow, int lane,
+                                            uint32_t (&qb)[NT][D / 16][2],
+                                            LogitScale<NT, FP8>& ls) {
   const int tig = lane & 3;
   const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int head = nt * 8 + gid;
-    const bool live = head < a.group;
-    const int64_t row =
-        (static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group + head) * D;
+    const int64_t qr = qrow(nt);
+    const bool live = qr >= 0;
+    const int64_t row = (live ? qr : 0) * D;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int64_t d0 = FP8 ? kk * 16 + tig * 4 : kk * 16 + tig * 2;
@@ -321,17 +343,35 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int 
   if constexpr (!FP8) ls.s[0][0] = a.scale_log2;
 }
 
+// q of the g heads of KV head kvh for sequence s (one decode query); heads
+// past g are zero columns.
+template <bool IS_BF16, int D, int NT, bool FP8>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int s, int kvh, int lane,
+                                       uint32_t (&qb)[NT][D / 16][2], LogitScale<NT, FP8>& ls) {
+  const int gid = lane >> 2;
+  const int64_t row0 = static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group;
+  load_q_rows<IS_BF16, D, NT, FP8>(
+      a, [&](int nt) -> int64_t { return nt * 8 + gid < a.group ? row0 + nt * 8 + gid : -1; }, lane,
+      qb, ls);
+}
+
 // Pulls the q rows that load_q(s, kvh) will read (g contiguous rows of D
 // 16-bit elements) into L1 ahead of time, one 128-byte line per lane. The
 // streamed pool evicts q from L2, so without this a warp that starts a new
 // piece waits a DRAM round trip for its q.
+// prefetch_q_group takes the g rows that start at q row `row`.
 template <int D>
-__device__ __forceinline__ void prefetch_q(const DecodeArgs& a, int s, int kvh, int lane) {
-  const char* base = static_cast<const char*>(a.q) +
-                     (static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group) * D * 2;
+__device__ __forceinline__ void prefetch_q_group(const DecodeArgs& a, int64_t row, int lane) {
+  const char* base = static_cast<const char*>(a.q) + row * D * 2;
   const int lines = (a.group * D * 2 + 127) / 128;
   for (int i = lane; i < lines; i += 32)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(base + static_cast<int64_t>(i) * 128));
+}
+
+template <int D>
+__device__ __forceinline__ void prefetch_q(const DecodeArgs& a, int s, int kvh, int lane) {
+  prefetch_q_group<D>(
+      a, static_cast<int64_t>(s) * a.num_q_heads + static_cast<int64_t>(kvh) * a.group, lane);
 }
 
 // Issues the TMA copies of one stage - tokens [t0, t0 + tt) of the sequence
@@ -416,15 +456,35 @@ struct GroupView {
   }
 };
 
+// Causal limits of the S^T tile's columns. Decode: every valid token row of
+// a stage is admitted. Multi-token rows (ColLimit): this lane's column c of
+// n-tile nt (tile column 2 * tig + c) admits the stage's token rows
+// 0 .. rel[nt][c] only.
+struct NoColLimit {
+  __device__ __forceinline__ bool ok(int, int, int) const { return true; }
+};
+
+template <int NT>
+struct ColLimit {
+  int rel[NT][2];
+  __device__ __forceinline__ bool ok(int nt, int c, int row) const { return row <= rel[nt][c]; }
+};
+
 // Folds one loaded stage into the warp's softmax state. `sv` (a WarpView or
 // GroupView) places the warp's rows; `smem_base` / `smem_base_ptr` are one shared address and its
-// generic pointer, used to zero masked V rows.
-template <bool IS_BF16, int D, int NT, bool SPLIT_P, bool FP8, class View>
+// generic pointer, used to zero masked V rows; `lim` masks (token, column)
+// pairs past a column's causal limit. LAZY raises the running maximum only
+// when a logit exceeds it by more than 8 (E4M3 caches always); VOTE (with
+// LAZY) first asks the warp whether any logit does, and reduces the column
+// maxima only then; QK2 splits the 16-bit S^T product into two independent
+// MMA chains (even and odd k-steps).
+template <bool IS_BF16, int D, int NT, bool SPLIT_P, bool FP8, class View, class Lim = NoColLimit,
+          bool LAZY = FP8, bool QK2 = false, bool VOTE = false>
 __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
                                               uint8_t* smem_base_ptr, uint32_t rowmask,
                                               const uint32_t (&qb)[NT][D / 16][2],
                                               Acc<D, NT>& acc, const LogitScale<NT, FP8>& ls,
-                                              int lane) {
+                                              int lane, const Lim& lim = Lim()) {
   constexpr bool MB = IS_BF16 && !FP8;  // MMA operand type: E4M3 caches run in fp16
   constexpr int TS = kStageRows;
   constexpr int KD = D / 16;
@@ -479,6 +539,26 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
 #pragma unroll
       for (int r = 0; r < 4; ++r) sacc[nt][r] += sodd[nt][r];
     }
+  } else if constexpr (QK2) {
+    const int i = lane >> 3;
+    const int row = ((i & 1) << 3) + (lane & 7);
+    float sodd[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sodd[nt][0] = sodd[nt][1] = sodd[nt][2] = sodd[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KD; ++kk) {
+      const int chunk = ((kk & 3) << 1) + (i >> 1);
+      uint32_t af[4];
+      ldsm_x4(sv.k + (kk >> 2) * View::half_stride + sv.row(row) + ((chunk ^ (row & 7)) << 4), af);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma16816<MB>((kk & 1) ? sodd[nt] : sacc[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sacc[nt][r] += sodd[nt][r];
+    }
   } else {
     const int i = lane >> 3;
     const int row = ((i & 1) << 3) + (lane & 7);
@@ -492,29 +572,59 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
     }
   }
 
-  // Online softmax update (log2 domain). For E4M3 caches the running maximum
-  // is raised lazily: only when a logit exceeds it by more than 8 (a factor
-  // of 2^8), so most stages keep it and skip rescaling the output; p then
-  // stays below 2^8, and o / l is unchanged.
+  // Online softmax update (log2 domain). LAZY (E4M3 caches, multi-token
+  // rows): the running maximum is raised only when a logit exceeds it by more
+  // than 8 (a factor of 2^8), so most stages keep it and skip rescaling the
+  // output; p then stays below 2^8, and o / l is unchanged.
   const bool v0 = (rowmask >> gid) & 1u;
   const bool v1 = (rowmask >> (gid + 8)) & 1u;
   float p[NT][4];
   float lazy_alpha[NT][2];
   bool grew = false;
+  bool quiet = false;  // VOTE: no logit of the stage passes its column's maximum + 8
+  if constexpr (VOTE) {
+    static_assert(LAZY, "the vote decides the lazy maximum");
+    float x[NT][4];
+    bool need = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      x[nt][0] = v0 && lim.ok(nt, 0, gid) ? sacc[nt][0] * ls(nt, 0) : -INFINITY;
+      x[nt][1] = v0 && lim.ok(nt, 1, gid) ? sacc[nt][1] * ls(nt, 1) : -INFINITY;
+      x[nt][2] = v1 && lim.ok(nt, 0, gid + 8) ? sacc[nt][2] * ls(nt, 0) : -INFINITY;
+      x[nt][3] = v1 && lim.ok(nt, 1, gid + 8) ? sacc[nt][3] * ls(nt, 1) : -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        need |= fmaxf(x[nt][c], x[nt][c + 2]) > acc.m[nt][c] + 8.f;
+    }
+    quiet = !__any_sync(0xffffffffu, need);
+    if (quiet) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float m_use = acc.m[nt][c] == -INFINITY ? 0.f : acc.m[nt][c];
+          p[nt][c] = exp2f(x[nt][c] - m_use);
+          p[nt][c + 2] = exp2f(x[nt][c + 2] - m_use);
+          acc.l[nt][c] += p[nt][c] + p[nt][c + 2];
+        }
+      }
+    }
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    if (quiet) break;
     float x[4];
-    x[0] = v0 ? sacc[nt][0] * ls(nt, 0) : -INFINITY;
-    x[1] = v0 ? sacc[nt][1] * ls(nt, 1) : -INFINITY;
-    x[2] = v1 ? sacc[nt][2] * ls(nt, 0) : -INFINITY;
-    x[3] = v1 ? sacc[nt][3] * ls(nt, 1) : -INFINITY;
+    x[0] = v0 && lim.ok(nt, 0, gid) ? sacc[nt][0] * ls(nt, 0) : -INFINITY;
+    x[1] = v0 && lim.ok(nt, 1, gid) ? sacc[nt][1] * ls(nt, 1) : -INFINITY;
+    x[2] = v1 && lim.ok(nt, 0, gid + 8) ? sacc[nt][2] * ls(nt, 0) : -INFINITY;
+    x[3] = v1 && lim.ok(nt, 1, gid + 8) ? sacc[nt][3] * ls(nt, 1) : -INFINITY;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       float mx = fmaxf(x[c], x[c + 2]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      if constexpr (FP8) {
+      if constexpr (LAZY) {
         const bool grow = mx > acc.m[nt][c] + 8.f;
         const float m_new = grow ? mx : acc.m[nt][c];
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -541,7 +651,7 @@ __device__ __forceinline__ void compute_stage(const View sv, uint32_t smem_base,
       }
     }
   }
-  if constexpr (FP8) {
+  if constexpr (LAZY) {
     if (__any_sync(0xffffffffu, grew)) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -790,6 +900,7 @@ struct Cursor {
   int len;   // sequence length (tokens)
 };
 
+template <bool MULTI = false>
 __device__ __forceinline__ Cursor cursor_at(const DecodeArgs& a, const int32_t* pre, int g) {
   int lo = 0;
   int hi = a.num_seqs - 1;  // largest s with pre[s] <= g: a non-empty sequence
@@ -802,10 +913,11 @@ __device__ __forceinline__ Cursor cursor_at(const DecodeArgs& a, const int32_t* 
   c.n = pre[lo + 1] - pre[lo];
   c.j = g - pre[lo];
   c.ps = pre[lo];
-  c.len = decode_seq_len(a, lo, false);
+  c.len = line_len<MULTI>(a, lo, false);
   return c;
 }
 
+template <bool MULTI = false>
 __device__ __forceinline__ void cursor_next(const DecodeArgs& a, const int32_t* pre, Cursor& c) {
   if (++c.j < c.n) return;
   c.j = 0;
@@ -815,7 +927,7 @@ __device__ __forceinline__ void cursor_next(const DecodeArgs& a, const int32_t* 
   if (c.s < a.num_seqs) {
     c.n = pre[c.s + 1] - pre[c.s];
     c.ps = pre[c.s];
-    c.len = decode_seq_len(a, c.s, false);
+    c.len = line_len<MULTI>(a, c.s, false);
   }
 }
 
@@ -829,8 +941,9 @@ __device__ __forceinline__ int64_t range_start(int64_t r, int64_t S, int64_t R) 
   return (r * S) / R;
 }
 
-// pre[s] = number of 16-token stages of sequences before s (lengths clamped),
-// pre[N] = all of them; built by the whole CTA (nwarps warps, nwarps <= 16).
+// pre[s] = number of 16-token stages of sequences before s (line_len tokens
+// each), pre[N] = all of them; built by the whole CTA (nwarps warps, nwarps <= 16).
+template <bool MULTI = false>
 __device__ __forceinline__ void build_line_prefix(const DecodeArgs& a, int32_t* pre, int tt,
                                                   int* warp_tot, int nwarps) {
   const int N = a.num_seqs;
@@ -840,7 +953,7 @@ __device__ __forceinline__ void build_line_prefix(const DecodeArgs& a, int32_t* 
   const int beg = min(N, static_cast<int>(threadIdx.x) * per);
   const int end = min(N, beg + per);
   int local = 0;
-  for (int s = beg; s < end; ++s) local += (decode_seq_len(a, s, blockIdx.x == 0) + tt - 1) / tt;
+  for (int s = beg; s < end; ++s) local += (line_len<MULTI>(a, s, blockIdx.x == 0) + tt - 1) / tt;
   int x = local;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -857,7 +970,7 @@ __device__ __forceinline__ void build_line_prefix(const DecodeArgs& a, int32_t* 
   }
   for (int s = beg; s < end; ++s) {
     pre[s] = run;
-    run += (decode_seq_len(a, s, false) + tt - 1) / tt;
+    run += (line_len<MULTI>(a, s, false) + tt - 1) / tt;
   }
   if (threadIdx.x == 0) pre[N] = total;
   __syncthreads();

@@ -32,6 +32,9 @@ struct DecodeArgs {
   int32_t out_dtype;             // pa_dtype
   float scale_log2;              // scale * log2(e) (times k_scale for E4M3 caches)
   float v_scale;                 // E4M3 caches: V code c stands for value(c) * v_scale
+  // Multi-token rows (pa_prefill on the grouped kernel); unused by decode.
+  const int32_t* q_start;        // [N + 1] query rows of each sequence
+  int32_t max_q;                 // bound of every n_s; rows past it are not computed
 };
 
 // Rows of shared memory one pipeline stage holds (one m16 tile of tokens).
@@ -76,6 +79,21 @@ cudaError_t launch_decode_e4m3_bf16_128(const CUtensorMap& tk, const CUtensorMap
 cudaError_t launch_decode_e4m3_bf16_256(const CUtensorMap& tk, const CUtensorMap& tv,
                                         const DecodeArgs& a, int group_tiles, int head_group,
                                         dim3 grid, int kernel, cudaStream_t st);
+
+// Multi-token rows on the grouped balanced kernel (pa_verify_inst.cu): head_dim
+// 128, blocks of 16 or more tokens, a.q_start / a.max_q set; (nt, row_tiles,
+// head_group) is (1, 1, 8), (2, 1, 8) or (2, 2, 4): at most 8, 16 or 32
+// (query, head) rows per KV head. Grid: one CTA per SM (a multiple of
+// H_kv / head_group); the workspace is the balanced one with column groups of
+// 8 * nt rows, H_kv * row_tiles of them per sequence.
+#define PA_DECLARE_MULTI(name)                                                               \
+  cudaError_t name(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int nt, \
+                   int row_tiles, int head_group, dim3 grid, cudaStream_t st);
+PA_DECLARE_MULTI(launch_multi_f16)
+PA_DECLARE_MULTI(launch_multi_bf16)
+PA_DECLARE_MULTI(launch_multi_e4m3_f16)
+PA_DECLARE_MULTI(launch_multi_e4m3_bf16)
+#undef PA_DECLARE_MULTI
 
 // Balanced mode: resident CTAs per SM of the per-warp-range kernel, the
 // largest batch whose per-sequence offsets fit shared memory, and the partial

@@ -285,16 +285,44 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     return out
 
 
+def prefill_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                            block_size: int, max_q_len: int) -> int:
+    return int(_lib.lib().pa_prefill_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                     block_size, max_q_len))
+
+
+def new_prefill_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          block_size: int, max_q_len: int, device) -> Optional[torch.Tensor]:
+    """A workspace for pa_prefill (None when the shape needs none); reusable
+    for any later call of the same shape, one call at a time."""
+    n = prefill_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_q_len)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def prefill_kernel_name(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                        block_size: int, max_q_len: int, with_workspace: bool = True,
+                        num_sms: int = 0) -> str:
+    """The kernel pa_prefill runs for this shape (num_sms 0: the current device's)."""
+    name = _lib.lib().pa_prefill_kernel_name(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             block_size, max_q_len, int(bool(with_workspace)),
+                                             int(num_sms))
+    _need(name is not None, "pa_prefill_kernel_name rejected these sizes")
+    return name.decode()
+
+
 def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
             seq_lens: torch.Tensor, q_start: torch.Tensor, scale: float, *, max_q_len: int,
             out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
-            k_scale: Optional[float] = None, v_scale: Optional[float] = None) -> torch.Tensor:
+            k_scale: Optional[float] = None, v_scale: Optional[float] = None,
+            workspace="auto") -> torch.Tensor:
     """Causal attention for several new tokens per sequence (chunked prefill,
     speculative verification): query row t of sequence s (rows q_start[s] ..
     q_start[s+1]) sits at position seq_lens[s] - n_s + (t - q_start[s]) and
     attends to positions 0 .. that position. The new tokens' K/V must already
     be in the cache. ``max_q_len`` bounds every n_s (it sizes the launch).
-    E4M3 caches take the layer's ``k_scale`` and ``v_scale``.
+    E4M3 caches take the layer's ``k_scale`` and ``v_scale``. ``workspace``:
+    a tensor from :func:`new_prefill_workspace`, "auto" (allocate one when the
+    shape can use it) or None (run without, on the per-sequence kernels).
     """
     dev = _cuda(q, k_cache, v_cache, block_tables, seq_lens, q_start)
     _need(q.dim() == 3 and q.shape[2] == k_cache.shape[3], "q: [T, Hq, D] with the cache's D")
@@ -309,9 +337,17 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
     _cuda(out, q)
     _need(out.shape == q.shape and out.dtype in _DTYPES, "out: [T, Hq, D] of float16/bfloat16/float32")
     cache = make_cache(k_cache, v_cache, act_dtype=q.dtype, k_scale=k_scale, v_scale=v_scale)
+    if isinstance(workspace, str):
+        _need(workspace == "auto", 'workspace: a tensor, "auto" or None')
+        workspace = new_prefill_workspace(n, hq, cache.num_kv_heads, d, cache.block_size,
+                                          int(max_q_len), dev)
+    if workspace is not None:
+        _cuda(workspace, q)
     st = _lib.lib().pa_prefill(_ptr(q), n, _ptr(q_start), int(max_q_len), hq, ctypes.byref(cache),
                                _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
-                               float(scale), _ptr(out), _DTYPES[out.dtype], _stream(dev))
+                               float(scale), _ptr(out), _DTYPES[out.dtype], _ptr(workspace),
+                               0 if workspace is None else workspace.numel() * workspace.element_size(),
+                               _stream(dev))
     _lib.check("pa_prefill", st)
     return out
 

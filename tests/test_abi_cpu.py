@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     import paged_kv_cache_114_gb300._lib as L
-    assert lib.pa_abi_version() == L.ABI_VERSION == 2
+    assert lib.pa_abi_version() == L.ABI_VERSION == 3
     assert lib.pa_status_string(0) == b"ok"
     assert lib.pa_status_string(-5).startswith(b"workspace")
     assert lib.pa_status_string(12345) == b"unknown status"
@@ -58,6 +58,7 @@ def test_workspace_bytes(lib):
     import torch
     if not torch.cuda.is_available():
         assert lib.pa_decode_workspace_bytes(8, 32, 8, 128, 4096, -1) == 0
+        assert lib.pa_prefill_workspace_bytes(128, 64, 8, 128, 16, 4) == 0
 
 
 def test_decode_kernel_name(lib):
@@ -80,6 +81,34 @@ def test_decode_kernel_name(lib):
     assert name(32, 8, 128, 12, 2048, 0) is None
     assert name(32, 8, 128, 16, 2048, 24) is None
     assert name(32, 8, 128, 16, 2048, -2) is None
+
+
+def test_prefill_kernel_name(lib):
+    def name(*a, sms=152):
+        r = lib.pa_prefill_kernel_name(*a, sms)
+        return None if r is None else r.decode()
+    # a few drafts (<= 32 (query, head) rows per KV head, head_dim 128, b >= 16)
+    # run on the balanced grouped kernel when a workspace is given; over 16 rows
+    # only while the batch has fewer than 6 (sequence, KV head) pairs per SM
+    assert name(128, 64, 8, 128, 16, 4, 1) == "prefill_kernel"          # 32 rows, 1024 pairs
+    assert name(113, 64, 8, 128, 16, 4, 1) == "multi_grouped_kernel"    # 904 pairs < 912
+    assert name(114, 64, 8, 128, 16, 4, 1) == "prefill_kernel"
+    assert name(128, 64, 8, 128, 16, 4, 1, sms=200) == "multi_grouped_kernel"
+    assert name(16, 64, 8, 128, 16, 4, 1) == "multi_grouped_kernel"
+    assert name(16, 64, 8, 128, 16, 4, 0) == "prefill_kernel"
+    assert name(128, 64, 8, 128, 16, 2, 1) == "multi_grouped_kernel"    # 16 rows
+    assert name(8, 32, 32, 128, 16, 32, 1) == "multi_grouped_kernel"    # MHA, 32 drafts
+    assert name(8, 32, 8, 128, 16, 1, 1) == "multi_grouped_kernel"      # 4 rows
+    assert name(8, 32, 8, 128, 16, 3, 1) == "multi_grouped_kernel"      # 12 rows
+    assert name(8, 32, 4, 128, 16, 2, 1) == "prefill_kernel"            # 16 rows want 8 | H_kv
+    assert name(8, 64, 8, 128, 16, 5, 1) == "prefill_kernel"            # 40 rows
+    assert name(8, 64, 8, 128, 8, 4, 1) == "prefill_kernel"             # blocks of 8
+    assert name(8, 64, 8, 64, 16, 4, 1) == "prefill_kernel"             # head_dim 64
+    assert name(3000, 64, 8, 128, 16, 2, 1) == "prefill_kernel"         # over 2048 sequences
+    assert name(8, 32, 8, 128, 16, 512, 1) == "prefill_tc_kernel"
+    assert name(8, 32, 8, 128, 16, 512, 0) == "prefill_tc_kernel"
+    assert name(8, 30, 8, 128, 16, 4, 1) is None
+    assert name(8, 64, 8, 128, 16, 4, 1, sms=-1) is None
 
 
 def test_check_copy_pairs(lib):
@@ -156,7 +185,7 @@ def test_host_argument_errors_launch_nothing(lib):
     assert dec(fp8(d=120)) == -3
     assert lib.pa_write_kv(vp(4096), vp(4096), vp(4096), 1, ctypes.byref(fp8(vs=-1.0)), vp(0)) == -6
     assert lib.pa_prefill(vp(4096), 1, vp(4096), 1, 8, ctypes.byref(fp8(d=64)), vp(4096), 1,
-                          vp(4096), 1.0, vp(4096), 0, vp(0)) == -3
+                          vp(4096), 1.0, vp(4096), 0, vp(0), 0, vp(0)) == -3
     # zero sequences is a no-op
     assert lib.pa_decode(vp(0), 0, 8, ctypes.byref(good), vp(0), 1, vp(0), 1, 1.0,
                          vp(0), 0, 0, vp(0), 0, vp(0)) == 0

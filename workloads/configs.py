@@ -417,7 +417,8 @@ def _config5(rng: np.random.Generator, kv_dtype: Optional[str] = None) -> Worklo
         **_fp8_fields(kv_dtype))
 
 
-PREFILL_NAMES = ("verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16")
+PREFILL_NAMES = ("verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16",
+                 "verify4_long_bf16_b16")
 
 
 def make_prefill_config(name: str, kv_dtype: Optional[str] = None) -> Workload:
@@ -430,6 +431,9 @@ def make_prefill_config(name: str, kv_dtype: Optional[str] = None) -> Workload:
       4096 cached tokens for 8 sequences (32 / 8 heads, d 128, bf16, b 16).
     * ``prompt2k_mha_fp16_b16``: whole 2048-token prompts of 16 sequences on
       the 7B/13B head shape (32 / 32 heads, d 128, fp16, b 16).
+    * ``verify4_long_bf16_b16``: verification of 4 drafts per sequence at long
+      context, the long-context decode shape (8 sequences of 32768 tokens,
+      32 / 8 heads, d 128, bf16, b 16): few (sequence, KV head) units.
 
     ``kv_dtype="e4m3"`` gives the same shapes an FP8 pool.
     """
@@ -448,6 +452,10 @@ def make_prefill_config(name: str, kv_dtype: Optional[str] = None) -> Workload:
         return make_prefill_case(seed, num_seqs=16, num_q_heads=32, num_kv_heads=32, head_dim=128,
                                  block_size=16, seq_lens=[2048] * 16, q_lens=[2048] * 16,
                                  dtype="f16", name=name, kv_dtype=kv_dtype)
+    if name == "verify4_long_bf16_b16":
+        return make_prefill_case(seed, num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                 block_size=16, seq_lens=[32768] * 8, q_lens=[4] * 8, dtype="bf16",
+                                 name=name, kv_dtype=kv_dtype)
     raise ValueError(f"unknown prefill workload {name!r}")
 
 
