@@ -17,8 +17,10 @@ byte per cached element, q and the new K/V rows fp16/bf16, codes quantised by
 the write and widened by decode.
 
 --prefill NAME times pa_prefill alone (multi-token causal attention) on a named
-workload instead: verify4_70b_bf16_b16 (speculative verification, HBM-bound),
-chunk512_gqa_bf16_b16 or prompt2k_mha_fp16_b16 (tensor-bound).
+workload instead: verify4_70b_bf16_b16 or verify4_long_bf16_b16 (speculative
+verification, HBM-bound), chunk512_gqa_bf16_b16 or prompt2k_mha_fp16_b16
+(tensor-bound). The call gets a workspace when the shape can use one
+(--no-workspace withholds it).
 
 --swap times pa_swap_blocks: a preempted batch's blocks (every layer, K and V)
 out to a pinned host pool and back in, against a contiguous copy of the same
@@ -28,7 +30,7 @@ bytes by the copy engine as the link's reference rate.
 prompts of 2,048 token ids (b = 16).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--kv-dtype e4m3]
-                       [--impl reference] [--prefill NAME] [--swap] [--hash]
+                       [--impl reference] [--prefill NAME [--no-workspace]] [--swap] [--hash]
 """
 from __future__ import annotations
 

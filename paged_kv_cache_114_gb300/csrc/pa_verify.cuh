@@ -20,8 +20,8 @@
 //    n-tiles of accumulators. The consumer that releases a slot last (a
 //    shared counter per slot, acquire-release) issues the slot's next stage.
 //    Every consumer reads that stage's block id a stage ahead, in a lane other
-//    than the releasing one (a release waits for the thread's outstanding
-//    loads), so neither the release nor the issue waits for the table.
+//    than the one that releases (the release orders only that lane's own
+//    accesses), so the issue does not wait for the table.
 #pragma once
 
 #include "pa_decode_grouped.cuh"
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(HG * R * 32, 1)
 
   // The stage NS ahead of the current one (a release of the current slot may
   // issue it) and its block id, read by lane 1 while the current stage
-  // computes: lane 0's release must not wait for that load.
+  // computes, apart from lane 0's release.
   Cursor ic{};
   if (pro < count) ic = cursor_at<true>(a, pre, g0 + pro);
   int next_blk = 0;
