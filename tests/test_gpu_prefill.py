@@ -27,7 +27,7 @@ def dev():
     return d
 
 
-def gpu_prefill(w, dev, out_dtype=torch.float32, max_q_len=None):
+def gpu_prefill(w, dev, out_dtype=torch.float32, max_q_len=None, workspace="auto"):
     """slot_mapping + write_kv of the new tokens, then prefill, on the device."""
     import paged_kv_cache_114_gb300 as pa
     k = to_dev(w.k_cache, dev, w.dtype)
@@ -41,7 +41,8 @@ def gpu_prefill(w, dev, out_dtype=torch.float32, max_q_len=None):
     out = torch.full(tuple(q.shape), float("nan"), dtype=out_dtype, device=dev)
     qn = np.diff(w.q_start)
     pa.prefill(q, k, v, tables, to_dev(w.seq_lens, dev), to_dev(w.q_start, dev), w.scale,
-               max_q_len=int(qn.max()) if max_q_len is None else max_q_len, out=out)
+               max_q_len=int(qn.max()) if max_q_len is None else max_q_len, out=out,
+               workspace=workspace)
     err = pa.get_device_error(dev)
     return out, err, (k, v, tables)
 
@@ -65,7 +66,8 @@ CASES = [
     # drafts only: 32, 32, 48 and 8 rows per KV head, so the 64-row kernel's
     # warps split each stage's tokens two ways, not at all, and four ways
     ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 6, 1]),
-    # at most 32 rows per KV head: the thin launch (two-stage ring, 3 CTAs per SM)
+    # at most 32 rows per KV head: the balanced kernel with a workspace, the thin
+    # launch (two-stage ring, 3 CTAs per SM) without
     ("bf16", 64, 8, 128, 16, [700, 129, 1000, 50], [4, 4, 3, 1]),
 ]
 
@@ -76,12 +78,16 @@ def test_prefill_matches_oracle(dev, case):
     w = make_prefill_case(sum(lens) + 7 * d + hq, num_seqs=len(lens), num_q_heads=hq,
                           num_kv_heads=hkv, head_dim=d, block_size=b, seq_lens=lens, q_lens=qn,
                           dtype=dtype)
-    out, err, _ = gpu_prefill(w, dev)
-    assert err == 0
-    assert_close(out, oracle_prefill(w), what="prefill fp32")
-    out16, err, _ = gpu_prefill(w, dev, out_dtype=torch.float16 if dtype == "f16" else torch.bfloat16)
-    assert err == 0
-    assert_close(out16, oracle_prefill(w), what="prefill 16-bit out")
+    want = oracle_prefill(w)
+    # without a workspace every shape runs on the per-sequence kernels
+    for ws in ("auto", None):
+        out, err, _ = gpu_prefill(w, dev, workspace=ws)
+        assert err == 0
+        assert_close(out, want, what=f"prefill fp32, workspace {ws}")
+        out16, err, _ = gpu_prefill(w, dev, out_dtype=torch.float16 if dtype == "f16" else torch.bfloat16,
+                                    workspace=ws)
+        assert err == 0
+        assert_close(out16, want, what=f"prefill 16-bit out, workspace {ws}")
 
 
 def test_single_query_agrees_with_decode(dev):

@@ -25,7 +25,7 @@ def dev():
     return d
 
 
-def run(w, dev, out_dtype=torch.float32):
+def run(w, dev, out_dtype=torch.float32, workspace="auto"):
     import paged_kv_cache_114_gb300 as pa
     k, v = to_dev(w.k_cache, dev), to_dev(w.v_cache, dev)
     tables = to_dev(w.block_tables, dev)
@@ -38,7 +38,7 @@ def run(w, dev, out_dtype=torch.float32):
     out = torch.full(tuple(q.shape), float("nan"), dtype=out_dtype, device=dev)
     qn = np.diff(w.q_start)
     pa.prefill(q, k, v, tables, to_dev(w.seq_lens, dev), to_dev(w.q_start, dev), w.scale,
-               max_q_len=int(qn.max()), out=out, **sc)
+               max_q_len=int(qn.max()), out=out, workspace=workspace, **sc)
     return out, pa.get_device_error(dev), k, v
 
 
@@ -71,11 +71,13 @@ def test_prefill_e4m3_matches_oracle(dev, case):
                           num_kv_heads=hkv, head_dim=d, block_size=b, seq_lens=lens, q_lens=qn,
                           dtype=dtype, kv_dtype="e4m3")
     want, kw, vw = reference(w)
-    for odt in (torch.float32, torch.float16 if dtype == "f16" else torch.bfloat16):
-        out, err, k, v = run(w, dev, odt)
-        assert err == 0
-        assert np.array_equal(bits_of(k), kw) and np.array_equal(bits_of(v), vw)
-        assert_close(out, want, what=f"prefill e4m3 out {odt}")
+    # without a workspace every shape runs on the per-sequence kernels
+    for ws in ("auto", None):
+        for odt in (torch.float32, torch.float16 if dtype == "f16" else torch.bfloat16):
+            out, err, k, v = run(w, dev, odt, workspace=ws)
+            assert err == 0
+            assert np.array_equal(bits_of(k), kw) and np.array_equal(bits_of(v), vw)
+            assert_close(out, want, what=f"prefill e4m3 out {odt}, workspace {ws}")
 
 
 def test_single_query_equals_decode(dev):
