@@ -276,7 +276,7 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
  *                new tokens per sequence (at most 32 (query, head) rows per KV
  *                head, head_dim 128, blocks of 16 or more tokens, at most 2048
  *                sequences; over 16 rows only while the batch has fewer than
- *                6 (sequence, KV head) pairs per SM) use it to run on the
+ *                4 (sequence, KV head) pairs per SM) use it to run on the
  *                balanced head-grouped kernel, whose per-SM ranges of the
  *                cache need partials and arrival counters (cleared by each
  *                call); without one they run one CTA per (sequence, KV head,

@@ -193,11 +193,12 @@ bool encode_grouped_map(CUtensorMap* m, const void* base, const pa_cache& c, int
 // per KV head, at most kMaxBalancedSeqs sequences. Eight warps per CTA: HG
 // KV heads x R tiles of 8 * NT rows, one CTA per SM. It is chosen over the
 // per-sequence kernel (3 CTAs of (sequence, KV head) per SM at these sizes)
-// for up to 16 rows per KV head, and for more when that kernel's grid is
-// under two waves: then its longest sequence, streamed by one CTA, bounds the
-// call. Measured on GB300 with 64 / 8 heads, 4 drafts, lengths U[512, 8192]:
-// 16 sequences 118 vs 357 us, 48 sequences 265 vs 392 us, 128 sequences 634
-// vs 535 us; with 2 drafts and 128 sequences 368 vs 477 us.
+// for up to 16 rows per KV head, and for more while the batch has fewer than
+// 4 (sequence, KV head) pairs per SM: below that the per-sequence kernel is
+// bound by its longest sequence, which one CTA streams. Measured on GB300 with
+// 64 / 8 heads, 4 drafts, lengths U[512, 8192] (balanced vs per-sequence):
+// 16 sequences 118 vs 357 us, 48: 265 vs 392, 64: 349 vs 406, 80: 410 vs 414,
+// 96: 483 vs 423, 128: 634 vs 535; with 2 drafts, 128 sequences 368 vs 477 us.
 struct MultiPlan {
   bool ok;
   int nt, row_tiles, head_group;
@@ -221,7 +222,7 @@ MultiPlan multi_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads
     p.nt = 2; p.row_tiles = 2; p.head_group = 4;
   }
   if (num_kv_heads % p.head_group != 0 || num_kv_heads / p.head_group > sms) return p;
-  if (rows > 16 && static_cast<int64_t>(num_seqs) * num_kv_heads >= 6LL * sms) return p;
+  if (rows > 16 && static_cast<int64_t>(num_seqs) * num_kv_heads >= 4LL * sms) return p;
   p.ctas = static_cast<unsigned>(sms);
   p.ok = true;
   return p;

@@ -89,11 +89,11 @@ def test_prefill_kernel_name(lib):
         return None if r is None else r.decode()
     # a few drafts (<= 32 (query, head) rows per KV head, head_dim 128, b >= 16)
     # run on the balanced grouped kernel when a workspace is given; over 16 rows
-    # only while the batch has fewer than 6 (sequence, KV head) pairs per SM
+    # only while the batch has fewer than 4 (sequence, KV head) pairs per SM
     assert name(128, 64, 8, 128, 16, 4, 1) == "prefill_kernel"          # 32 rows, 1024 pairs
-    assert name(113, 64, 8, 128, 16, 4, 1) == "multi_grouped_kernel"    # 904 pairs < 912
-    assert name(114, 64, 8, 128, 16, 4, 1) == "prefill_kernel"
-    assert name(128, 64, 8, 128, 16, 4, 1, sms=200) == "multi_grouped_kernel"
+    assert name(75, 64, 8, 128, 16, 4, 1) == "multi_grouped_kernel"     # 600 pairs < 608
+    assert name(76, 64, 8, 128, 16, 4, 1) == "prefill_kernel"
+    assert name(128, 64, 8, 128, 16, 4, 1, sms=300) == "multi_grouped_kernel"
     assert name(16, 64, 8, 128, 16, 4, 1) == "multi_grouped_kernel"
     assert name(16, 64, 8, 128, 16, 4, 0) == "prefill_kernel"
     assert name(128, 64, 8, 128, 16, 2, 1) == "multi_grouped_kernel"    # 16 rows

@@ -122,11 +122,11 @@ def test_multi_kernel_long_verify_sampled(dev):
 
 
 def test_verify_workload_routes_to_the_per_sequence_kernel(dev):
-    """128 sequences of 32 rows per KV head give the per-sequence kernel more
-    than two waves: it runs even with a workspace, and no workspace is made."""
+    """Batches of 32 rows per KV head with 4 or more (sequence, KV head) pairs per
+    SM run on the per-sequence kernel even with a workspace, and need none."""
     import paged_kv_cache_114_gb300 as pa
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    n = -(-6 * sms // 8)  # the fewest sequences giving 6 (sequence, KV head) pairs per SM
+    n = -(-4 * sms // 8)  # the fewest sequences giving 4 (sequence, KV head) pairs per SM
     assert pa.prefill_kernel_name(n, 64, 8, 128, 16, 4) == "prefill_kernel"
     assert pa.prefill_workspace_bytes(n, 64, 8, 128, 16, 4) == 0
     assert pa.prefill_kernel_name(n - 1, 64, 8, 128, 16, 4) == "multi_grouped_kernel"
