@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(HG * R * 32, 1)
   constexpr int TC = 8 * NT;  // columns of one tile
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int warp_tot[16];
-  __shared__ uint32_t released[NS];  // releases per slot, over all rounds
+  __shared__ uint32_t released[NS];  // releases per slot, over all its uses
   __shared__ int last_issued[NS];    // latest stage issued into each slot
   __shared__ int any_abort;
 
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(HG * R * 32, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (refill) {  // the last of this round's CW releases refills the slot
+      if (refill) {  // the last of the CW releases of this use of the slot refills it
         uint32_t old = 0;
         if (lane == 0) old = atom_add_acq_rel_smem(smem_u32(released + slot), 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
