@@ -11,6 +11,9 @@ C ABI, declared in ``include/pa.h``); this package is its Python binding.
 * :func:`prefix_hash` - prefix-cache keys of full blocks (SHA-256 chain);
 * :func:`decode` - decode attention through block tables (single pass,
   split-K with a reduce, or a balanced split), GQA heads packed per KV head;
+* :func:`prefill` - causal attention for several new tokens per sequence
+  (chunked prefill, speculative verification); a few-token batch given a
+  workspace (:func:`new_prefill_workspace`) may run on the balanced kernel;
 * :class:`DecodeStep` - the three calls bound to fixed buffers for loops.
 """
 from ._lib import (DEVERR_BLOCK_ID, DEVERR_POSITION, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_TIMEOUT,
