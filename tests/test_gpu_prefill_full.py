@@ -38,7 +38,9 @@ def sample_pairs(w, n, seed):
 
 
 @pytest.mark.parametrize("name,kv", [("verify4_70b_bf16_b16", None),
-                                     ("chunk512_gqa_bf16_b16", None)])
+                                     ("chunk512_gqa_bf16_b16", None),
+                                     ("chunk512_gqa_bf16_b16", "e4m3"),
+                                     ("prompt2k_mha_fp16_b16", None)])
 def test_prefill_workload_sampled(dev, name, kv):
     import paged_kv_cache_114_gb300 as pa
     w = make_prefill_config(name, kv_dtype=kv)
