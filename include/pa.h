@@ -12,7 +12,10 @@
  *  - All buffers are caller-owned. Pointers documented as "device" must be CUDA
  *    device memory of the current device; "host" pointers are ordinary memory.
  *    The library allocates no device memory and keeps only one static device
- *    error word per device.
+ *    error word per device. Its address (and the device's SM count) is looked
+ *    up on the first call made with that device current and kept until the
+ *    process exits, so a device that went through cudaDeviceReset must not be
+ *    used with the library again.
  *  - Every call enqueues work on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and returns without synchronising, except pa_get_device_error.
  *  - Return value: PA_OK (0) or a negative PA_ERR_* status. A negative status
@@ -47,7 +50,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 3
+#define PA_ABI_VERSION 4
 
 typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
@@ -182,7 +185,8 @@ int pa_swap_blocks(const pa_cache* src, const pa_cache* dst, int32_t num_layers,
  *                  token_offsets[s] .. token_offsets[s+1] - 1
  *   key_offsets    device int64 [num_seqs + 1]: sequence s writes keys
  *                  key_offsets[s] .. key_offsets[s+1] - 1, which must number
- *                  floor(length_s / block_size)
+ *                  floor(length_s / block_size) (pa_prefix_key_offsets
+ *                  computes the packed layout on the device)
  *   root           host, 32 bytes, or NULL for 32 zero bytes (a distinct root,
  *                  e.g. per adapter, keeps caches apart)
  *   keys           device [key_offsets[num_seqs]][32] bytes (digest byte
@@ -193,6 +197,23 @@ int pa_swap_blocks(const pa_cache* src, const pa_cache* dst, int32_t num_layers,
 int pa_prefix_hash(const int32_t* token_ids, const int64_t* token_offsets,
                    const int64_t* key_offsets, int32_t num_seqs, int32_t block_size,
                    const uint8_t* root, uint8_t* keys, void* stream);
+
+/*
+ * pa_prefix_key_offsets - where pa_prefix_hash writes each sequence's keys
+ * when they are packed back to back: key_offsets[0] = 0 and
+ * key_offsets[s + 1] = key_offsets[s] + floor(length_s / block_size), with
+ * length_s = token_offsets[s + 1] - token_offsets[s] (only full blocks get a
+ * key: "PagedAttention: Virtual-Memory KV Cache Management, Continuous
+ * Batching, and PyTorch Architecture", ailinkdeeptech.com, Step 1). One
+ * device scan; the result can be passed straight to pa_prefix_hash, and
+ * key_offsets[num_seqs] is the number of keys.
+ *   token_offsets  device int64 [num_seqs + 1], as for pa_prefix_hash
+ *   key_offsets    device int64 [num_seqs + 1], output
+ * Errors (device): a negative length counts as zero keys and sets
+ * PA_DEVERR_SEQ_LEN. num_seqs == 0 writes key_offsets[0] = 0.
+ */
+int pa_prefix_key_offsets(const int64_t* token_offsets, int32_t num_seqs, int32_t block_size,
+                          int64_t* key_offsets, void* stream);
 
 /* Host-side check of copy pairs: ids in range, distinct destinations, no
  * destination used as a source. Returns PA_OK or PA_ERR_PAIRS / PA_ERR_NULL. */
@@ -300,10 +321,14 @@ size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
                                   int32_t head_dim, int32_t block_size, int32_t max_q_len);
 
 /* Name of the kernel pa_prefill launches for this shape, given a workspace
- * (with_workspace != 0) or not, for 16-byte aligned q and out, on a device of
- * num_sms SMs (0: the current device): "multi_grouped_kernel",
- * "prefill_tc_kernel" or "prefill_kernel"; NULL for sizes it rejects (or
- * num_sms 0 without a device). */
+ * (with_workspace != 0) or not, on a device of num_sms SMs (0: the current
+ * device): "multi_grouped_kernel", "prefill_tc_kernel" or "prefill_kernel";
+ * NULL for sizes it rejects (or num_sms 0 without a device). pa_prefill makes
+ * the same choice from the same helper, and two more inputs that this call
+ * takes as met: q and out 16-byte aligned (otherwise "prefill_tc_kernel"
+ * becomes "prefill_kernel"), and num_seqs * ceil(max_blocks_per_seq *
+ * block_size / 16) below 2^31 (otherwise "multi_grouped_kernel" becomes one
+ * of the other two). */
 const char* pa_prefill_kernel_name(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t block_size, int32_t max_q_len,
                                    int32_t with_workspace, int32_t num_sms);
@@ -346,9 +371,18 @@ const char* pa_decode_kernel_name(int32_t num_q_heads, int32_t num_kv_heads, int
  * the cache, the tables, the lengths and out.
  *   - Sizes whose workspace (pa_decode_workspace_bytes) exceeds
  *     PA_STATIC_WORKSPACE_BYTES return PA_ERR_WORKSPACE and launch nothing.
+ *     The balanced mode (PA_PARTITION_BALANCED, the default for most batches)
+ *     needs 16 * SMs * g * (head_dim + 2) * 4 bytes of partials plus 4 bytes
+ *     per (sequence, KV head), g = num_q_heads / num_kv_heads, whatever the
+ *     batch: on a 152-SM GB300 that fits while g * (head_dim + 2) <= 1,700 or
+ *     so, e.g. g <= 13 at head_dim 128 and g <= 6 at head_dim 256. Larger
+ *     groups (g = 16 at head_dim 128, g = 8 at head_dim 256) are refused in
+ *     that mode even for one sequence; a fixed partition size may still fit.
  *   - The call allocates nothing. The first call on a device looks up the
  *     array's device address (once per device, with that device current); make
- *     that first call before any stream capture.
+ *     that first call before any stream capture. Like the error word's, that
+ *     address is kept for the life of the process: after cudaDeviceReset on a
+ *     device, do not call the library on that device again.
  *   - Every call shares the one array, which keeps the previous call's
  *     partials. Nothing in it needs to start at zero: each call writes every
  *     partial before reading it, and clears the balanced mode's arrival

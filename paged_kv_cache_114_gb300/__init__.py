@@ -8,7 +8,8 @@ C ABI, declared in ``include/pa.h``); this package is its Python binding.
 * :func:`copy_blocks` - whole-block copies for copy-on-write;
 * :func:`swap_blocks` - block copies between the GPU pool and a pinned host
   pool, for preemption by swapping;
-* :func:`prefix_hash` - prefix-cache keys of full blocks (SHA-256 chain);
+* :func:`prefix_hash` - prefix-cache keys of full blocks (SHA-256 chain), packed
+  by :func:`prefix_key_offsets`;
 * :func:`decode` - decode attention through block tables (single pass,
   split-K with a reduce, or a balanced split), GQA heads packed per KV head;
 * :func:`prefill` - causal attention for several new tokens per sequence
@@ -23,7 +24,8 @@ from .step import DecodeStep
 from .ops import (check_copy_pairs, copy_blocks, decode, decode_kernel_name, decode_static_workspace,
                   decode_workspace_bytes, default_partition, get_device_error, make_cache,
                   new_prefill_workspace, new_workspace, prefill, prefill_kernel_name,
-                  prefill_workspace_bytes, prefix_hash, slot_mapping, swap_blocks, write_kv)
+                  prefill_workspace_bytes, prefix_hash, prefix_key_offsets, slot_mapping,
+                  swap_blocks, write_kv)
 
 __all__ = [
     "DEVERR_BLOCK_ID", "DEVERR_POSITION", "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
@@ -32,5 +34,5 @@ __all__ = [
     "slot_mapping", "write_kv", "decode_static_workspace", "STATIC_WORKSPACE_BYTES",
     "PA_PARTITION_BALANCED", "new_workspace", "DecodeStep", "decode_kernel_name",
     "prefill", "prefill_workspace_bytes", "new_prefill_workspace", "prefill_kernel_name",
-    "swap_blocks", "prefix_hash",
+    "swap_blocks", "prefix_hash", "prefix_key_offsets",
 ]

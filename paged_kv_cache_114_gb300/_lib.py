@@ -12,7 +12,7 @@ import threading
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
 
 PA_F16, PA_BF16, PA_F32, PA_FP8_E4M3 = 0, 1, 2, 3
-ABI_VERSION = 3  # PA_ABI_VERSION this binding is written for
+ABI_VERSION = 4  # PA_ABI_VERSION this binding is written for
 PA_OK = 0
 PA_PARTITION_BALANCED = -1
 STATUS = {
@@ -28,7 +28,7 @@ EXPORTED = (
     "pa_decode_workspace_bytes", "pa_decode_default_partition", "pa_get_device_error",
     "pa_status_string", "pa_abi_version", "pa_decode_static_workspace", "pa_decode_kernel_name",
     "pa_prefill", "pa_prefill_workspace_bytes", "pa_prefill_kernel_name", "pa_swap_blocks",
-    "pa_prefix_hash",
+    "pa_prefix_hash", "pa_prefix_key_offsets",
 )
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
@@ -69,6 +69,7 @@ def _declare(lib):
         "pa_copy_blocks": (ctypes.c_int, [cache_p, i32, vp, i64, vp]),
         "pa_swap_blocks": (ctypes.c_int, [cache_p, cache_p, i32, vp, i64, vp]),
         "pa_prefix_hash": (ctypes.c_int, [vp, vp, vp, i32, i32, ctypes.c_char_p, vp, vp]),
+        "pa_prefix_key_offsets": (ctypes.c_int, [vp, i32, i32, vp, vp]),
         "pa_check_copy_pairs": (ctypes.c_int, [vp, i64, i64]),
         "pa_decode": (ctypes.c_int, [vp, i32, i32, cache_p, vp, i32, vp, i32, ctypes.c_float, vp,
                                      ctypes.c_int, i32, vp, sz, vp]),

@@ -228,6 +228,20 @@ MultiPlan multi_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads
   return p;
 }
 
+// Which kernel pa_prefill runs. The balanced grouped kernel needs its plan,
+// a workspace and a stage line whose per-sequence offsets fit int32; the
+// tcgen05 kernel needs head_dim 128, at least 128 (query, head) rows per KV
+// head and 16-byte aligned q and out (its rows move as 16-byte vectors);
+// everything else runs on the mma.sync kernel.
+enum PrefillKernel { kPrefillMulti, kPrefillTc, kPrefillMma };
+
+PrefillKernel route_prefill(bool multi_ok, bool have_workspace, bool line_fits, int32_t head_dim,
+                            int64_t rows_per_kv_head, bool vec_aligned) {
+  if (multi_ok && have_workspace && line_fits) return kPrefillMulti;
+  if (head_dim == 128 && rows_per_kv_head >= 128 && vec_aligned) return kPrefillTc;
+  return kPrefillMma;
+}
+
 // Its workspace: arrival counters [N][H_kv * R], then kBalancedSlotsPerSm * SMs
 // partial slots of 8 * NT rows ((m, l), then o).
 BalancedLayout multi_layout(int32_t num_seqs, int32_t num_kv_heads, const MultiPlan& p, int sms) {
@@ -460,6 +474,19 @@ int pa_prefix_hash(const int32_t* token_ids, const int64_t* token_offsets,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_prefix_key_offsets(const int64_t* token_offsets, int32_t num_seqs, int32_t block_size,
+                          int64_t* key_offsets, void* stream) {
+  if (num_seqs < 0) return PA_ERR_ARG;
+  if (!token_offsets || !key_offsets) return PA_ERR_NULL;
+  if (block_size <= 0 || block_size > 4096) return PA_ERR_SHAPE;
+  if (!aligned(token_offsets, 8) || !aligned(key_offsets, 8)) return PA_ERR_ALIGN;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  const cudaError_t e = pa::launch_key_offsets(token_offsets, num_seqs, block_size, key_offsets,
+                                               di.err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_seq_len, int32_t partition_tokens) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
@@ -536,11 +563,14 @@ const char* pa_prefill_kernel_name(int32_t num_seqs, int32_t num_q_heads, int32_
     if (!device_info(&di)) return nullptr;
     num_sms = di.sms;
   }
-  if (with_workspace &&
-      multi_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_q_len, num_sms).ok)
-    return "multi_grouped_kernel";
+  const bool multi_ok =
+      multi_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_q_len, num_sms).ok;
   const int64_t rows = static_cast<int64_t>(max_q_len) * (num_q_heads / num_kv_heads);
-  return head_dim == 128 && rows >= 128 ? "prefill_tc_kernel" : "prefill_kernel";
+  switch (route_prefill(multi_ok, with_workspace != 0, true, head_dim, rows, true)) {
+    case kPrefillMulti: return "multi_grouped_kernel";
+    case kPrefillTc: return "prefill_tc_kernel";
+    default: return "prefill_kernel";
+  }
 }
 
 int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t max_q_len,
@@ -600,7 +630,10 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   const int64_t line_cap = static_cast<int64_t>(num_seqs) *
                            ((static_cast<int64_t>(max_blocks_per_seq) * b + pa::kStageRows - 1) /
                             pa::kStageRows);
-  if (mp.ok && workspace_bytes > 0 && line_cap <= 0x7fffffffLL) {
+  const PrefillKernel route =
+      route_prefill(mp.ok, workspace_bytes > 0, line_cap <= 0x7fffffffLL, D,
+                    static_cast<int64_t>(max_q_len) * g, aligned(q, 16) && aligned(out, 16));
+  if (route == kPrefillMulti) {
     // A few new tokens per sequence: the balanced, head-grouped stream with
     // (query, head) rows as the MMA columns.
     const BalancedLayout lay = multi_layout(num_seqs, hkv, mp, di.sms);
@@ -658,8 +691,7 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
   if (!encode_cache_map(&tk, cache->k, *cache, a.tok_per_op) ||
       !encode_cache_map(&tv, cache->v, *cache, a.tok_per_op))
     return PA_ERR_CUDA;
-  if (D == 128 && static_cast<int64_t>(max_q_len) * g >= 128 && aligned(q, 16) &&
-      aligned(out, 16)) {
+  if (route == kPrefillTc) {
     // 5th-generation tensor cores: 256 (query, head) rows per CTA, S and O in
     // TMEM. Batches of fewer rows per KV head (speculative verification of a few
     // drafts) stay on the 64-row kernel, whose tiles they fill.

@@ -180,6 +180,8 @@ struct Sha256Root {
   uint32_t w[8];
 };
 const Sha256Consts& sha256_consts();
+cudaError_t launch_key_offsets(const int64_t* tok_off, int32_t num_seqs, int32_t block_size,
+                               int64_t* key_off, int* err, cudaStream_t st);
 cudaError_t launch_prefix_hash(const int32_t* tokens, const int64_t* tok_off, const int64_t* key_off,
                                int32_t num_seqs, int32_t block_size, const Sha256Root& root,
                                uint8_t* keys, int* err, cudaStream_t st);

@@ -178,7 +178,87 @@ __global__ void prefix_hash_kernel(const int32_t* __restrict__ tokens,
   }
 }
 
+// key_off[0] = 0, key_off[s + 1] = key_off[s] + floor(len_s / block_size):
+// the first key of each sequence when keys are packed back to back. One CTA
+// scans chunks of kScanThreads * kScanItems sequences in order, each thread
+// summing kScanItems consecutive counts before a block-wide exclusive scan of
+// the thread totals; the running carry moves on to the next chunk. A negative
+// length counts as zero keys and sets PA_DEVERR_SEQ_LEN (the hash kernel then
+// skips that sequence).
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 8;
+
+__global__ void __launch_bounds__(kScanThreads)
+    key_offsets_kernel(const int64_t* __restrict__ tok_off, int32_t num_seqs, int32_t block_size,
+                       int64_t* __restrict__ key_off, int* err) {
+  __shared__ int64_t warp_sums[kScanThreads / 32];
+  __shared__ int64_t carry_s;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    carry_s = 0;
+    key_off[0] = 0;
+  }
+  __syncthreads();
+  constexpr int kChunk = kScanThreads * kScanItems;
+  for (int64_t base = 0; base < num_seqs; base += kChunk) {
+    const int64_t s0 = base + static_cast<int64_t>(threadIdx.x) * kScanItems;
+    int64_t cnt[kScanItems];
+    int64_t mine = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      const int64_t s = s0 + i;
+      int64_t c = 0;
+      if (s < num_seqs) {
+        const int64_t n = tok_off[s + 1] - tok_off[s];
+        if (n < 0) bad = true;
+        c = n > 0 ? n / block_size : 0;
+      }
+      cnt[i] = c;
+      mine += c;
+    }
+    if (bad) atomicOr(err, PA_DEVERR_SEQ_LEN);
+    // inclusive scan of the thread totals: within each warp, then across warps
+    int64_t incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t w = warp_sums[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, d);
+        if (lane >= d) w += y;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t carry = carry_s;
+    int64_t run = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - mine;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      const int64_t s = s0 + i;
+      run += cnt[i];
+      if (s < num_seqs) key_off[s + 1] = run;
+    }
+    __syncthreads();  // every thread has read carry_s and warp_sums
+    if (threadIdx.x == 0) carry_s = carry + warp_sums[kScanThreads / 32 - 1];
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_key_offsets(const int64_t* tok_off, int32_t num_seqs, int32_t block_size,
+                               int64_t* key_off, int* err, cudaStream_t st) {
+  key_offsets_kernel<<<1, kScanThreads, 0, st>>>(tok_off, num_seqs, block_size, key_off, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefix_hash(const int32_t* tokens, const int64_t* tok_off, const int64_t* key_off,
                                int32_t num_seqs, int32_t block_size, const Sha256Root& root,

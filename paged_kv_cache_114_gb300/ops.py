@@ -31,6 +31,13 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+def _on(device: torch.device):
+    """Make ``device`` current for one library call: the library looks up its
+    per-device state (error word, SM count, static workspace) and launches on
+    the current device, which must be the one the tensors live on."""
+    return torch.cuda.device(device)
+
+
 def _need(cond: bool, msg: str) -> None:
     if not cond:
         raise ValueError(msg)
@@ -89,7 +96,8 @@ def slot_mapping(block_tables: torch.Tensor, seq_idx: torch.Tensor, positions: t
         out = torch.empty(positions.shape[0], dtype=torch.int64, device=dev)
     _need(out.dtype == torch.int64 and out.shape == positions.shape, "out: int64 [T]")
     _cuda(out, block_tables)
-    st = _lib.lib().pa_slot_mapping(_ptr(block_tables), block_tables.shape[0], block_tables.shape[1],
+    with _on(dev):
+        st = _lib.lib().pa_slot_mapping(_ptr(block_tables), block_tables.shape[0], block_tables.shape[1],
                                     _ptr(seq_idx), _ptr(positions), positions.shape[0], block_size,
                                     num_blocks, _ptr(out), _stream(dev))
     _lib.check("pa_slot_mapping", st)
@@ -110,7 +118,8 @@ def write_kv(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
     _check_act(key, k_cache, "key/value")
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == key.shape[:1], "slot_mapping: int64 [T]")
     cache = make_cache(k_cache, v_cache, act_dtype=key.dtype, k_scale=k_scale, v_scale=v_scale)
-    st = _lib.lib().pa_write_kv(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
+    with _on(dev):
+        st = _lib.lib().pa_write_kv(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
                                 ctypes.byref(cache), _stream(dev))
     _lib.check("pa_write_kv", st)
 
@@ -132,7 +141,8 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
     fp8 = dict(act_dtype=torch.float16, k_scale=1.0, v_scale=1.0)  # codes are copied as bytes
     arr = (_lib.PaCache * len(k_caches))(
         *[make_cache(k, v, **(fp8 if is_fp8_cache(k) else {})) for k, v in zip(k_caches, v_caches)])
-    st = _lib.lib().pa_copy_blocks(arr, len(k_caches), _ptr(pairs), pairs.shape[0], _stream(dev))
+    with _on(dev):
+        st = _lib.lib().pa_copy_blocks(arr, len(k_caches), _ptr(pairs), pairs.shape[0], _stream(dev))
     _lib.check("pa_copy_blocks", st)
 
 
@@ -175,6 +185,24 @@ def swap_blocks(src_k: Sequence[torch.Tensor], src_v: Sequence[torch.Tensor],
     _lib.check("pa_swap_blocks", st)
 
 
+def prefix_key_offsets(token_offsets: torch.Tensor, block_size: int,
+                       out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """int64 [N + 1] first key of each sequence when full-block keys are packed
+    back to back (``out[s + 1] - out[s]`` = floor(len_s / block_size)),
+    computed on the device by pa_prefix_key_offsets."""
+    dev = _cuda(token_offsets)
+    _need(token_offsets.dtype == torch.int64 and token_offsets.dim() == 1, "token_offsets: int64 [N + 1]")
+    if out is None:
+        out = torch.empty_like(token_offsets)
+    _cuda(out, token_offsets)
+    _need(out.dtype == torch.int64 and out.shape == token_offsets.shape, "out: int64 [N + 1]")
+    with _on(dev):
+        st = _lib.lib().pa_prefix_key_offsets(_ptr(token_offsets), token_offsets.shape[0] - 1,
+                                              int(block_size), _ptr(out), _stream(dev))
+    _lib.check("pa_prefix_key_offsets", st)
+    return out
+
+
 def prefix_hash(token_ids: torch.Tensor, token_offsets: torch.Tensor, block_size: int, *,
                 key_offsets: Optional[torch.Tensor] = None, root: Optional[bytes] = None,
                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -182,16 +210,15 @@ def prefix_hash(token_ids: torch.Tensor, token_offsets: torch.Tensor, block_size
     int32 ids of block j), key_{-1} = ``root`` (32 bytes, zeros by default).
     ``token_offsets`` (int64 [N + 1]) splits ``token_ids`` (int32) into
     sequences; returns uint8 [sum_s floor(len_s / block_size), 32]. Without
-    ``key_offsets`` they are computed here from the lengths (one copy of the
-    offsets to the host)."""
+    ``key_offsets`` the library computes the packed layout
+    (:func:`prefix_key_offsets`); only its last entry, the key count, is read
+    back to size ``out`` when ``out`` is not given."""
     dev = _cuda(token_ids, token_offsets)
     _need(token_ids.dtype == torch.int32 and token_ids.dim() == 1, "token_ids: int32 [T]")
     _need(token_offsets.dtype == torch.int64 and token_offsets.dim() == 1, "token_offsets: int64 [N + 1]")
     n = token_offsets.shape[0] - 1
     if key_offsets is None:
-        lens = torch.diff(token_offsets.cpu())
-        key_offsets = torch.cat([torch.zeros(1, dtype=torch.int64),
-                                 torch.cumsum(lens // block_size, 0)]).to(dev)
+        key_offsets = prefix_key_offsets(token_offsets, block_size)
     _cuda(key_offsets, token_ids)
     _need(key_offsets.dtype == torch.int64 and key_offsets.shape == token_offsets.shape,
           "key_offsets: int64 [N + 1]")
@@ -201,9 +228,10 @@ def prefix_hash(token_ids: torch.Tensor, token_offsets: torch.Tensor, block_size
     _cuda(out, token_ids)
     _need(out.dtype == torch.uint8 and out.dim() == 2 and out.shape[1] == 32, "out: uint8 [K, 32]")
     _need(root is None or len(root) == 32, "root: 32 bytes")
-    st = _lib.lib().pa_prefix_hash(_ptr(token_ids), _ptr(token_offsets), _ptr(key_offsets), n,
-                                   int(block_size), None if root is None else bytes(root),
-                                   _ptr(out), _stream(dev))
+    with _on(dev):
+        st = _lib.lib().pa_prefix_hash(_ptr(token_ids), _ptr(token_offsets), _ptr(key_offsets), n,
+                                       int(block_size), None if root is None else bytes(root),
+                                       _ptr(out), _stream(dev))
     _lib.check("pa_prefix_hash", st)
     return out
 
@@ -276,7 +304,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     if workspace is not None:
         _cuda(workspace, q)
     cache = make_cache(k_cache, v_cache, act_dtype=q.dtype, k_scale=k_scale, v_scale=v_scale)
-    st = _lib.lib().pa_decode(_ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables),
+    with _on(dev):
+        st = _lib.lib().pa_decode(_ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables),
                               block_tables.shape[1], _ptr(seq_lens), int(max_seq_len), float(scale),
                               _ptr(out), _DTYPES[out.dtype], int(partition_tokens), _ptr(workspace),
                               0 if workspace is None else workspace.numel() * workspace.element_size(),
@@ -343,7 +372,8 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
                                           int(max_q_len), dev)
     if workspace is not None:
         _cuda(workspace, q)
-    st = _lib.lib().pa_prefill(_ptr(q), n, _ptr(q_start), int(max_q_len), hq, ctypes.byref(cache),
+    with _on(dev):
+        st = _lib.lib().pa_prefill(_ptr(q), n, _ptr(q_start), int(max_q_len), hq, ctypes.byref(cache),
                                _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
                                float(scale), _ptr(out), _DTYPES[out.dtype], _ptr(workspace),
                                0 if workspace is None else workspace.numel() * workspace.element_size(),
@@ -378,7 +408,8 @@ def decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     _cuda(out, q)
     _need(out.shape == q.shape and out.dtype in _DTYPES, "out: [N, Hq, D] of float16/bfloat16/float32")
     cache = make_cache(k_cache, v_cache, act_dtype=q.dtype, k_scale=k_scale, v_scale=v_scale)
-    st = _lib.lib().pa_decode_static_workspace(
+    with _on(dev):
+        st = _lib.lib().pa_decode_static_workspace(
         _ptr(q), n, hq, ctypes.byref(cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), int(max_seq_len), float(scale), _ptr(out), _DTYPES[out.dtype],
         int(partition_tokens), _stream(dev))

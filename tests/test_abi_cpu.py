@@ -40,9 +40,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert re.search(rf"\bT {name}\b", nm), f"{name} not exported as a text symbol"
 
 
+def test_static_workspace_size_matches_header():
+    """The binding's copy of PA_STATIC_WORKSPACE_BYTES is the header's value."""
+    import paged_kv_cache_114_gb300 as pa
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    m = re.search(r"#define PA_STATIC_WORKSPACE_BYTES \(([0-9u*\s]+)\)", text)
+    assert m is not None
+    value = 1
+    for f in m.group(1).split("*"):
+        value *= int(f.strip().rstrip("u"))
+    assert value == pa.STATIC_WORKSPACE_BYTES
+
+
 def test_version_and_status_strings(lib):
     import paged_kv_cache_114_gb300._lib as L
-    assert lib.pa_abi_version() == L.ABI_VERSION == 3
+    assert lib.pa_abi_version() == L.ABI_VERSION == 4
     assert lib.pa_status_string(0) == b"ok"
     assert lib.pa_status_string(-5).startswith(b"workspace")
     assert lib.pa_status_string(12345) == b"unknown status"

@@ -83,3 +83,30 @@ def test_wrong_key_range_is_flagged(dev):
     pa.prefix_hash(toks, off, 16, key_offsets=bad, out=out)
     assert pa.get_device_error(dev) & pa.DEVERR_SEQ_LEN
     assert torch.count_nonzero(out[:3]) == 0  # sequence 0 wrote nothing
+
+
+@pytest.mark.parametrize("n_seqs", [0, 1, 5, 8192, 8193, 20000])
+def test_key_offsets_on_device(dev, n_seqs):
+    """pa_prefix_key_offsets packs floor(len / b) keys per sequence back to
+    back, exactly the oracle's key counts summed in order; chunk edges of the
+    device scan (8,192 sequences) included."""
+    import paged_kv_cache_114_gb300 as pa
+    rng = np.random.default_rng(n_seqs)
+    lens = rng.integers(0, 200, n_seqs)
+    lens[::7] = 0
+    off = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)).to(dev)
+    for b in (1, 16, 33):
+        got = pa.prefix_key_offsets(off, b).cpu().numpy()
+        counts = [len(oracle.prefix_block_keys([0] * int(n), b)) for n in lens] if n_seqs <= 5 \
+            else (lens // b).tolist()
+        want = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+        assert pa.get_device_error(dev) == 0
+        assert np.array_equal(got, want)
+
+
+def test_negative_length_is_flagged_in_offsets(dev):
+    import paged_kv_cache_114_gb300 as pa
+    off = torch.tensor([0, 40, 30, 64], dtype=torch.int64, device=dev)  # sequence 1 has length -10
+    got = pa.prefix_key_offsets(off, 16).cpu().numpy()
+    assert pa.get_device_error(dev) & pa.DEVERR_SEQ_LEN
+    assert got.tolist() == [0, 2, 2, 4]

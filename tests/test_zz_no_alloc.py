@@ -5,14 +5,16 @@ application whose own pool owns all device memory, latency-critical paths
 where cudaMalloc may synchronise the device, runtimes with no device
 allocator). Its partials live in a fixed array inside the library. These tests
 check it, through the C ABI, against pa_decode with a caller-allocated
-workspace, on two calls in a row, and check that a too-large request is
-refused. The file is named so that pytest collects it last.
+workspace, on two calls in a row (bit for bit: the same kernels run on the
+same inputs), and check that a too-large request is refused, including the
+balanced mode's fixed-size partials for a large query group. The file is
+named so that pytest collects it last.
 """
 import numpy as np
 import pytest
 import torch
 
-from tests.helpers import ATOL, to_dev
+from tests.helpers import to_dev
 from workloads import make_random_case
 
 pytestmark = pytest.mark.gpu
@@ -57,7 +59,8 @@ def test_static_workspace_matches_caller_workspace(dev, part):
                                    max_seq_len=w.max_seq_len, partition_tokens=part, out=got)
         assert pa.get_device_error(dev) == 0
         assert torch.all(torch.isfinite(got))
-        assert torch.max(torch.abs(got - want)).item() <= ATOL
+        # the same kernels on the same inputs: only where the partials live differs
+        assert torch.equal(got, want)
 
 
 def test_static_workspace_refuses_oversize(dev):
@@ -74,3 +77,28 @@ def test_static_workspace_refuses_oversize(dev):
         pa.decode_static_workspace(t["q"], t["k"], t["v"], t["tables"], t["lens"], w.scale,
                                    max_seq_len=max_len, partition_tokens=16)
     assert pa.get_device_error(dev) == 0
+
+
+def test_static_workspace_refuses_large_group_balanced(dev):
+    """The balanced mode's partials scale with the SM count and the query group,
+    not the batch: at g = 16, head_dim 128 they exceed the array on a GB300
+    even for one sequence, while a fixed partition size still fits."""
+    import paged_kv_cache_114_gb300 as pa
+    w = make_random_case(2026, num_seqs=1, num_q_heads=32, num_kv_heads=2, head_dim=128,
+                         block_size=16, seq_lens=[700], dtype="f16")
+    t = _upload(w, dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    need = pa.decode_workspace_bytes(1, 32, 2, 128, w.max_seq_len, -1)
+    assert need >= 16 * sms * 16 * 130 * 4
+    if need <= pa.STATIC_WORKSPACE_BYTES:
+        pytest.skip(f"{sms} SMs: the balanced partials fit the array")
+    with pytest.raises(pa.PagedKVError, match="workspace"):
+        pa.decode_static_workspace(t["q"], t["k"], t["v"], t["tables"], t["lens"], w.scale,
+                                   max_seq_len=w.max_seq_len, partition_tokens=-1)
+    want = pa.decode(t["q"], t["k"], t["v"], t["tables"], t["lens"], w.scale,
+                     max_seq_len=w.max_seq_len, out_dtype=torch.float32, partition_tokens=256)
+    got = pa.decode_static_workspace(t["q"], t["k"], t["v"], t["tables"], t["lens"], w.scale,
+                                     max_seq_len=w.max_seq_len, partition_tokens=256,
+                                     out_dtype=torch.float32)
+    assert pa.get_device_error(dev) == 0
+    assert torch.equal(got, want)
