@@ -397,6 +397,21 @@ int pa_decode_static_workspace(const void* q, int32_t num_seqs, int32_t num_q_he
                                int32_t max_seq_len, float scale, void* out, pa_dtype out_dtype,
                                int32_t partition_tokens, void* stream);
 
+/*
+ * pa_test_set_stall - test hook for the bounded waits; not for production use.
+ * With stop_stage >= 0, every later pa_decode call, and pa_prefill on the
+ * tcgen05 kernel, runs with each TMA ring issuing only its first stop_stage
+ * stages of K/V copies, and a consumer's wait for a stage bounded by wait_us
+ * microseconds (1 .. 1,000,000) instead of 2 s. The consumers of the stages
+ * that never arrive give up, set PA_DEVERR_TIMEOUT and finish without them;
+ * the copies that were issued are still waited for (under the full bound), so
+ * no copy is in flight when a CTA exits and the context stays usable. Rows
+ * that lost stages hold unspecified values. stop_stage < 0 turns the hook off
+ * (the default). The setting is process-wide; calls made while it changes may
+ * see either value. Returns PA_ERR_ARG for a wait_us out of range.
+ */
+int pa_test_set_stall(int32_t stop_stage, uint32_t wait_us);
+
 /* Synchronise `stream`, copy the current device's error word to *err_out and
  * clear it. */
 int pa_get_device_error(int32_t* err_out, void* stream);

@@ -28,7 +28,7 @@ EXPORTED = (
     "pa_decode_workspace_bytes", "pa_decode_default_partition", "pa_get_device_error",
     "pa_status_string", "pa_abi_version", "pa_decode_static_workspace", "pa_decode_kernel_name",
     "pa_prefill", "pa_prefill_workspace_bytes", "pa_prefill_kernel_name", "pa_swap_blocks",
-    "pa_prefix_hash", "pa_prefix_key_offsets",
+    "pa_prefix_hash", "pa_prefix_key_offsets", "pa_test_set_stall",
 )
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
@@ -83,6 +83,7 @@ def _declare(lib):
         "pa_decode_default_partition": (i32, [i32, i32, i32, i32]),
         "pa_decode_kernel_name": (ctypes.c_char_p, [i32, i32, i32, i32, i32, i32]),
         "pa_get_device_error": (ctypes.c_int, [ctypes.POINTER(i32), vp]),
+        "pa_test_set_stall": (ctypes.c_int, [i32, ctypes.c_uint32]),
         "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "pa_abi_version": (ctypes.c_int, []),
     }

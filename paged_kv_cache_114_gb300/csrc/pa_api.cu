@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <atomic>
 #include <mutex>
 #include <unordered_set>
 
@@ -25,6 +26,10 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
+
+// pa_test_set_stall: copied into the kernels' arguments by every later call.
+std::atomic<int32_t> g_stall_stage{-1};
+std::atomic<uint32_t> g_stall_wait_ns{0};
 
 // The device address of g_device_error and the SM count of the current device.
 // The address comes from cudaGetSymbolAddress once per device: in host code
@@ -275,6 +280,13 @@ const char* pa_status_string(int status) {
     case PA_ERR_PAIRS: return "copy pairs violate the distinct-destination rule";
     default: return "unknown status";
   }
+}
+
+int pa_test_set_stall(int32_t stop_stage, uint32_t wait_us) {
+  if (stop_stage >= 0 && (wait_us == 0 || wait_us > 1000000u)) return PA_ERR_ARG;
+  g_stall_wait_ns.store(stop_stage >= 0 ? wait_us * 1000u : 0u);
+  g_stall_stage.store(stop_stage >= 0 ? stop_stage : -1);
+  return PA_OK;
 }
 
 int pa_get_device_error(int32_t* err_out, void* stream) {
@@ -620,6 +632,8 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
                                     (fp8 ? static_cast<double>(cache->k_scale) : 1.0) *
                                     1.4426950408889634);
   a.v_scale = fp8 ? cache->v_scale : 1.f;
+  a.test_stop_stage = g_stall_stage.load();
+  a.test_wait_ns = g_stall_wait_ns.load();
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   a.err = di.err;
@@ -769,6 +783,8 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   const double kscale = fp8 ? static_cast<double>(cache->k_scale) : 1.0;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kscale * 1.4426950408889634);
   a.v_scale = fp8 ? cache->v_scale : 1.f;
+  a.test_stop_stage = g_stall_stage.load();
+  a.test_wait_ns = g_stall_wait_ns.load();
   dim3 grid(static_cast<unsigned>(hkv), static_cast<unsigned>(parts),
             static_cast<unsigned>(num_seqs));
   if (!balanced && parts > 1) {

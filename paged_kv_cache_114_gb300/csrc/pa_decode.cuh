@@ -783,11 +783,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const uint32_t ring = sm_base + warp * NS * S::kStageBytes;
   uint8_t* const ring_ptr = sm + warp * NS * S::kStageBytes;
   const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
+  int n_issued = 0;  // stages 0 .. n_issued - 1 have their copies issued
   auto issue = [&](int it) {
+    if (a.test_stop_stage >= 0 && it >= a.test_stop_stage) return;
     const int slot = it % NS;
     issue_stage<D, FP8>(a, &tmk, &tmv, table_row, kvh, tok_begin + (warp + it * W) * tt, tok_end,
                         ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
+    n_issued = it + 1;
   };
+  const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kWaitLimitNs);
 
   Acc<D, NT> acc;
   acc.reset();
@@ -798,7 +802,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   int it = 0;
   for (; it < my_n; ++it) {
     const int slot = it % NS;
-    const bool got = mbar_wait_bounded(bar0 + 8 * slot, (it / NS) & 1, kWaitLimitNs);
+    const bool got = mbar_wait_bounded(bar0 + 8 * slot, (it / NS) & 1, wait_ns);
     if (__any_sync(0xffffffffu, !got)) {
       aborted = true;
       break;
@@ -813,8 +817,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   if (aborted) {
     if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
-    const int last = (it + NS < my_n) ? it + NS : my_n;
-    for (int j = it; j < last; ++j) mbar_wait_bounded(bar0 + 8 * (j % NS), (j / NS) & 1, kWaitLimitNs);
+    // copies this warp issued and has not consumed complete before it moves on
+    for (int j = it; j < n_issued; ++j) mbar_wait_bounded(bar0 + 8 * (j % NS), (j / NS) & 1, kWaitLimitNs);
     acc.reset();
   }
   acc.reduce_l();
@@ -1136,12 +1140,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   Cursor ic = cursor_at(a, pre, g0);  // next stage to issue
   Cursor cc = ic;                     // stage being computed
+  int n_issued = 0;  // stages 0 .. n_issued - 1 have their copies issued
   auto issue = [&](int it) {
+    if (a.test_stop_stage >= 0 && it >= a.test_stop_stage) return;
     const int slot = it % NS;
     issue_stage<D, FP8>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, kvh, ic.j * tt,
                         ic.len, ring + slot * S::kStageBytes, bar0 + 8 * slot, masks + slot, lane);
     cursor_next(a, pre, ic);
+    n_issued = it + 1;
   };
+  const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kWaitLimitNs);
   const int pro = count < NS ? count : NS;
   for (int i = 0; i < pro; ++i) issue(i);
 
@@ -1155,12 +1163,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   for (int it = 0; it < count; ++it) {
     const int slot = it % NS;
     if (!aborted) {
-      const bool got = mbar_wait_bounded(bar0 + 8 * slot, (it / NS) & 1, kWaitLimitNs);
+      const bool got = mbar_wait_bounded(bar0 + 8 * slot, (it / NS) & 1, wait_ns);
       if (__any_sync(0xffffffffu, !got)) {
         aborted = true;
         if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
-        const int last = (it + NS < count) ? it + NS : count;
-        for (int j = it; j < last; ++j)
+        for (int j = it; j < n_issued; ++j)
           mbar_wait_bounded(bar0 + 8 * (j % NS), (j / NS) & 1, kWaitLimitNs);
       }
     }

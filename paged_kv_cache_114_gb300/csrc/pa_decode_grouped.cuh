@@ -161,7 +161,8 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
     // ------------------------------------------------------------ producer
     Cursor ic = cursor_at(a, pre, g0);
     int issued = 0;
-    for (; issued < count; ++issued) {
+    const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < count ? a.test_stop_stage : count;
+    for (; issued < stop; ++issued) {
       const int slot = issued % NS;
       if (issued >= NS) {  // every consumer released this slot's previous stage
         const bool got = mbar_wait_bounded(empty0 + 8 * slot, ((issued / NS) - 1) & 1, kWaitLimitNs);
@@ -202,10 +203,11 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   acc.reset();
   bool aborted = false;
 
+  const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kWaitLimitNs);
   for (int it = 0; it < count; ++it) {
     const int slot = it % NS;
     if (!aborted) {
-      const bool got = mbar_wait_bounded(full0 + 8 * slot, (it / NS) & 1, kWaitLimitNs);
+      const bool got = mbar_wait_bounded(full0 + 8 * slot, (it / NS) & 1, wait_ns);
       if (__any_sync(0xffffffffu, !got)) {
         aborted = true;
         if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);

@@ -35,7 +35,18 @@ struct DecodeArgs {
   // Multi-token rows (pa_prefill on the grouped kernel); unused by decode.
   const int32_t* q_start;        // [N + 1] query rows of each sequence
   int32_t max_q;                 // bound of every n_s; rows past it are not computed
+  // Stall hook for tests of the bounded waits (pa_test_set_stall): when
+  // test_stop_stage >= 0, each TMA ring issues only its first test_stop_stage
+  // stages, and a consumer waits test_wait_ns (not the 2 s bound) for a stage
+  // before giving up with PA_DEVERR_TIMEOUT. Copies already issued are still
+  // drained under the full bound, so no copy is in flight when a CTA exits.
+  int32_t test_stop_stage = -1;  // < 0: off
+  uint32_t test_wait_ns = 0;
 };
+
+// The bound a consumer's wait for a TMA stage uses (the test hook can shorten it).
+#define PA_STAGE_WAIT_NS(args, full_ns) \
+  ((args).test_stop_stage >= 0 && (args).test_wait_ns > 0 ? static_cast<uint64_t>((args).test_wait_ns) : (full_ns))
 
 // Rows of shared memory one pipeline stage holds (one m16 tile of tokens).
 constexpr int kStageRows = 16;
@@ -118,6 +129,8 @@ struct PrefillArgs {
   int32_t out_dtype;             // pa_dtype
   float scale_log2;              // scale * log2(e) (times k_scale for E4M3 caches)
   float v_scale;                 // E4M3 caches: V code c stands for value(c) * v_scale
+  int32_t test_stop_stage = -1;  // stall hook, as in DecodeArgs (tcgen05 kernel)
+  uint32_t test_wait_ns = 0;
 };
 // Grid: (ceil(max_q_len * g / 64), H_kv, N). bf16: q/out MMA type (the act
 // dtype for E4M3 caches); fp8: E4M3 cache (head_dim 128 or 256); thin: head

@@ -289,11 +289,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Bounded wait that also gives up once another role of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile uint32_t* abort) {
+                                              volatile uint32_t* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-    if (*abort != 0u || globaltimer_ns() - t0 > kLimitTcNs) return false;
+    if (*abort != 0u || globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -439,15 +439,18 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
+  // bound of every wait that depends on a K/V tile arriving (the test hook can shorten it)
+  const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kLimitTcNs);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     const int tpo = a.tok_per_op;
+    const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < ntiles ? a.test_stop_stage : ntiles;
     int issued = 0;
-    for (; issued < ntiles; ++issued) {
+    for (; issued < stop; ++issued) {
       const int slot = issued % LS;
       if (issued >= LS &&
-          !wait_or_abort(kv_empty(slot), ((issued / LS) - 1) & 1, abort)) {
+          !wait_or_abort(kv_empty(slot), ((issued / LS) - 1) & 1, abort, wait_ns)) {
         if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
         break;
       }
@@ -503,8 +506,8 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
     auto mma_tile = [&](int t) { return t % NB; };
     // wait until tile t is readable by the MMAs
     auto tile_ready = [&](int t) {
-      return FP8 ? wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort)
-                 : wait_or_abort(kv_full(t % LS), (t / LS) & 1, abort);
+      return FP8 ? wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort, wait_ns)
+                 : wait_or_abort(kv_full(t % LS), (t / LS) & 1, abort, wait_ns);
     };
     // A descriptor's start address is its low 14 bits in 16-byte units and
     // shared memory stays below 256 KB, so an offset is a plain add: one
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
         }
         for (int q = 0; ok && q < kQTiles; ++q) {
           if (t >= nt[q]) continue;
-          ok = wait_or_abort(p_full(q, t & 1), (t >> 1) & 1, abort);
+          ok = wait_or_abort(p_full(q, t & 1), (t >> 1) & 1, abort, wait_ns);
           if (!ok) break;
           tc_fence_after();
           issue_pv(q, t);
@@ -577,11 +580,11 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
     for (int t = 0; t < ntiles; ++t) {
       const int slot = t % LS;
       const int b = t % NB;
-      if (!wait_or_abort(kv_full(slot), (t / LS) & 1, abort)) {
+      if (!wait_or_abort(kv_full(slot), (t / LS) & 1, abort, wait_ns)) {
         if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
         break;
       }
-      if (t >= NB && !wait_or_abort(conv_empty(b), ((t / NB) - 1) & 1, abort)) {
+      if (t >= NB && !wait_or_abort(conv_empty(b), ((t / NB) - 1) & 1, abort, wait_ns)) {
         if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
         break;
       }
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
     const int my_tiles = nt[q];
     for (int t = 0; t < my_tiles; ++t) {
       const int slot = t % LS;
-      if (!wait_or_abort(s_full(q, t & 1), (t >> 1) & 1, abort)) { ok = false; break; }
+      if (!wait_or_abort(s_full(q, t & 1), (t >> 1) & 1, abort, wait_ns)) { ok = false; break; }
       tc_fence_after();
       float x[kBn];
       tmem_ld64(s_col + (t & 1) * kBn, x);
@@ -656,10 +659,10 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       // (FP8: the K converter copied it before arming conv_full)
       uint64_t vmask;
       if constexpr (FP8) {
-        if (!wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort)) { ok = false; break; }
+        if (!wait_or_abort(conv_full(t % NB), (t / NB) & 1, abort, wait_ns)) { ok = false; break; }
         vmask = conv_masks[t % NB];
       } else {
-        if (!wait_or_abort(kv_full(slot), (t / LS) & 1, abort)) { ok = false; break; }
+        if (!wait_or_abort(kv_full(slot), (t / LS) & 1, abort, wait_ns)) { ok = false; break; }
         vmask = masks[slot];
       }
       const int k0 = t * kBn;
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       const float alpha = grow ? exp2f(m - m_use) : 1.f;
       // O is rescaled only after the previous O update of this tile completed
       if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) {
-        if (!wait_or_abort(o_done(q, (t - 1) & 1), ((t - 1) >> 1) & 1, abort)) { ok = false; break; }
+        if (!wait_or_abort(o_done(q, (t - 1) & 1), ((t - 1) >> 1) & 1, abort, wait_ns)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kD; c += 32) {
@@ -763,7 +766,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
     } else if (my_tiles > 0) {
       // ---- epilogue: O / l once the last P V has completed
-      if (wait_or_abort(o_done(q, (my_tiles - 1) & 1), ((my_tiles - 1) >> 1) & 1, abort)) {
+      if (wait_or_abort(o_done(q, (my_tiles - 1) & 1), ((my_tiles - 1) >> 1) & 1, abort, wait_ns)) {
         tc_fence_after();
         const float inv = l > 0.f ? (FP8 ? a.v_scale : 1.f) / l : 0.f;
         const int64_t ob = row_ok ? ((static_cast<int64_t>(q0) + i) * a.num_q_heads +

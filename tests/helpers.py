@@ -96,15 +96,3 @@ def assert_close(got: torch.Tensor, want: np.ndarray, heads=None, what=""):
     worst = float(np.max(err - tol)) if err.size else -1.0
     assert worst <= 0, f"{what}: max abs error {float(err.max()):.3e} exceeds tolerance"
     return float(err.max()) if err.size else 0.0
-
-
-def sample_heads(w, n: int, seed: int = 0):
-    """(s, h) pairs: the longest and shortest sequences, group edges, then random."""
-    rng = np.random.default_rng(seed)
-    lens = w.seq_lens
-    g = w.group
-    picks = {(int(np.argmax(lens)), 0), (int(np.argmax(lens)), w.num_q_heads - 1),
-             (int(np.argmin(lens)), g - 1), (int(np.argmin(lens)), w.num_q_heads // 2)}
-    while len(picks) < n:
-        picks.add((int(rng.integers(0, w.num_seqs)), int(rng.integers(0, w.num_q_heads))))
-    return sorted(picks)

@@ -7,9 +7,8 @@ import numpy as np
 import pytest
 import torch
 
-from tests.helpers import (assert_close, bits_of, gpu_scenario, oracle_scenario, sample_heads,
-                           to_dev)
-from workloads import make_config, make_random_case
+from tests.helpers import assert_close, bits_of, gpu_scenario, oracle_scenario, to_dev
+from workloads import make_config, make_config5_steps, make_random_case
 
 pytestmark = pytest.mark.gpu
 
@@ -120,13 +119,15 @@ def test_repeat_is_deterministic(dev):
 # ---------------------------------------------------------------- full-size configs
 
 
-def _full_config(dev, w, n_heads=48, partition=None):
+def _full_config(dev, w, partition=None):
+    """The whole scenario on the device and in the oracle; every (sequence,
+    head) output row is compared, the pieces the balanced split cuts across
+    CTAs (merged by the last arriver) included."""
     res = gpu_scenario(w, dev, partition_tokens=partition)
-    heads = sample_heads(w, n_heads)
-    ref = oracle_scenario(w, heads=heads)
+    ref = oracle_scenario(w)
     assert res["err"] == 0
     _check_bytes(res, ref)
-    return res, ref, heads
+    return res, ref, None
 
 
 def test_config2_mha_full(dev):
@@ -145,7 +146,7 @@ def test_config3_gqa_full(dev):
 @pytest.mark.parametrize("b", [8, 16, 32])
 def test_config4_long_split_full(dev, b, partition):
     w = make_config(4, block_size=b)
-    res, ref, heads = _full_config(dev, w, n_heads=24, partition=partition)
+    res, ref, heads = _full_config(dev, w, partition=partition)
     assert_close(res["out"], ref["out"], heads, what=f"config 4 b={b} partition {partition}")
 
 
@@ -176,6 +177,58 @@ def test_config5_prefix_cow_full(dev):
                      out_dtype=torch.float32)
     assert pa.get_device_error(dev) == 0
     assert torch.equal(out2, res["out"])
+
+
+@pytest.mark.parametrize("kv", [None, "e4m3"])
+def test_config5_decode_steps(dev, kv):
+    """Config 5 as a decode loop: 32 steps of slot mapping, KV write of one new
+    token per sequence and decode, on 256 sequences sharing a 1000-token prefix.
+    Step 0 copies the shared partial block for 255 sequences (copy-on-write)
+    before the write lands in the copies; steps 8 and 24 open fresh blocks.
+    Every step's slots and every output row are compared with the oracle
+    running the same loop, and the pools byte for byte at the end."""
+    import oracle
+    import paged_kv_cache_114_gb300 as pa
+    w = make_config5_steps(32, kv_dtype=kv)
+    fp8 = kv == "e4m3"
+    sc = dict(k_scale=w["k_scale"], v_scale=w["v_scale"]) if fp8 else {}
+    if fp8:
+        k, v = to_dev(w["k_cache"], dev), to_dev(w["v_cache"], dev)
+    else:
+        k, v = to_dev(w["k_cache"], dev, w["dtype"]), to_dev(w["v_cache"], dev, w["dtype"])
+    ko, vo = w["k_cache"], w["v_cache"]
+    part = pa.default_partition(w["num_seqs"], w["num_kv_heads"], 1032, w["block_size"])
+    for i, st in enumerate(w["steps"]):
+        if len(st["pairs"]):
+            pa.copy_blocks([k], [v], to_dev(st["pairs"], dev))
+            ks, vs = oracle.copy_blocks([ko], [vo], [tuple(p) for p in st["pairs"].tolist()])
+            ko, vo = ks[0], vs[0]
+        tables = to_dev(st["block_tables"], dev)
+        slots = pa.slot_mapping(tables, to_dev(st["seq_idx"], dev), to_dev(st["positions"], dev),
+                                w["block_size"], w["num_blocks"])
+        pa.write_kv(to_dev(st["key"], dev, w["dtype"]), to_dev(st["value"], dev, w["dtype"]), slots,
+                    k, v, **sc)
+        out = torch.full((w["num_seqs"], w["num_q_heads"], w["head_dim"]), float("nan"),
+                         dtype=torch.float32, device=dev)
+        pa.decode(to_dev(st["q"], dev, w["dtype"]), k, v, tables, to_dev(st["seq_lens"], dev),
+                  w["scale"], max_seq_len=int(st["seq_lens"].max()), out=out,
+                  partition_tokens=part, **sc)
+        assert pa.get_device_error(dev) == 0, f"step {i}"
+        so = oracle.slot_mapping(st["block_tables"], st["seq_idx"], st["positions"], w["block_size"])
+        assert np.array_equal(slots.cpu().numpy(), so), f"step {i}: slots differ"
+        if fp8:
+            ko, vo = oracle.write_kv_e4m3(ko, vo, st["key"], st["value"], so, w["dtype"],
+                                          w["k_scale"], w["v_scale"])
+            want = oracle.decode(st["q"], ko, vo, st["block_tables"], st["seq_lens"], w["scale"],
+                                 w["dtype"], kv_dtype="e4m3", k_scale=w["k_scale"],
+                                 v_scale=w["v_scale"])
+        else:
+            ko, vo = oracle.write_kv(ko, vo, st["key"], st["value"], so)
+            want = oracle.decode(st["q"], ko, vo, st["block_tables"], st["seq_lens"], w["scale"],
+                                 w["dtype"])
+        assert_close(out, want, what=f"config 5 step {i}{' e4m3' if fp8 else ''}")
+    assert np.array_equal(bits_of(k), ko), "K pool bytes differ after 32 steps"
+    assert np.array_equal(bits_of(v), vo), "V pool bytes differ after 32 steps"
 
 
 # ---------------------------------------------------------------- device-side errors

@@ -417,6 +417,58 @@ def _config5(rng: np.random.Generator, kv_dtype: Optional[str] = None) -> Worklo
         **_fp8_fields(kv_dtype))
 
 
+def make_config5_steps(steps: int = 32, kv_dtype: Optional[str] = None, seed: int = 1005) -> dict:
+    """Config 5 as a decode loop: 256 sequences share one 1000-token prefix
+    (62 full blocks and 8 rows of a 63rd) and then take ``steps`` decode steps;
+    in step i every sequence appends its token at position 1000 + i.
+
+    Step 0's tokens land in the shared partial block, so every sequence but
+    the last to write copies it first (255 copy-on-write pairs, in sequence
+    order); steps 8 and 24 open a fresh block for every sequence. Returns the
+    initial pools (prefix rows filled, every other slot NaN) and, per step, the
+    copy pairs to apply before the write, the new tokens' (seq_idx, positions,
+    key, value), the step's q, the block tables and the lengths after the
+    write.
+    """
+    rng = np.random.default_rng(seed)
+    n, hq, hkv, d, b, dtype = 256, 32, 8, 128, 16, "f16"
+    prefix = 1000
+    need = 63 + n * (-(-(prefix + steps) // b) - 62)
+    nb = int(np.ceil(1.25 * need))
+    pool = BlockPool(nb, b, free_order=rng.permutation(nb))
+    root = SeqTable(pool)
+    root.admit(prefix)
+    prefix_blocks = list(root.table)
+    seqs = [root.fork() for _ in range(n)]
+    root.free()
+    cdt = kv_dtype or dtype
+    k, v, nan = _new_pool(nb, b, hkv, d, cdt)
+    fk, fv = _Filler(rng, cdt), _Filler(rng, cdt)
+    _fill_sequences(k, v, [prefix_blocks], [prefix], fk, fv, nan)
+    out_steps = []
+    for _ in range(steps):
+        pairs, positions = [], []
+        for sq in seqs:
+            positions.append(sq.length)
+            p = sq.append()
+            if p is not None:
+                pairs.append(p)
+        out_steps.append({
+            "pairs": np.array(pairs, dtype=np.int64).reshape(-1, 2),
+            "seq_idx": np.arange(n, dtype=np.int32),
+            "positions": np.array(positions, dtype=np.int32),
+            "key": _normal_bits(rng, (n, hkv, d), dtype),
+            "value": _normal_bits(rng, (n, hkv, d), dtype),
+            "q": _normal_bits(rng, (n, hq, d), dtype),
+            "block_tables": _pad_tables([sq.table for sq in seqs], 0),
+            "seq_lens": np.array([sq.length for sq in seqs], dtype=np.int32),
+        })
+    return {"name": "prefix_cow_steps_fp16_b16", "dtype": dtype, "num_seqs": n, "num_q_heads": hq,
+            "num_kv_heads": hkv, "head_dim": d, "block_size": b, "num_blocks": nb,
+            "scale": float(1.0 / np.sqrt(d)), "k_cache": k, "v_cache": v,
+            "shared_blocks": prefix_blocks, "steps": out_steps, **_fp8_fields(kv_dtype)}
+
+
 PREFILL_NAMES = ("verify4_70b_bf16_b16", "chunk512_gqa_bf16_b16", "prompt2k_mha_fp16_b16",
                  "verify4_long_bf16_b16")
 
