@@ -322,7 +322,8 @@ size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
 
 /* Name of the kernel pa_prefill launches for this shape, given a workspace
  * (with_workspace != 0) or not, on a device of num_sms SMs (0: the current
- * device): "multi_grouped_kernel", "prefill_tc_kernel" or "prefill_kernel";
+ * device): "multi_grouped_kernel", "prefill_tc_kernel" (tcgen05; with an
+ * E4M3 cache its variant "prefill_tc_e4m3_kernel" runs) or "prefill_kernel";
  * NULL for sizes it rejects (or num_sms 0 without a device). pa_prefill makes
  * the same choice from the same helper, and two more inputs that this call
  * takes as met: q and out 16-byte aligned (otherwise "prefill_tc_kernel"

@@ -34,7 +34,8 @@ def _units():
              ("pa_decode_reduce", "pa_decode_reduce.cu", []),
              ("pa_noalloc", "pa_noalloc.cu", []), ("pa_prefill", "pa_prefill.cu", []),
              ("pa_prefix_hash", "pa_prefix_hash.cu", []),
-             ("pa_prefill_tc", "pa_prefill_tc.cu", [])]
+             ("pa_prefill_tc", "pa_prefill_tc.cu", []),
+             ("pa_prefill_tc128", "pa_prefill_tc128.cu", [])]
     for bf in (0, 1):
         for d in (64, 128, 256):
             tag = f"pa_decode_{'bf16' if bf else 'f16'}_{d}"

@@ -235,15 +235,18 @@ MultiPlan multi_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads
 
 // Which kernel pa_prefill runs. The balanced grouped kernel needs its plan,
 // a workspace and a stage line whose per-sequence offsets fit int32; the
-// tcgen05 kernel needs head_dim 128, at least 128 (query, head) rows per KV
-// head and 16-byte aligned q and out (its rows move as 16-byte vectors);
+// tcgen05 kernels need head_dim 128, 128 to 2^30 (query, head) rows per KV
+// head (rows are numbered in int32) and 16-byte aligned q and out (its rows
+// move as 16-byte vectors);
 // everything else runs on the mma.sync kernel.
 enum PrefillKernel { kPrefillMulti, kPrefillTc, kPrefillMma };
 
 PrefillKernel route_prefill(bool multi_ok, bool have_workspace, bool line_fits, int32_t head_dim,
                             int64_t rows_per_kv_head, bool vec_aligned) {
   if (multi_ok && have_workspace && line_fits) return kPrefillMulti;
-  if (head_dim == 128 && rows_per_kv_head >= 128 && vec_aligned) return kPrefillTc;
+  if (head_dim == 128 && rows_per_kv_head >= 128 && rows_per_kv_head <= (1LL << 30) &&
+      vec_aligned)
+    return kPrefillTc;
   return kPrefillMma;
 }
 
@@ -712,7 +715,8 @@ int pa_prefill(const void* q, int32_t num_seqs, const int32_t* q_start, int32_t 
     const int64_t tiles256 = (static_cast<int64_t>(max_q_len) * g + 255) / 256;
     const dim3 grid(static_cast<unsigned>(tiles256), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));
-    e = pa::launch_prefill_tc(tk, tv, a, act_bf16, fp8, grid, static_cast<cudaStream_t>(stream));
+    e = fp8 ? pa::launch_prefill_tc_e4m3(tk, tv, a, act_bf16, grid, static_cast<cudaStream_t>(stream))
+            : pa::launch_prefill_tc128(tk, tv, a, act_bf16, grid, static_cast<cudaStream_t>(stream));
   } else {
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(hkv),
                     static_cast<unsigned>(num_seqs));

@@ -138,10 +138,13 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
                            int head_dim, bool bf16, bool fp8, bool thin, dim3 grid,
                            cudaStream_t st);
-// tcgen05/TMEM kernel for head_dim 128 (pa_prefill_tc.cu). Grid: (ceil(max_q_len * g / 256),
-// H_kv, N); needs q and out 16-byte aligned. fp8: E4M3 cache (q / out type bf16 or fp16).
-cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                              bool bf16, bool fp8, dim3 grid, cudaStream_t st);
+// tcgen05/TMEM kernels for head_dim 128. Grid: (ceil(max_q_len * g / 256), H_kv, N);
+// q and out 16-byte aligned. fp16 / bf16 caches: 128-key tiles (pa_prefill_tc128.cu);
+// E4M3 caches: 64-key tiles with converter warps (pa_prefill_tc.cu), bf16 = q / out type.
+cudaError_t launch_prefill_tc128(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
+                                 bool bf16, dim3 grid, cudaStream_t st);
+cudaError_t launch_prefill_tc_e4m3(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const PrefillArgs& a, bool bf16, dim3 grid, cudaStream_t st);
 
 // Merges split-K partials into out (pa_decode_reduce.cu).
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);
