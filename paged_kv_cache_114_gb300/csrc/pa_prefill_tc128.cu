@@ -16,7 +16,8 @@
 //   P = exp2(S * scale*log2e - m)   online softmax, one row per thread
 //   O += P V_t       tcgen05.mma M=128 N=128 K=16 (x8), P from TMEM, V MN-major
 // TMEM: row tile q uses columns 256q .. 256q+127 for S, overwritten in place
-// by P, and 256q+128 .. 256q+255 for O. Each row tile has one S buffer, so the
+// by P (each 32-column chunk of S holds its 32 keys' P: 16-bit pairs of the
+// high parts, then the bf16 low parts), and 256q+128 .. 256q+255 for O. Each row tile has one S buffer, so the
 // two tiles take turns on the tensor core: the MMA warp issues
 //   PV(A, t), S(A, t+1), PV(B, t), S(B, t+1), ...
 // and tile B's softmax of step t runs while the tensor core computes tile A's
@@ -25,22 +26,24 @@
 // it. Scores come 128 keys at a time, the N at which an MMA runs at the tensor
 // core's full rate.
 //
-// K and V tiles (32 KB each) stream through a ring of five shared-memory
-// slots in the order K_0, V_0, K_1, V_1, ..., so the producer runs two tiles
-// ahead of the MMAs. Warp 8 issues the TMA copies (one box of 64 head-dim
-// elements x block piece per column half) and publishes each tile's mask of
-// tokens with valid data; warp 9 issues the MMAs from one thread; warps 0-3
-// and 4-7 run the two softmaxes (warp w owns TMEM lanes 32 (w % 4) ..), so
-// every SM sub-partition alternates one warp of each.
+// K and V tiles (32 KB each) stream through a ring of four shared-memory
+// slots in the order K_0, V_0, K_1, V_1, ..., so the next tile loads while
+// the MMAs use the current one. Warp 16 issues the TMA copies (one box of 64
+// head-dim elements x block piece per column half) and publishes each tile's
+// mask of tokens with valid data; warp 17 issues the MMAs from one thread.
+// Sixteen warps run the softmaxes: warp w serves row tile (w / 4) % 2 in TMEM
+// lanes 32 (w % 4) .. and key / output-dim half w / 8, so every SM
+// sub-partition holds two warps of each row tile. The two halves of a row
+// meet once per tile in shared memory to agree on the running maximum.
 //
 // The running maximum rises only when a row's tile maximum passes it by more
 // than 8 (log2 units); the softmax warp then rescales its rows of O in TMEM
 // (the previous PV of its tile has completed: S was committed after it).
-// fp16 P carries 11 significant bits and is used whole. bf16 P carries 8: a
-// tile's P is split into a high and a low bf16 part (O += P_hi V + P_lo V,
-// about 16 bits per weight) when, for some row of the row tile, the tile's
-// weights sum to more than 1/8 of the row's running normaliser; otherwise the
-// high part alone is used. Every weight of an unsplit tile then errs by at most
+// fp16 P carries 11 significant bits and is used whole. bf16 P carries 8: it
+// is stored as a high and a low bf16 part, and the MMA warp adds the low part
+// (O += P_hi V + P_lo V, about 16 bits per weight) when, for some row of the
+// row tile, the tile's weights sum to more than 1/8 of the row's running
+// normaliser; otherwise the high part alone is used. Every weight of an unsplit tile then errs by at most
 // 2^-9 * 1/8 = 2^-12 of its row's total, the bound of a whole fp16 P.
 //
 // Masking: keys past a row's position get p = 0; V rows of tokens without
@@ -63,12 +66,12 @@ using namespace tc;
 constexpr int kD = 128;        // head dim
 constexpr int kRows = 128;     // query rows per row tile (TMEM lanes)
 constexpr int kKeys = 128;     // tokens per K/V tile
-constexpr int kSlots = 5;      // K/V ring slots (one K or V tile each)
+constexpr int kSlots = 4;      // K/V ring slots (one K or V tile each)
 constexpr int kMaskSlots = 8;  // per-tile valid-token masks in flight
-constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 16;  // per row tile: 4 lane groups x 2 column halves
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kLimitNs = 2000000000ull;
 constexpr float kShareLimit = 0.125f;  // bf16: split P when a tile's weight passes this share
@@ -81,11 +84,15 @@ struct Smem {
   static constexpr uint32_t kRing = kQ + 2 * kQTile;
   static constexpr uint32_t kBar = kRing + kSlots * kItem;
   // full[kSlots], empty[kSlots], mask_full[kMaskSlots], s_full[2], p_full[2],
-  // o_done[2], fin
-  static constexpr uint32_t kNumBars = 2 * kSlots + kMaskSlots + 2 + 2 + 2 + 1;
+  // o_done[2], fin, mx_bar[2], l_bar[2]
+  static constexpr uint32_t kNumBars = 2 * kSlots + kMaskSlots + 2 + 2 + 2 + 1 + 2 + 2;
   static constexpr uint32_t kMask = kBar + kNumBars * 8;        // 2 x uint64 per mask slot
   static constexpr uint32_t kVotes = kMask + kMaskSlots * 16;   // [row tile][parity][warp] u32
-  static constexpr uint32_t kMisc = kVotes + 2 * 2 * 4 * 4;     // tmem base, abort flag
+  // half-row maxima [parity][row tile][column half][row], then normalisers
+  // [row tile][column half][row]
+  static constexpr uint32_t kHalfMax = kVotes + 2 * 2 * 8 * 4;
+  static constexpr uint32_t kHalfSum = kHalfMax + 2 * 2 * 2 * kRows * 4;
+  static constexpr uint32_t kMisc = kHalfSum + 2 * 2 * kRows * 4;  // tmem base, abort flag
   static constexpr uint32_t kTotal = kMisc + 16 + 1024;         // + base-alignment slack
 };
 static_assert(Smem::kTotal <= 232448, "shared memory budget");
@@ -179,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_full = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 2 + q); };
   auto o_done = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 4 + q); };
   const uint32_t fin = bar + 8u * (2 * kSlots + kMaskSlots + 6);
+  auto mx_bar = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 7 + q); };
+  auto l_bar = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 9 + q); };
   uint64_t* masks = reinterpret_cast<uint64_t*>(sm + S::kMask);
   volatile uint32_t* votes = reinterpret_cast<volatile uint32_t*>(sm + S::kVotes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kMisc);
@@ -192,8 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaskSlots; ++i) mbar_init(mask_full(i), 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(s_full(q), 1);
-      mbar_init(p_full(q), 4);
+      mbar_init(p_full(q), 8);
       mbar_init(o_done(q), 1);
+      mbar_init(mx_bar(q), 8);
+      mbar_init(l_bar(q), 8);
     }
     mbar_init(fin, 1);
     *abort = 0u;
@@ -206,23 +217,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  // ---- Q rows into shared memory (K-major, 128-byte swizzle), one row per thread
+  // ---- Q rows into shared memory (K-major, 128-byte swizzle): the two
+  // softmax warps of a lane group take one 64-element half of each row
   if (warp < kSoftmaxWarps) {
-    const int q = warp >> 2;
+    const int q = (warp >> 2) & 1;
+    const int h = warp >> 3;
     const int r = (warp & 3) * 32 + lane;
     const int R = row0 + q * kRows + r;
     const uint4* src = nullptr;
     if (R < rows)
       src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
                                            ((static_cast<int64_t>(q0) + R / g) * a.num_q_heads +
-                                            static_cast<int64_t>(kvh) * g + R % g) * kD);
-    uint4 row[16];
+                                            static_cast<int64_t>(kvh) * g + R % g) * kD) + 8 * h;
+    uint4 row[8];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) row[c] = src != nullptr ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    for (int c = 0; c < 8; ++c) row[c] = src != nullptr ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint32_t off = S::kQ + q * S::kQTile + (c >> 3) * S::kHalf + r * 128u +
-                           (((c & 7) ^ (r & 7)) << 4);
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t off = S::kQ + q * S::kQTile + h * S::kHalf + r * 128u + ((c ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(sm + off) = row[c];
     }
   }
@@ -274,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m[1] &= (1ull << (valid_tokens - 64)) - 1ull;
         }
         // the slot was last read for tile t - kMaskSlots, whose softmaxes have
-        // finished: the ring holds at most two tiles ahead of the MMAs
+        // finished: issuing tile t - 1 needed V_{t-3} released, after every
+        // softmax of tile t - 3
         masks[2 * (t % kMaskSlots)] = m[0];
         masks[2 * (t % kMaskSlots) + 1] = m[1];
         mbar_arrive(mask_full(t % kMaskSlots));
@@ -327,14 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = dring_v + ((((2 * t + 1) % kSlots) * S::kItem) >> 4);
       const uint32_t p_col = tmem + q * 256u;
       const uint32_t d = tmem + q * 256u + 128u;
+      // keys 16kk .. 16kk + 15: chunk kk / 2, high parts at 32 (kk / 2) + 8 (kk % 2)
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk)
-        umma_tmem_a(d, p_col + kk * 8u, dv + ((kk * 16u * 128u) >> 4), id_o,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-      if (split) {
+        umma_tmem_a(d, p_col + 32u * (kk >> 1) + 8u * (kk & 1), dv + ((kk * 16u * 128u) >> 4),
+                    id_o, (t > 0 || kk > 0) ? 1u : 0u);
+      if (split) {  // low parts, 16 columns further on
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma_tmem_a(d, p_col + 64u + kk * 8u, dv + ((kk * 16u * 128u) >> 4), id_o, 1u);
+          umma_tmem_a(d, p_col + 32u * (kk >> 1) + 8u * (kk & 1) + 16u,
+                      dv + ((kk * 16u * 128u) >> 4), id_o, 1u);
       }
     };
     bool ok = true;
@@ -362,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           bool split = false;
           if constexpr (IS_BF16) {
-            const volatile uint32_t* v = votes + (q * 2 + (t & 1)) * 4;
-            split = (v[0] | v[1] | v[2] | v[3]) != 0u;
+            const volatile uint32_t* v = votes + (q * 2 + (t & 1)) * 8;
+            split = (v[0] | v[1] | v[2] | v[3] | v[4] | v[5] | v[6] | v[7]) != 0u;
           }
           issue_pv(q, t, split);
           if (t + 1 == nt[q]) umma_commit(o_done(q));
@@ -388,73 +403,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int q = warp >> 2;
+    // Warp w serves row tile q = (w / 4) % 2, TMEM lanes 32 (w % 4) .. and
+    // column half h = w / 8: keys 64h .. 64h + 63 of each tile and output
+    // dims 64h .. 64h + 63. The two halves of a row share the running maximum
+    // (each tile's half maxima meet in shared memory); each keeps its own part
+    // of the normaliser until the end.
+    const int q = (warp >> 2) & 1;
+    const int h = warp >> 3;
     const int wq = warp & 3;
+    const int vw = h * 4 + wq;  // vote slot of this warp within its row tile
     const int r = wq * 32 + lane;
     const int R = row0 + q * kRows + r;
     const int i = R / g;
     const bool row_ok = R < rows;
     const int pos = row_ok ? L - n + i : -1;  // last key this row sees
     const uint32_t lane_base = tmem + q * 256u + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t s_col = lane_base;         // S, then P
-    const uint32_t o_col = lane_base + 128u;  // O
+    const uint32_t s_col = lane_base + 64u * h;         // this half's S, then P
+    const uint32_t o_col = lane_base + 128u + 64u * h;  // this half's O
+    float* half_max = reinterpret_cast<float*>(sm + S::kHalfMax);
+    float* half_sum = reinterpret_cast<float*>(sm + S::kHalfSum);
     const float sl = a.scale_log2;
     const bool pos_scale = sl > 0.f;
-    float m = -INFINITY;  // running max, log2 units
-    float l = 0.f;
+    const float fs = pos_scale ? sl : 1.f;
+    float m = -INFINITY;  // running max, log2 units (the same in both halves)
+    float l = 0.f;        // this half's part of the normaliser
     bool ok = true;
     const int my_tiles = nt[q];
     for (int t = 0; t < my_tiles; ++t) {
       if (!wait_or_abort(s_full(q), t & 1, abort, wait_ns)) { ok = false; break; }
-      tc_fence_after();
-      float x[kKeys];
-      tmem_ld128(s_col, x);
       if (!wait_or_abort(mask_full(t % kMaskSlots), (t / kMaskSlots) & 1, abort, wait_ns)) {
         ok = false;
         break;
       }
+      tc_fence_after();
       const uint64_t vm0 = masks[2 * (t % kMaskSlots)];
       const uint64_t vm1 = masks[2 * (t % kMaskSlots) + 1];
-      const int k0 = t * kKeys;
-      // logits in log2 units are x * sl; with sl > 0 the max commutes with the
-      // scaling and the scaling folds into the exponent's FMA
-      if (!pos_scale) {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) x[c] *= sl;
-      }
-      const float fs = pos_scale ? sl : 1.f;
+      const uint64_t vmh = h ? vm1 : vm0;  // this half's 64 keys
+      const int kh = t * kKeys + 64 * h;   // position of this half's first key
       const bool all_valid = vm0 == ~0ull && vm1 == ~0ull;
-      if (!__all_sync(0xffffffffu, all_valid && k0 + kKeys - 1 <= pos)) {
+      const bool whole = __all_sync(0xffffffffu, vmh == ~0ull && kh + 63 <= pos);
+      // logits in log2 units are x * sl; with sl > 0 the max commutes with the
+      // scaling and the scaling folds into the exponent's FMA. Both passes
+      // read S from TMEM 32 columns at a time and mask it the same way.
+      auto load_chunk = [&](int cc, float (&x)[32]) {
+        tmem_ld32(s_col + 32 * cc, x);
+        if (!pos_scale) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const uint64_t w = c < 64 ? vm0 : vm1;
-          const bool valid = (k0 + c <= pos) && ((w >> (c & 63)) & 1ull);
-          x[c] = valid ? x[c] : -INFINITY;
+          for (int c = 0; c < 32; ++c) x[c] *= sl;
         }
+        if (!whole) {
+          const uint32_t w = static_cast<uint32_t>(vmh >> (32 * cc));
+          const int k0 = kh + 32 * cc;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const bool valid = (k0 + c <= pos) && ((w >> c) & 1u);
+            x[c] = valid ? x[c] : -INFINITY;
+          }
+        }
+      };
+      // ---- pass 1: this half's maximum, then the row's through shared memory
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        float x[32];
+        load_chunk(cc, x);
+        float t11[11];  // 32 -> 11 -> 4 -> 1 with three-input maxima
+#pragma unroll
+        for (int c = 0; c < 10; ++c) t11[c] = max3(x[c], x[c + 10], x[c + 20]);
+        t11[10] = fmaxf(x[30], x[31]);
+        const float t4a = max3(t11[0], t11[1], t11[2]);
+        const float t4b = max3(t11[3], t11[4], t11[5]);
+        const float t4c = max3(t11[6], t11[7], t11[8]);
+        mx = max3(mx, max3(t4a, t4b, t4c), fmaxf(t11[9], t11[10]));
       }
-      float mx;
-      {  // 128 -> 43 -> 15 -> 5 -> 1 with three-input maxima
-        float t43[43];
-#pragma unroll
-        for (int c = 0; c < 42; ++c) t43[c] = max3(x[c], x[c + 42], x[c + 84]);
-        t43[42] = fmaxf(x[126], x[127]);
-        float t15[15];
-#pragma unroll
-        for (int c = 0; c < 14; ++c) t15[c] = max3(t43[c], t43[c + 14], t43[c + 28]);
-        t15[14] = t43[42];
-        float t5[5];
-#pragma unroll
-        for (int c = 0; c < 5; ++c) t5[c] = max3(t15[c], t15[c + 5], t15[c + 10]);
-        mx = max3(max3(t5[0], t5[1], t5[2]), t5[3], t5[4]) * fs;
+      {
+        // slots alternate by tile parity: a half writes tile t + 2's maximum
+        // only after both halves have passed tile t + 1's meeting
+        float* hm = half_max + ((t & 1) * 2 + q) * 2 * kRows;
+        hm[h * kRows + r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mx_bar(q));
+        if (!wait_or_abort(mx_bar(q), t & 1, abort, wait_ns)) { ok = false; break; }
+        mx = fmaxf(mx, hm[(1 - h) * kRows + r]);
       }
+      mx *= fs;
       const bool grow = mx > m + 8.f;
       const float m_new = grow ? mx : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = grow ? exp2f(m - m_use) : 1.f;
+      const float alpha = grow ? fast_exp2(m - m_use) : 1.f;
       // the previous PV of this row tile completed before S was committed
       if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) {
 #pragma unroll 1
-        for (int c = 0; c < kD; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
           float o[32];
           tmem_ld32(o_col + c, o);
 #pragma unroll
@@ -463,62 +503,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       m = m_new;
-      // p = exp2(x * fs - m), in place, summed into eight packed accumulators
-      constexpr int kAcc = 8;
-      uint64_t ps[kAcc];
+      // ---- pass 2: p = exp2(x * fs - m). Each 32-key chunk's P goes over its
+      // own S columns: 16-bit pairs of its high parts in the first 16 columns,
+      // bf16 low parts in the last 16 (written every tile; the MMA warp adds
+      // them when a warp of the row tile voted)
       const uint64_t fs2 = f2(fs, fs);
       const uint64_t nm2 = f2(-m_use, -m_use);
+      uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f pairs
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        float x[32];
+        load_chunk(cc, x);
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 2) {
-        const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
-        x[c] = fast_exp2(e.x);
-        x[c + 1] = fast_exp2(e.y);
-        const uint64_t pp = f2(x[c], x[c + 1]);
-        if (c < 2 * kAcc) ps[c >> 1] = pp;
-        else ps[(c >> 1) % kAcc] = add_f2(ps[(c >> 1) % kAcc], pp);
+        for (int c = 0; c < 32; c += 2) {
+          const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
+          x[c] = fast_exp2(e.x);
+          x[c + 1] = fast_exp2(e.y);
+          ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], f2(x[c], x[c + 1]));
+        }
+        uint32_t hi[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) hi[j] = pack2<IS_BF16>(x[2 * j], x[2 * j + 1]);
+        tmem_st16u(s_col + 32 * cc, hi);
+        if constexpr (IS_BF16) {
+          uint32_t lo[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 hh = unpack2<true>(hi[j]);
+            const float2 d = f2_split(sub_f2(f2(x[2 * j], x[2 * j + 1]), f2(hh.x, hh.y)));
+            lo[j] = pack2<true>(d.x, d.y);
+          }
+          tmem_st16u(s_col + 32 * cc + 16, lo);
+        }
       }
-#pragma unroll
-      for (int w = kAcc / 2; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int c = 0; c < w; ++c) ps[c] = add_f2(ps[c], ps[c + w]);
-      }
+      ps[0] = add_f2(ps[0], ps[1]);
+      ps[2] = add_f2(ps[2], ps[3]);
+      ps[0] = add_f2(ps[0], ps[2]);
       const float2 psum2 = f2_split(ps[0]);
-      const float psum = psum2.x + psum2.y;
+      const float psum = psum2.x + psum2.y;  // this half's share of the tile
       const float l_new = l * alpha + psum;
-      bool split = false;
       if constexpr (IS_BF16) {
         // One vote per warp (votes alternate by tile parity, so a vote for
         // t + 2 is written only after the MMA warp has read the one for t).
-        // The MMA warp runs the low-part pass when any of the four warps voted;
-        // a warp that did not writes zeros there, so its rows add nothing.
-        split = __any_sync(0xffffffffu, psum > kShareLimit * l_new);
-        if (lane == 0) votes[(q * 2 + (t & 1)) * 4 + wq] = split ? 1u : 0u;
+        // A half's own normaliser is at most the row's, so comparing the
+        // half's weight with its own normaliser only splits more often.
+        const bool split = __any_sync(0xffffffffu, psum > kShareLimit * l_new);
+        if (lane == 0) votes[(q * 2 + (t & 1)) * 8 + vw] = split ? 1u : 0u;
       }
       l = l_new;
-      // P over this row tile's S: high parts in columns 0..63 (16-bit pairs);
-      // bf16: low parts (or zeros) in 64..127
-#pragma unroll
-      for (int c = 0; c < kKeys; c += 32) {
-        uint32_t hi[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) hi[j] = pack2<IS_BF16>(x[c + 2 * j], x[c + 2 * j + 1]);
-        tmem_st16u(s_col + c / 2, hi);
-        if constexpr (IS_BF16) {
-          uint32_t lo[16];
-          if (split) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 h = unpack2<true>(hi[j]);
-              const float2 d = f2_split(sub_f2(f2(x[c + 2 * j], x[c + 2 * j + 1]), f2(h.x, h.y)));
-              lo[j] = pack2<true>(d.x, d.y);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) lo[j] = 0u;
-          }
-          tmem_st16u(s_col + 64 + c / 2, lo);
-        }
-      }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       // tokens without valid data: zero their V rows so 0 * garbage never
       // enters O (the slot holds V_t until this tile's PVs have completed;
@@ -530,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t vbase = S::kRing + (iv % kSlots) * S::kItem;
-        for (int idx = r; idx < kKeys * 16; idx += kRows) {
+        for (int idx = h * kRows + r; idx < kKeys * 16; idx += 2 * kRows) {
           const int tok = idx >> 4;
           const int rem = idx & 15;
           const uint64_t w = tok < 64 ? vm0 : vm1;
@@ -544,18 +576,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(q));
     }
+    if (ok && my_tiles > 0) {  // the row's normaliser: both halves' parts
+      half_sum[(q * 2 + h) * kRows + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(l_bar(q));
+      if (wait_or_abort(l_bar(q), 0, abort, wait_ns)) {
+        l += half_sum[(q * 2 + (1 - h)) * kRows + r];
+      } else {
+        ok = false;
+      }
+    }
     if (!ok) {
       if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
     } else if (my_tiles > 0) {
-      // ---- epilogue: O / l once this row tile's last PV has completed
+      // ---- epilogue: this half of O / l once the row tile's last PV has completed
       if (wait_or_abort(o_done(q), 0, abort, wait_ns)) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t ob = row_ok ? ((static_cast<int64_t>(q0) + i) * a.num_q_heads +
-                                     static_cast<int64_t>(kvh) * g + R % g) * kD
+                                     static_cast<int64_t>(kvh) * g + R % g) * kD + 64 * h
                                   : 0;
 #pragma unroll 1
-        for (int c = 0; c < kD; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
           float o[32];
           tmem_ld32(o_col + c, o);
           if (row_ok) {
@@ -572,10 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 uint32_t w[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                  const float lo = o[8 * e + 2 * h] * inv;
-                  const float hi = o[8 * e + 2 * h + 1] * inv;
-                  w[h] = bf ? pack2<true>(lo, hi) : pack2<false>(lo, hi);
+                for (int hh = 0; hh < 4; ++hh) {
+                  const float lo = o[8 * e + 2 * hh] * inv;
+                  const float hi = o[8 * e + 2 * hh + 1] * inv;
+                  w[hh] = bf ? pack2<true>(lo, hi) : pack2<false>(lo, hi);
                 }
                 dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
               }
