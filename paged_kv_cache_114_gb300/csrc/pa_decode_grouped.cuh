@@ -44,42 +44,14 @@ struct GroupedSmem {
   }
 };
 
-// Where a stage of the line sits and which blocks hold it, as the producer's
-// lane k knows it for stage w0 + k of a 32-stage window: the stage's first
-// token t0, its sequence's length, and the block ids of its one or two block
-// pieces (tok_per_op tokens each; -1 where the piece starts past the length).
-// The id of the first piece is read without waiting for the length (it lies
-// inside the table row), so both global loads are in flight together.
-struct StageDesc {
-  int t0, len, b0, b1;
-};
-
-__device__ __forceinline__ StageDesc describe_stage(const DecodeArgs& a, const int32_t* pre, int g,
-                                                    bool live) {
-  StageDesc d{0, 0, -1, -1};
-  if (!live) return d;
-  const Cursor c = cursor_at(a, pre, g);
-  d.t0 = c.j * kStageRows;
-  d.len = c.len;
-  const int64_t row = static_cast<int64_t>(c.s) * a.max_blocks;
-  const int j0 = d.t0 / a.block_size;
-  d.b0 = __ldg(a.block_tables + row + j0);
-  if (a.ops_per_stage > 1 && j0 + 1 < a.max_blocks) {
-    const int b1 = __ldg(a.block_tables + row + j0 + 1);
-    d.b1 = d.t0 + a.tok_per_op < d.len ? b1 : -1;
-  }
-  return d;
-}
-
-// The producer's issue of one stage (tokens [t0, t0 + 16) of a sequence of
-// length tok_end) for KV heads [head0, head0 + hg): one box per block piece
-// and column half, for K and for V, all completing on `bar`. Lane p handles
-// block piece p, whose id (b0 or b1) the caller already read. Stores the
-// valid-row mask to *mask.
+// The producer's issue of one stage (tokens [t0, t0 + 16) of the sequence at
+// table_row, clipped at tok_end) for KV heads [head0, head0 + hg): one box per
+// block piece and column half, for K and for V, all completing on `bar`.
+// Lane j handles the j-th block piece. Stores the valid-row mask to *mask.
 template <int D, bool FP8>
 __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUtensorMap* tmk,
-                                                  const CUtensorMap* tmv, int head0, int hg,
-                                                  int t0, int tok_end, int b0, int b1,
+                                                  const CUtensorMap* tmv, int64_t table_row,
+                                                  int head0, int hg, int t0, int tok_end,
                                                   uint32_t stage, uint32_t half_bytes, uint32_t bar,
                                                   uint32_t* mask, int lane) {
   constexpr int PE = KvLayout<FP8>::kPieceElems;
@@ -91,8 +63,9 @@ __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUt
   if (lane < a.ops_per_stage) {
     const int t = t0 + lane * tpo;
     if (t < tok_end) {
-      off = t % a.block_size;
-      blk = lane == 0 ? b0 : b1;
+      const int j = t / a.block_size;
+      off = t - j * a.block_size;
+      blk = __ldg(a.block_tables + table_row + j);
       ok = blk >= 0 && blk < a.num_blocks;
       if (!ok) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
     }
@@ -186,21 +159,11 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
 
   if (warp == hg) {
     // ------------------------------------------------------------ producer
-    // Stage positions and block ids come from a 32-stage window described
-    // lane-parallel (lane k: stage w0 + k); the next window's loads start as
-    // soon as the current one is in use, so no stage waits on a table read.
-    const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < count ? a.test_stop_stage : count;
-    int w0 = 0;
-    StageDesc cur = describe_stage(a, pre, g0 + lane, lane < stop);
-    StageDesc nxt = describe_stage(a, pre, g0 + 32 + lane, 32 + lane < stop);
+    Cursor ic = cursor_at(a, pre, g0);
     int issued = 0;
+    const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < count ? a.test_stop_stage : count;
     for (; issued < stop; ++issued) {
       const int slot = issued % NS;
-      if (issued - w0 == 32) {
-        w0 += 32;
-        cur = nxt;
-        nxt = describe_stage(a, pre, g0 + w0 + 32 + lane, w0 + 32 + lane < stop);
-      }
       if (issued >= NS) {  // every consumer released this slot's previous stage
         const bool got = mbar_wait_bounded(empty0 + 8 * slot, ((issued / NS) - 1) & 1, kWaitLimitNs);
         if (__any_sync(0xffffffffu, !got)) {
@@ -208,14 +171,10 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
           break;
         }
       }
-      const int k = issued - w0;
-      const int t0 = __shfl_sync(0xffffffffu, cur.t0, k);
-      const int len = __shfl_sync(0xffffffffu, cur.len, k);
-      const int b0 = __shfl_sync(0xffffffffu, cur.b0, k);
-      const int b1 = __shfl_sync(0xffffffffu, cur.b1, k);
-      issue_group_stage<D, FP8>(a, &tmk, &tmv, head0, hg, t0, len, b0, b1,
-                                sm_base + slot * stage_bytes, half_bytes, full0 + 8 * slot,
-                                masks + slot, lane);
+      issue_group_stage<D, FP8>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, head0,
+                                hg, ic.j * tt, ic.len, sm_base + slot * stage_bytes, half_bytes,
+                                full0 + 8 * slot, masks + slot, lane);
+      cursor_next(a, pre, ic);
     }
     // the last stages' copies complete before the producer leaves
     for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)

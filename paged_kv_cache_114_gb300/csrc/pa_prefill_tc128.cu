@@ -26,15 +26,13 @@
 // it. Scores come 128 keys at a time, the N at which an MMA runs at the tensor
 // core's full rate.
 //
-// K and V tiles (32 KB each) stream through a ring of four shared-memory
-// slots in the order K_0, V_0, K_1, V_1, ..., so the next tile loads while
-// the MMAs use the current one. Warp 16 issues the TMA copies (one box of 64
-// head-dim elements x block piece per column half) and publishes each tile's
-// mask of tokens with valid data; warp 17 issues the MMAs from one thread.
-// Sixteen warps run the softmaxes: warp w serves row tile (w / 4) % 2 in TMEM
-// lanes 32 (w % 4) .. and key / output-dim half w / 8, so every SM
-// sub-partition holds two warps of each row tile. The two halves of a row
-// meet once per tile in shared memory to agree on the running maximum.
+// K and V tiles (32 KB each) stream through a ring of five shared-memory
+// slots in the order K_0, V_0, K_1, V_1, ..., so the producer runs two tiles
+// ahead of the MMAs. Warp 8 issues the TMA copies (one box of 64 head-dim
+// elements x block piece per column half) and publishes each tile's mask of
+// tokens with valid data; warp 9 issues the MMAs from one thread; warps 0-3
+// and 4-7 run the two softmaxes (warp w owns TMEM lanes 32 (w % 4) ..), so
+// every SM sub-partition alternates one warp of each.
 //
 // The running maximum rises only when a row's tile maximum passes it by more
 // than 8 (log2 units); the softmax warp then rescales its rows of O in TMEM
@@ -66,12 +64,12 @@ using namespace tc;
 constexpr int kD = 128;        // head dim
 constexpr int kRows = 128;     // query rows per row tile (TMEM lanes)
 constexpr int kKeys = 128;     // tokens per K/V tile
-constexpr int kSlots = 4;      // K/V ring slots (one K or V tile each)
+constexpr int kSlots = 5;      // K/V ring slots (one K or V tile each)
 constexpr int kMaskSlots = 8;  // per-tile valid-token masks in flight
-constexpr int kSoftmaxWarps = 16;  // per row tile: 4 lane groups x 2 column halves
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 18 * 32;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kLimitNs = 2000000000ull;
 constexpr float kShareLimit = 0.125f;  // bf16: split P when a tile's weight passes this share
@@ -84,15 +82,11 @@ struct Smem {
   static constexpr uint32_t kRing = kQ + 2 * kQTile;
   static constexpr uint32_t kBar = kRing + kSlots * kItem;
   // full[kSlots], empty[kSlots], mask_full[kMaskSlots], s_full[2], p_full[2],
-  // o_done[2], fin, mx_bar[2], l_bar[2]
-  static constexpr uint32_t kNumBars = 2 * kSlots + kMaskSlots + 2 + 2 + 2 + 1 + 2 + 2;
+  // o_done[2], fin, q_full
+  static constexpr uint32_t kNumBars = 2 * kSlots + kMaskSlots + 2 + 2 + 2 + 1 + 1;
   static constexpr uint32_t kMask = kBar + kNumBars * 8;        // 2 x uint64 per mask slot
   static constexpr uint32_t kVotes = kMask + kMaskSlots * 16;   // [row tile][parity][warp] u32
-  // half-row maxima [parity][row tile][column half][row], then normalisers
-  // [row tile][column half][row]
-  static constexpr uint32_t kHalfMax = kVotes + 2 * 2 * 8 * 4;
-  static constexpr uint32_t kHalfSum = kHalfMax + 2 * 2 * 2 * kRows * 4;
-  static constexpr uint32_t kMisc = kHalfSum + 2 * 2 * kRows * 4;  // tmem base, abort flag
+  static constexpr uint32_t kMisc = kVotes + 2 * 2 * 4 * 4;     // tmem base, abort flag
   static constexpr uint32_t kTotal = kMisc + 16 + 1024;         // + base-alignment slack
 };
 static_assert(Smem::kTotal <= 232448, "shared memory budget");
@@ -186,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_full = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 2 + q); };
   auto o_done = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 4 + q); };
   const uint32_t fin = bar + 8u * (2 * kSlots + kMaskSlots + 6);
-  auto mx_bar = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 7 + q); };
-  auto l_bar = [&](int q) { return bar + 8u * (2 * kSlots + kMaskSlots + 9 + q); };
+  const uint32_t q_full = bar + 8u * (2 * kSlots + kMaskSlots + 7);  // Q rows in shared memory
   uint64_t* masks = reinterpret_cast<uint64_t*>(sm + S::kMask);
   volatile uint32_t* votes = reinterpret_cast<volatile uint32_t*>(sm + S::kVotes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kMisc);
@@ -201,12 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaskSlots; ++i) mbar_init(mask_full(i), 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(s_full(q), 1);
-      mbar_init(p_full(q), 8);
+      mbar_init(p_full(q), 4);
       mbar_init(o_done(q), 1);
-      mbar_init(mx_bar(q), 8);
-      mbar_init(l_bar(q), 8);
     }
     mbar_init(fin, 1);
+    mbar_init(q_full, kSoftmaxWarps);
     *abort = 0u;
     fence_mbar_init();
   }
@@ -217,79 +209,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  // ---- Q rows into shared memory (K-major, 128-byte swizzle): the two
-  // softmax warps of a lane group take one 64-element half of each row
-  if (warp < kSoftmaxWarps) {
-    const int q = (warp >> 2) & 1;
-    const int h = warp >> 3;
-    const int r = (warp & 3) * 32 + lane;
-    const int R = row0 + q * kRows + r;
-    const uint4* src = nullptr;
-    if (R < rows)
-      src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
-                                           ((static_cast<int64_t>(q0) + R / g) * a.num_q_heads +
-                                            static_cast<int64_t>(kvh) * g + R % g) * kD) + 8 * h;
-    uint4 row[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) row[c] = src != nullptr ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t off = S::kQ + q * S::kQTile + h * S::kHalf + r * 128u + ((c ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(sm + off) = row[c];
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // barriers initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
   // bound of every wait that depends on a K/V tile arriving (the test hook can shorten it)
   const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kLimitNs);
 
+  // ---- Q rows into shared memory (K-major, 128-byte swizzle), one row per
+  // softmax thread, while the producer already streams K and V; the MMA warp
+  // waits on q_full before the first scores
+  if (warp < kSoftmaxWarps) {
+    const int q = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const int R = row0 + q * kRows + r;
+    const uint4* src = nullptr;
+    if (R < rows)
+      src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                           ((static_cast<int64_t>(q0) + R / g) * a.num_q_heads +
+                                            static_cast<int64_t>(kvh) * g + R % g) * kD);
+    uint4 row[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) row[c] = src != nullptr ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint32_t off = S::kQ + q * S::kQTile + (c >> 3) * S::kHalf + r * 128u +
+                           (((c & 7) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + off) = row[c];
+    }
+    fence_proxy_async_smem();  // the MMAs read Q through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_full);
+  }
+
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    const int tpo = a.tok_per_op;  // tokens per box: min(block_size, 64)
+    const int tpo = a.tok_per_op;  // tokens per box: min(block_size, 64), a power of two
+    const int tpo_shift = __ffs(tpo) - 1;
     const int ops = kKeys / tpo;   // boxes per column half of a tile (<= 16)
     const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < ntiles ? a.test_stop_stage : ntiles;
+    // lane j < ops reads the block id of piece j of a tile; the ids of tile
+    // t + 1 are requested while tile t is issued, so no tile waits on them
+    auto read_id = [&](int t) {
+      int id = -1;
+      const int tok = t * kKeys + lane * tpo;
+      if (lane < ops && tok < L) id = __ldg(a.block_tables + table_row + tok / a.block_size);
+      return id;
+    };
+    int blk_next = stop > 0 ? read_id(0) : -1;
     int issued = 0;  // ring items (K or V tiles) issued
     bool ok = true;
     for (int t = 0; ok && t < stop; ++t) {
       const int t0 = t * kKeys;
-      int blk = 0, off = 0;
+      const int blk = blk_next;
+      if (t + 1 < stop) blk_next = read_id(t + 1);
+      int off = 0;
       bool valid = false;
-      if (lane < ops) {
-        const int tok = t0 + lane * tpo;
-        if (tok < L) {
-          const int j = tok / a.block_size;
-          off = tok - j * a.block_size;
-          blk = __ldg(a.block_tables + table_row + j);
-          valid = blk >= 0 && blk < a.num_blocks;
-          if (!valid) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
-        }
+      if (lane < ops && t0 + lane * tpo < L) {
+        off = (t0 + lane * tpo) % a.block_size;
+        valid = blk >= 0 && blk < a.num_blocks;
+        if (!valid) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
       }
       const uint32_t okmask = __ballot_sync(0xffffffffu, valid);
+      // tokens with valid data (a piece with a good block id, below L): lane
+      // i answers for tokens 32k + i, one ballot per k
+      uint32_t mk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int tok = 32 * k + lane;
+        mk[k] = __ballot_sync(0xffffffffu, t0 + tok < L && ((okmask >> (tok >> tpo_shift)) & 1u));
+      }
       if (lane == 0) {
-        // tokens with valid data: whole pieces with a good block id, below L
-        const uint64_t piece = tpo >= 64 ? ~0ull : ((1ull << tpo) - 1ull);
-        uint64_t m[2] = {0ull, 0ull};
-        for (int j = 0; j < ops; ++j) {
-          if (!((okmask >> j) & 1u)) continue;
-          const int first = j * tpo;
-          m[first >> 6] |= piece << (first & 63);
-        }
-        const int valid_tokens = L - t0;  // > 0 for every issued tile
-        if (valid_tokens < 64) {
-          m[0] &= (1ull << valid_tokens) - 1ull;
-          m[1] = 0ull;
-        } else if (valid_tokens < 128) {
-          m[1] &= (1ull << (valid_tokens - 64)) - 1ull;
-        }
         // the slot was last read for tile t - kMaskSlots, whose softmaxes have
-        // finished: issuing tile t - 1 needed V_{t-3} released, after every
-        // softmax of tile t - 3
-        masks[2 * (t % kMaskSlots)] = m[0];
-        masks[2 * (t % kMaskSlots) + 1] = m[1];
+        // finished: the ring holds at most two tiles ahead of the MMAs
+        masks[2 * (t % kMaskSlots)] = static_cast<uint64_t>(mk[0]) | (static_cast<uint64_t>(mk[1]) << 32);
+        masks[2 * (t % kMaskSlots) + 1] =
+            static_cast<uint64_t>(mk[2]) | (static_cast<uint64_t>(mk[3]) << 32);
         mbar_arrive(mask_full(t % kMaskSlots));
       }
 #pragma unroll 1
@@ -354,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     if (lane == 0) {
-      ok = wait_or_abort(full(0), 0, abort, wait_ns);
+      ok = wait_or_abort(q_full, 0, abort, wait_ns) && wait_or_abort(full(0), 0, abort, wait_ns);
       if (ok) {
         tc_fence_after();
         for (int q = 0; q < 2; ++q)
@@ -377,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           bool split = false;
           if constexpr (IS_BF16) {
-            const volatile uint32_t* v = votes + (q * 2 + (t & 1)) * 8;
-            split = (v[0] | v[1] | v[2] | v[3] | v[4] | v[5] | v[6] | v[7]) != 0u;
+            const volatile uint32_t* v = votes + (q * 2 + (t & 1)) * 4;
+            split = (v[0] | v[1] | v[2] | v[3]) != 0u;
           }
           issue_pv(q, t, split);
           if (t + 1 == nt[q]) umma_commit(o_done(q));
@@ -403,30 +399,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
-    // Warp w serves row tile q = (w / 4) % 2, TMEM lanes 32 (w % 4) .. and
-    // column half h = w / 8: keys 64h .. 64h + 63 of each tile and output
-    // dims 64h .. 64h + 63. The two halves of a row share the running maximum
-    // (each tile's half maxima meet in shared memory); each keeps its own part
-    // of the normaliser until the end.
-    const int q = (warp >> 2) & 1;
-    const int h = warp >> 3;
+    const int q = warp >> 2;
     const int wq = warp & 3;
-    const int vw = h * 4 + wq;  // vote slot of this warp within its row tile
     const int r = wq * 32 + lane;
     const int R = row0 + q * kRows + r;
     const int i = R / g;
     const bool row_ok = R < rows;
     const int pos = row_ok ? L - n + i : -1;  // last key this row sees
     const uint32_t lane_base = tmem + q * 256u + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t s_col = lane_base + 64u * h;         // this half's S, then P
-    const uint32_t o_col = lane_base + 128u + 64u * h;  // this half's O
-    float* half_max = reinterpret_cast<float*>(sm + S::kHalfMax);
-    float* half_sum = reinterpret_cast<float*>(sm + S::kHalfSum);
+    const uint32_t s_col = lane_base;         // S, then P
+    const uint32_t o_col = lane_base + 128u;  // O
     const float sl = a.scale_log2;
     const bool pos_scale = sl > 0.f;
-    const float fs = pos_scale ? sl : 1.f;
-    float m = -INFINITY;  // running max, log2 units (the same in both halves)
-    float l = 0.f;        // this half's part of the normaliser
+    float m = -INFINITY;  // running max, log2 units
+    float l = 0.f;
     bool ok = true;
     const int my_tiles = nt[q];
     for (int t = 0; t < my_tiles; ++t) {
@@ -438,53 +424,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint64_t vm0 = masks[2 * (t % kMaskSlots)];
       const uint64_t vm1 = masks[2 * (t % kMaskSlots) + 1];
-      const uint64_t vmh = h ? vm1 : vm0;  // this half's 64 keys
-      const int kh = t * kKeys + 64 * h;   // position of this half's first key
+      const int k0 = t * kKeys;
       const bool all_valid = vm0 == ~0ull && vm1 == ~0ull;
-      const bool whole = __all_sync(0xffffffffu, vmh == ~0ull && kh + 63 <= pos);
+      const bool whole = __all_sync(0xffffffffu, all_valid && k0 + kKeys - 1 <= pos);
       // logits in log2 units are x * sl; with sl > 0 the max commutes with the
       // scaling and the scaling folds into the exponent's FMA. Both passes
-      // read S from TMEM 32 columns at a time and mask it the same way.
-      auto load_chunk = [&](int cc, float (&x)[32]) {
-        tmem_ld32(s_col + 32 * cc, x);
+      // below read S from TMEM, 64 columns at a time, and mask it the same way.
+      const float fs = pos_scale ? sl : 1.f;
+      auto load_half = [&](int h, float (&x)[64]) {
+        tmem_ld64(s_col + 64 * h, x);
         if (!pos_scale) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) x[c] *= sl;
+          for (int c = 0; c < 64; ++c) x[c] *= sl;
         }
         if (!whole) {
-          const uint32_t w = static_cast<uint32_t>(vmh >> (32 * cc));
-          const int k0 = kh + 32 * cc;
+          const uint64_t w = h ? vm1 : vm0;
+          const int kh = k0 + 64 * h;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const bool valid = (k0 + c <= pos) && ((w >> c) & 1u);
+          for (int c = 0; c < 64; ++c) {
+            const bool valid = (kh + c <= pos) && ((w >> c) & 1ull);
             x[c] = valid ? x[c] : -INFINITY;
           }
         }
       };
-      // ---- pass 1: this half's maximum, then the row's through shared memory
+      // ---- pass 1: the tile's row maximum
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        float x[32];
-        load_chunk(cc, x);
-        float t11[11];  // 32 -> 11 -> 4 -> 1 with three-input maxima
+      for (int h = 0; h < 2; ++h) {
+        float x[64];
+        load_half(h, x);
+        float t22[22];  // 64 -> 22 -> 8 -> 3 -> 1 with three-input maxima
 #pragma unroll
-        for (int c = 0; c < 10; ++c) t11[c] = max3(x[c], x[c + 10], x[c + 20]);
-        t11[10] = fmaxf(x[30], x[31]);
-        const float t4a = max3(t11[0], t11[1], t11[2]);
-        const float t4b = max3(t11[3], t11[4], t11[5]);
-        const float t4c = max3(t11[6], t11[7], t11[8]);
-        mx = max3(mx, max3(t4a, t4b, t4c), fmaxf(t11[9], t11[10]));
-      }
-      {
-        // slots alternate by tile parity: a half writes tile t + 2's maximum
-        // only after both halves have passed tile t + 1's meeting
-        float* hm = half_max + ((t & 1) * 2 + q) * 2 * kRows;
-        hm[h * kRows + r] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(mx_bar(q));
-        if (!wait_or_abort(mx_bar(q), t & 1, abort, wait_ns)) { ok = false; break; }
-        mx = fmaxf(mx, hm[(1 - h) * kRows + r]);
+        for (int c = 0; c < 21; ++c) t22[c] = max3(x[c], x[c + 21], x[c + 42]);
+        t22[21] = x[63];
+        float t8[8];
+#pragma unroll
+        for (int c = 0; c < 7; ++c) t8[c] = max3(t22[c], t22[c + 7], t22[c + 14]);
+        t8[7] = t22[21];
+        mx = max3(mx, max3(max3(t8[0], t8[1], t8[2]), max3(t8[3], t8[4], t8[5]), t8[6]), t8[7]);
       }
       mx *= fs;
       const bool grow = mx > m + 8.f;
@@ -494,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the previous PV of this row tile completed before S was committed
       if (t > 0 && __any_sync(0xffffffffu, grow && m != -INFINITY)) {
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kD; c += 32) {
           float o[32];
           tmem_ld32(o_col + c, o);
 #pragma unroll
@@ -504,51 +481,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m = m_new;
       // ---- pass 2: p = exp2(x * fs - m). Each 32-key chunk's P goes over its
-      // own S columns: 16-bit pairs of its high parts in the first 16 columns,
-      // bf16 low parts in the last 16 (written every tile; the MMA warp adds
-      // them when a warp of the row tile voted)
+      // own S columns 32c .. 32c + 31: 16-bit pairs of its high parts in the
+      // first 16, bf16 low parts in the last 16 (written every tile; the MMA
+      // warp adds them when a warp of the row tile voted). In tiles without
+      // masked keys a quarter of the pairs take exp2 on the FMA pipe, so the
+      // special-function unit is not the whole softmax's bound.
       const uint64_t fs2 = f2(fs, fs);
       const uint64_t nm2 = f2(-m_use, -m_use);
       uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f pairs
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        float x[32];
-        load_chunk(cc, x);
+      for (int h = 0; h < 2; ++h) {
+        float x[64];
+        load_half(h, x);
+        if (whole) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
-          x[c] = fast_exp2(e.x);
-          x[c + 1] = fast_exp2(e.y);
-          ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], f2(x[c], x[c + 1]));
-        }
-        uint32_t hi[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) hi[j] = pack2<IS_BF16>(x[2 * j], x[2 * j + 1]);
-        tmem_st16u(s_col + 32 * cc, hi);
-        if constexpr (IS_BF16) {
-          uint32_t lo[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 hh = unpack2<true>(hi[j]);
-            const float2 d = f2_split(sub_f2(f2(x[2 * j], x[2 * j + 1]), f2(hh.x, hh.y)));
-            lo[j] = pack2<true>(d.x, d.y);
+          for (int c = 0; c < 64; c += 2) {
+            const uint64_t e = fma_f2(f2(x[c], x[c + 1]), fs2, nm2);
+            uint64_t pp;
+            if (((c >> 1) & 3) == 3) {
+              pp = exp2_poly_f2(e);
+            } else {
+              const float2 ee = f2_split(e);
+              pp = f2(fast_exp2(ee.x), fast_exp2(ee.y));
+            }
+            const float2 pv = f2_split(pp);
+            x[c] = pv.x;
+            x[c + 1] = pv.y;
+            ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], pp);
           }
-          tmem_st16u(s_col + 32 * cc + 16, lo);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
+            x[c] = fast_exp2(e.x);
+            x[c + 1] = fast_exp2(e.y);
+            ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], f2(x[c], x[c + 1]));
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t hi[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hi[j] = pack2<IS_BF16>(x[32 * cc + 2 * j], x[32 * cc + 2 * j + 1]);
+          const uint32_t col = s_col + 64 * h + 32 * cc;
+          tmem_st16u(col, hi);
+          if constexpr (IS_BF16) {
+            uint32_t lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 hh = unpack2<true>(hi[j]);
+              const float2 d = f2_split(
+                  sub_f2(f2(x[32 * cc + 2 * j], x[32 * cc + 2 * j + 1]), f2(hh.x, hh.y)));
+              lo[j] = pack2<true>(d.x, d.y);
+            }
+            tmem_st16u(col + 16, lo);
+          }
         }
       }
       ps[0] = add_f2(ps[0], ps[1]);
       ps[2] = add_f2(ps[2], ps[3]);
       ps[0] = add_f2(ps[0], ps[2]);
       const float2 psum2 = f2_split(ps[0]);
-      const float psum = psum2.x + psum2.y;  // this half's share of the tile
+      const float psum = psum2.x + psum2.y;
       const float l_new = l * alpha + psum;
       if constexpr (IS_BF16) {
-        // One vote per warp (votes alternate by tile parity, so a vote for
-        // t + 2 is written only after the MMA warp has read the one for t).
-        // A half's own normaliser is at most the row's, so comparing the
-        // half's weight with its own normaliser only splits more often.
+        // one vote per warp (votes alternate by tile parity, so a vote for
+        // t + 2 is written only after the MMA warp has read the one for t)
         const bool split = __any_sync(0xffffffffu, psum > kShareLimit * l_new);
-        if (lane == 0) votes[(q * 2 + (t & 1)) * 8 + vw] = split ? 1u : 0u;
+        if (lane == 0) votes[(q * 2 + (t & 1)) * 4 + wq] = split ? 1u : 0u;
       }
       l = l_new;
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t vbase = S::kRing + (iv % kSlots) * S::kItem;
-        for (int idx = h * kRows + r; idx < kKeys * 16; idx += 2 * kRows) {
+        for (int idx = r; idx < kKeys * 16; idx += kRows) {
           const int tok = idx >> 4;
           const int rem = idx & 15;
           const uint64_t w = tok < 64 ? vm0 : vm1;
@@ -576,28 +576,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(q));
     }
-    if (ok && my_tiles > 0) {  // the row's normaliser: both halves' parts
-      half_sum[(q * 2 + h) * kRows + r] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(l_bar(q));
-      if (wait_or_abort(l_bar(q), 0, abort, wait_ns)) {
-        l += half_sum[(q * 2 + (1 - h)) * kRows + r];
-      } else {
-        ok = false;
-      }
-    }
     if (!ok) {
       if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
     } else if (my_tiles > 0) {
-      // ---- epilogue: this half of O / l once the row tile's last PV has completed
+      // ---- epilogue: O / l once this row tile's last PV has completed
       if (wait_or_abort(o_done(q), 0, abort, wait_ns)) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t ob = row_ok ? ((static_cast<int64_t>(q0) + i) * a.num_q_heads +
-                                     static_cast<int64_t>(kvh) * g + R % g) * kD + 64 * h
+                                     static_cast<int64_t>(kvh) * g + R % g) * kD
                                   : 0;
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kD; c += 32) {
           float o[32];
           tmem_ld32(o_col + c, o);
           if (row_ok) {
@@ -614,10 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 uint32_t w[4];
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                  const float lo = o[8 * e + 2 * hh] * inv;
-                  const float hi = o[8 * e + 2 * hh + 1] * inv;
-                  w[hh] = bf ? pack2<true>(lo, hi) : pack2<false>(lo, hi);
+                for (int h = 0; h < 4; ++h) {
+                  const float lo = o[8 * e + 2 * h] * inv;
+                  const float hi = o[8 * e + 2 * h + 1] * inv;
+                  w[h] = bf ? pack2<true>(lo, hi) : pack2<false>(lo, hi);
                 }
                 dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
               }

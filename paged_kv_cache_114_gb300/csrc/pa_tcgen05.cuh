@@ -109,6 +109,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x for a pair on the FMA pipe, for x in [-126, 8]: x = j + f with j the
+// nearest integer (a float add of 1.5 * 2^23 rounds it) and f in [-1/2, 1/2];
+// 2^f by a degree-5 polynomial fitted here (relative error below 2.4e-7 in
+// fp32), then j added to the exponent field.
+__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x2);
+
 // Packed pairs of fp32 (sm_100 and later): one instruction rounds each half
 // exactly as its scalar form would.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -136,6 +142,29 @@ __device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x2) {
+  const float2 x = f2_split(x2);
+  const float lo = -126.f;
+  const uint64_t xc = f2(fmaxf(x.x, lo), fmaxf(x.y, lo));
+  const uint64_t magic = f2(12582912.f, 12582912.f);  // 1.5 * 2^23
+  const uint64_t t = add_f2(xc, magic);                // round to nearest integer
+  const uint64_t j = sub_f2(t, magic);
+  const uint64_t f = sub_f2(xc, j);                    // in [-1/2, 1/2]
+  uint64_t p = f2(1.327697653323412e-3f, 1.327697653323412e-3f);
+  p = fma_f2(p, f, f2(9.675545617938042e-3f, 9.675545617938042e-3f));
+  p = fma_f2(p, f, f2(5.55071160197258e-2f, 5.55071160197258e-2f));
+  p = fma_f2(p, f, f2(2.4022120237350464e-1f, 2.4022120237350464e-1f));
+  p = fma_f2(p, f, f2(6.931469440460205e-1f, 6.931469440460205e-1f));
+  p = fma_f2(p, f, f2(1.0000001192092896f, 1.0000001192092896f));
+  const float2 tt = f2_split(t);
+  const float2 pp = f2_split(p);
+  // the integer j sits in the low mantissa bits of t
+  const int j0 = __float_as_int(tt.x) - 0x4B400000;
+  const int j1 = __float_as_int(tt.y) - 0x4B400000;
+  return f2(__int_as_float(__float_as_int(pp.x) + (j0 << 23)),
+            __int_as_float(__float_as_int(pp.y) + (j1 << 23)));
+}
+
 // max of three (sm_100 and later)
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
