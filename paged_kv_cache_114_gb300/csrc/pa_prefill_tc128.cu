@@ -15,8 +15,6 @@
 //   S = Q K_t^T      tcgen05.mma M=128 N=128 K=16 (x8), Q and K K-major
 //   P = exp2(S * scale*log2e - m)   online softmax, one row per thread
 //   O += P V_t       tcgen05.mma M=128 N=128 K=16 (x8), P from TMEM, V MN-major
-// Row tile B's first scores are issued one step behind A's, so the two
-// softmaxes alternate instead of running side by side.
 // TMEM: row tile q uses columns 256q .. 256q+127 for S, overwritten in place
 // by P (each 32-column chunk of S holds its 32 keys' P: 16-bit pairs of the
 // high parts, then the bf16 low parts), and 256q+128 .. 256q+255 for O. Each row tile has one S buffer, so the
@@ -353,13 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (lane == 0) {
       ok = wait_or_abort(q_full, 0, abort, wait_ns) && wait_or_abort(full(0), 0, abort, wait_ns);
-      // Row tile B starts one softmax behind A: its first scores are issued
-      // in step 0, after A's first PV, so from then on each row tile's
-      // softmax runs while the tensor core works for the other one.
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        if (nt[1] == 0) umma_commit(empty(0));  // K_0 (otherwise after S(B, 0))
+        for (int q = 0; q < 2; ++q)
+          if (nt[q] > 0) issue_s(q, 0);
+        umma_commit(empty(0));  // K_0
       }
       for (int t = 0; ok && t < ntiles; ++t) {
         const int iv = 2 * t + 1;  // V_t
@@ -367,10 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool v_ready = false, k_ready = false;
         for (int q = 0; q < 2; ++q) {
           if (t >= nt[q]) continue;
-          if (q == 1 && t == 0) {
-            issue_s(1, 0);
-            umma_commit(empty(0));  // K_0: both row tiles' first scores issued
-          }
           if (!v_ready) {
             ok = wait_or_abort(full(iv % kSlots), (iv / kSlots) & 1, abort, wait_ns);
             if (!ok) break;
