@@ -37,11 +37,11 @@
 // The running maximum rises only when a row's tile maximum passes it by more
 // than 8 (log2 units); the softmax warp then rescales its rows of O in TMEM
 // (the previous PV of its tile has completed: S was committed after it).
-// fp16 P carries 11 significant bits and is used whole. bf16 P carries 8: it
-// is stored as a high and a low bf16 part, and the MMA warp adds the low part
-// (O += P_hi V + P_lo V, about 16 bits per weight) when, for some row of the
-// row tile, the tile's weights sum to more than 1/8 of the row's running
-// normaliser; otherwise the high part alone is used. Every weight of an unsplit tile then errs by at most
+// fp16 P carries 11 significant bits and is used whole. bf16 P carries 8: a
+// 64-key half of a tile keeps a low bf16 part as well (O += P_hi V + P_lo V,
+// about 16 bits per weight) when, for some row of the warp, the half's weights
+// sum to more than 1/8 of the row's normaliser so far; otherwise the high part
+// alone is used. Every weight of an unsplit half then errs by at most
 // 2^-9 * 1/8 = 2^-12 of its row's total, the bound of a whole fp16 P.
 //
 // Masking: keys past a row's position get p = 0; V rows of tokens without
@@ -480,44 +480,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       m = m_new;
-      // ---- pass 2: p = exp2(x * fs - m). Each 32-key chunk's P goes over its
-      // own S columns 32c .. 32c + 31: 16-bit pairs of its high parts in the
-      // first 16, bf16 low parts in the last 16 (written every tile; the MMA
-      // warp adds them when a warp of the row tile voted). In tiles without
-      // masked keys a quarter of the pairs take exp2 on the FMA pipe, so the
-      // special-function unit is not the whole softmax's bound.
+      // ---- pass 2: p = exp2(x * fs - m), 64 keys at a time. Each 32-key
+      // chunk's P goes over its own S columns 32c .. 32c + 31: 16-bit pairs of
+      // its high parts in the first 16. bf16: the low parts go in the last 16
+      // when, for some row of the warp, this half's weights pass 1/8 of the
+      // normaliser so far (l * alpha plus the halves done, at most the final
+      // one); otherwise zeros, and those rows use the high parts alone. The
+      // MMA warp runs the low-part pass when any warp of the row tile voted.
       const uint64_t fs2 = f2(fs, fs);
       const uint64_t nm2 = f2(-m_use, -m_use);
-      uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f pairs
+      float l_run = l * alpha;
+      bool voted = false;
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         float x[64];
         load_half(h, x);
-        if (whole) {
+        uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f pairs
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const uint64_t e = fma_f2(f2(x[c], x[c + 1]), fs2, nm2);
-            uint64_t pp;
-            if (((c >> 1) & 3) == 3) {
-              pp = exp2_poly_f2(e);
-            } else {
-              const float2 ee = f2_split(e);
-              pp = f2(fast_exp2(ee.x), fast_exp2(ee.y));
-            }
-            const float2 pv = f2_split(pp);
-            x[c] = pv.x;
-            x[c + 1] = pv.y;
-            ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], pp);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
-            x[c] = fast_exp2(e.x);
-            x[c + 1] = fast_exp2(e.y);
-            ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], f2(x[c], x[c + 1]));
-          }
+        for (int c = 0; c < 64; c += 2) {
+          const float2 e = f2_split(fma_f2(f2(x[c], x[c + 1]), fs2, nm2));
+          x[c] = fast_exp2(e.x);
+          x[c + 1] = fast_exp2(e.y);
+          ps[(c >> 1) & 3] = add_f2(ps[(c >> 1) & 3], f2(x[c], x[c + 1]));
         }
+        ps[0] = add_f2(ps[0], ps[1]);
+        ps[2] = add_f2(ps[2], ps[3]);
+        ps[0] = add_f2(ps[0], ps[2]);
+        const float2 psum2 = f2_split(ps[0]);
+        const float psum = psum2.x + psum2.y;
+        l_run += psum;
+        bool split = false;
+        if constexpr (IS_BF16) split = __any_sync(0xffffffffu, psum > kShareLimit * l_run);
+        voted = voted || split;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t hi[16];
@@ -527,30 +521,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16u(col, hi);
           if constexpr (IS_BF16) {
             uint32_t lo[16];
+            if (split) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 hh = unpack2<true>(hi[j]);
-              const float2 d = f2_split(
-                  sub_f2(f2(x[32 * cc + 2 * j], x[32 * cc + 2 * j + 1]), f2(hh.x, hh.y)));
-              lo[j] = pack2<true>(d.x, d.y);
+              for (int j = 0; j < 16; ++j) {
+                const float2 hh = unpack2<true>(hi[j]);
+                const float2 d = f2_split(
+                    sub_f2(f2(x[32 * cc + 2 * j], x[32 * cc + 2 * j + 1]), f2(hh.x, hh.y)));
+                lo[j] = pack2<true>(d.x, d.y);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) lo[j] = 0u;
             }
             tmem_st16u(col + 16, lo);
           }
         }
       }
-      ps[0] = add_f2(ps[0], ps[1]);
-      ps[2] = add_f2(ps[2], ps[3]);
-      ps[0] = add_f2(ps[0], ps[2]);
-      const float2 psum2 = f2_split(ps[0]);
-      const float psum = psum2.x + psum2.y;
-      const float l_new = l * alpha + psum;
+      // one vote per warp (votes alternate by tile parity, so a vote for t + 2
+      // is written only after the MMA warp has read the one for t)
       if constexpr (IS_BF16) {
-        // one vote per warp (votes alternate by tile parity, so a vote for
-        // t + 2 is written only after the MMA warp has read the one for t)
-        const bool split = __any_sync(0xffffffffu, psum > kShareLimit * l_new);
-        if (lane == 0) votes[(q * 2 + (t & 1)) * 4 + wq] = split ? 1u : 0u;
+        if (lane == 0) votes[(q * 2 + (t & 1)) * 4 + wq] = voted ? 1u : 0u;
       }
-      l = l_new;
+      l = l_run;
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       // tokens without valid data: zero their V rows so 0 * garbage never
       // enters O (the slot holds V_t until this tile's PVs have completed;
