@@ -344,8 +344,9 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
 #define PA_PARTITION_BALANCED (-1)
 
 /* A partition_tokens value for pa_decode chosen from the batch shape and the
- * current device's SM count: 0 (single pass), PA_PARTITION_BALANCED, or a
- * partition size. Returns a negative status (other than -1) on error. */
+ * current device's SM count: 0 (single pass; always for max_seq_len <= 256),
+ * PA_PARTITION_BALANCED, or a partition size. Returns a negative status (other
+ * than -1) on error. */
 int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                                     int32_t block_size);
 

@@ -543,7 +543,11 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
   // once there are many of them per SM; below that, ragged lengths leave SMs
   // idle at the end and the balanced split (equal stage ranges per warp) wins.
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
-  if (units == 0 || max_seq_len <= 16) return 0;
+  // Short contexts: one CTA streams a (sequence, KV head) of at most 16 stages
+  // in about the balanced split's fixed cost (its line prefix, counter memset
+  // and persistent grid; measured on GB300: 4 sequences of up to 33 tokens
+  // decode in 8.5 us single pass, 35.3 us balanced).
+  if (units == 0 || max_seq_len <= 256) return 0;
   const int64_t tt = block_size < pa::kStageRows ? 2LL * block_size : pa::kStageRows;
   const bool balanced_fits = num_seqs <= pa::kMaxBalancedSeqs &&
                              num_kv_heads <= 2LL * di.sms * pa::kDecodeWarps &&
