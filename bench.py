@@ -251,9 +251,11 @@ class Run:
             t.view(src.dtype).copy_(src.view(t.shape))
         with torch.cuda.stream(self.step_obj.stream):
             self.step_obj.staging.copy_(self.step_obj._host_staging)
-        # slot mapping + KV write + decode (+ the reduce of fixed split-K partitions)
-        ws = self.step_obj.workspace
-        self.launches_per_step = 3 + (1 if (ws is not None and partition > 0) else 0)
+        # slot mapping + KV write + the decode's kernels (the reduce of fixed
+        # split-K partitions, the merge of the grouped kernel's cut pieces)
+        kname = pa.decode_kernel_name(w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                      w.max_seq_len, partition)
+        self.launches_per_step = 2 + len(kname.split("+"))
 
     def step(self, ev=None):
         self.step_obj.run(decode_events=ev)

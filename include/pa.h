@@ -247,13 +247,16 @@ int pa_check_copy_pairs(const int64_t* host_pairs, int64_t num_pairs, int64_t nu
  *                  partials a second kernel merges with the rescale identity;
  *                  PA_PARTITION_BALANCED: a persistent grid in which every warp
  *                  streams an equal share of all sequences' 16-token stages;
- *                  a (sequence, KV head) cut between warps is merged by the
- *                  last warp to finish its share (num_seqs <= 2048)
+ *                  a (sequence, KV head) cut between warps is merged by a
+ *                  second kernel on `stream` (head-grouped kernel) or by the
+ *                  last warp to finish its share (per-warp kernel)
+ *                  (num_seqs <= 2048)
  *   workspace      device, >= pa_decode_workspace_bytes(...) bytes; 16-byte
  *                  aligned (256-byte in balanced mode); unused (may be NULL)
  *                  when no sequence needs more than one partition. Its prior
- *                  contents do not matter: balanced mode clears its arrival
- *                  counters (a memset on `stream`) at the start of each call
+ *                  contents do not matter: the per-warp balanced kernel's
+ *                  arrival counters are cleared (a memset on `stream`) at the
+ *                  start of each call
  * Errors (device): L_s outside [0, min(max_seq_len, max_blocks_per_seq*b)]
  * sets PA_DEVERR_SEQ_LEN and is clamped; a table entry out of range sets
  * PA_DEVERR_BLOCK_ID and its tokens are left out.
@@ -352,8 +355,9 @@ int32_t pa_decode_default_partition(int32_t num_seqs, int32_t num_kv_heads, int3
 
 /* Name of the kernel(s) pa_decode launches for this shape and partition_tokens:
  * "decode_kernel" (single pass), "decode_kernel+decode_reduce_kernel" (fixed
- * split with more than one partition), "decode_grouped_kernel" (balanced, one
- * TMA box per stage for a group of KV heads) or "decode_balanced_kernel"
+ * split with more than one partition), "decode_grouped_kernel+
+ * decode_piece_merge_kernel" (balanced, one TMA box per stage for a group of
+ * KV heads, then the merge of cut pieces) or "decode_balanced_kernel"
  * (balanced, per-warp boxes). NULL when pa_decode would reject the shape.
  * Host only: reads no device state. */
 const char* pa_decode_kernel_name(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -387,7 +391,7 @@ const char* pa_decode_kernel_name(int32_t num_q_heads, int32_t num_kv_heads, int
  *     device, do not call the library on that device again.
  *   - Every call shares the one array, which keeps the previous call's
  *     partials. Nothing in it needs to start at zero: each call writes every
- *     partial before reading it, and clears the balanced mode's arrival
+ *     partial before reading it, and clears the per-warp balanced kernel's arrival
  *     counters itself. Calls that overlap on the GPU (other streams, other
  *     threads) race on the array: serialise them.
  * Other arguments, errors and results are those of pa_decode.

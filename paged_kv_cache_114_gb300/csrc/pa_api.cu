@@ -123,9 +123,10 @@ int64_t decode_parts(int32_t max_seq_len, int32_t partition_tokens) {
 
 // Balanced-mode workspace: arrival counters [N][H_kv] (cleared by every call),
 // then kBalancedSlotsPerSm * SMs partial slots of (m, l) and o for the g query
-// heads of a KV head. Both balanced kernels stay within that many slots.
+// heads of a KV head, then kPieceDescPerSm * SMs cut-piece descriptors of the
+// grouped kernel. Both balanced kernels stay within that many slots.
 struct BalancedLayout {
-  size_t ml_offset, o_offset, total;
+  size_t ml_offset, o_offset, desc_offset, total;
 };
 
 BalancedLayout balanced_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -136,7 +137,9 @@ BalancedLayout balanced_layout(int32_t num_seqs, int32_t num_q_heads, int32_t nu
   const size_t counters = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(unsigned int);
   l.ml_offset = (counters + 255) / 256 * 256;
   l.o_offset = l.ml_offset + static_cast<size_t>(slots * g * 2) * sizeof(float);
-  l.total = l.o_offset + static_cast<size_t>(slots * g * head_dim) * sizeof(float);
+  const size_t o_end = l.o_offset + static_cast<size_t>(slots * g * head_dim) * sizeof(float);
+  l.desc_offset = (o_end + 255) / 256 * 256;
+  l.total = l.desc_offset + static_cast<size_t>(pa::kPieceDescPerSm) * sms * sizeof(int4);
   return l;
 }
 
@@ -527,7 +530,8 @@ const char* pa_decode_kernel_name(int32_t num_q_heads, int32_t num_kv_heads, int
   if (partition_tokens == PA_PARTITION_BALANCED) {
     const BalancedPlan plan =
         balanced_plan(num_kv_heads, num_q_heads / num_kv_heads, head_dim, block_size, 1);
-    return plan.kernel == pa::kGroupedRanges ? "decode_grouped_kernel" : "decode_balanced_kernel";
+    return plan.kernel == pa::kGroupedRanges ? "decode_grouped_kernel+decode_piece_merge_kernel"
+                                             : "decode_balanced_kernel";
   }
   if (partition_tokens != 0 && partition_tokens % pa::kStageRows != 0) return nullptr;
   return decode_parts(max_seq_len, partition_tokens) > 1 ? "decode_kernel+decode_reduce_kernel"
@@ -822,6 +826,7 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
     a.counters = reinterpret_cast<unsigned int*>(ws);
     a.part_ml = reinterpret_cast<float*>(ws + lay.ml_offset);
     a.part_o = reinterpret_cast<float*>(ws + lay.o_offset);
+    a.piece_desc = reinterpret_cast<int4*>(ws + lay.desc_offset);
     head_group = plan.head_group;
     kernel = plan.kernel;
     grid = dim3(plan.ctas, 1, 1);
@@ -838,8 +843,9 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   const int tiles = (g + 7) / 8;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (balanced) {
+  if (balanced && !grouped) {
     // arrival counters start each call at zero, whatever the workspace held
+    // (the grouped kernel counts nothing: its merge is a kernel of its own)
     static_assert(pa::kPerWarpRanges == 1, "kernel ids");
     e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(num_seqs) * hkv * sizeof(unsigned int), st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
@@ -864,6 +870,11 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (!balanced && parts > 1) {
     e = pa::launch_decode_reduce(a, D, st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if (grouped) {
+    const int64_t ranges = static_cast<int64_t>(grid.x) / (hkv / head_group);
+    e = pa::launch_decode_piece_merge(a, D, ranges, di.sms, st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

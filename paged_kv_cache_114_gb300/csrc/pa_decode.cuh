@@ -985,8 +985,11 @@ __device__ __forceinline__ void build_line_prefix(const DecodeArgs& a, int32_t* 
 // cut from the line of stot stages. A piece the warp covered whole is
 // normalised and written; otherwise the warp leaves an (m, l, o) partial in
 // slot (range * H_kv + kvh) * 2 + (0: its first piece, 1: its last) and the
-// last contributor to arrive merges the piece.
-template <int D, int NT, bool FP8>
+// last contributor to arrive merges the piece. DEFER: the warp only leaves
+// its partial; decode_piece_merge_kernel merges every cut piece once the
+// stream kernel has finished, so no piece end waits on a fence, an atomic or
+// a merge.
+template <int D, int NT, bool FP8, bool DEFER = false>
 __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& acc, int s, int ps,
                                              int pe, int g0, int g1, int64_t stot, int64_t ranges,
                                              int64_t range, int kvh, int lane) {
@@ -1051,6 +1054,7 @@ __device__ __forceinline__ void finish_piece(const DecodeArgs& a, Acc<D, NT>& ac
         }
       }
     }
+    if constexpr (DEFER) return;
     __threadfence();
     __syncwarp();
     // Contributors: the warps of head kvh in the non-empty ranges ra..rb that

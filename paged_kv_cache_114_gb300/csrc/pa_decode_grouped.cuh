@@ -17,8 +17,15 @@
 // ldmatrix addressing as the per-warp kernels. Consumers release a slot on an
 // "empty" mbarrier (HG arrivals); the producer refills it.
 //
-// Partials, counters and merges are those of the balanced kernel: warp slot
-// (range * H_kv + kv_head), last arriver merges.
+// Partials are those of the balanced kernel (warp slot range * H_kv + kv_head),
+// but a piece end only stores: no fence, no arrival counter, no merge. While
+// HBM is saturated every global round trip waits behind the stream (several
+// microseconds), so those steps cost a warp that is as fast as the stream
+// time it never makes up. Each (range, KV head) also leaves a descriptor of
+// the cut piece that starts in the range, if any: a piece that runs past its
+// range's end is that range's last piece, so one slot per (range, KV head)
+// describes every cut piece exactly once. decode_piece_merge_kernel, launched
+// right after on the same stream as a programmatic dependent, merges them.
 //
 // FP8 caches: a 128-byte line holds 128 head-dim codes, so a box is 128 x 16
 // tokens x HG heads and a stage is half the bytes; the ring has twice the
@@ -122,6 +129,10 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   const uint32_t half_bytes = S::half_bytes(hg);
   const uint32_t stage_bytes = S::stage_bytes(hg);
 
+  // the merge kernel may be scheduled now; it waits for this grid to finish
+  // before it reads a partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sm_base = smem_u32(sm);
   int32_t* pre = reinterpret_cast<int32_t*>(sm + S::prefix_offset(hg));
@@ -145,6 +156,9 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   const int64_t stot = pre[N];
   const int g0 = static_cast<int>(range_start(range, stot, ranges));
   const int g1 = static_cast<int>(range_start(range + 1, stot, ranges));
+  // this range's descriptors say "no cut piece starts here" unless a consumer
+  // warp overwrites its own at its last piece end (after the barrier below)
+  if (threadIdx.x < hg) a.piece_desc[range * hkv + head0 + threadIdx.x] = make_int4(-1, 0, 0, 0);
   if (g0 >= g1) return;
   const int count = g1 - g0;
 
@@ -230,8 +244,16 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
       continue;
     }
     if (aborted) acc.reset();  // contribute nothing, but still take part
-    finish_piece<D, NT, FP8>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, range, kvh,
-                             lane);
+    finish_piece<D, NT, FP8, true>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, range,
+                                   kvh, lane);
+    const int pe = cc.ps + cc.n;
+    if (it == count - 1 && lane == 0 && cc.ps >= g0 && pe > g1) {
+      // the range's last piece starts here and runs on: describe it for the
+      // merge (its partial sits in slot 0 when it is also the first piece)
+      a.piece_desc[range * hkv + kvh] =
+          make_int4(cc.s, static_cast<int>(stage_owner(pe - 1, stot, ranges)), cc.ps == g0 ? 0 : 1,
+                    static_cast<int>(stot));
+    }
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
       load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);

@@ -42,7 +42,217 @@ __global__ void decode_reduce_kernel(const DecodeArgs a, int head_dim) {
   }
 }
 
+constexpr int kMergeThreads = 256;
+constexpr int kMergeLoadRounds = 8;  // descriptor loads in flight per thread
+
+// Merge of the cut pieces decode_grouped_kernel leaves: it stores their
+// partials and, per (range, KV head), a descriptor of the cut piece that
+// starts in that range - {sequence or -1, last range rb, slot of the first
+// partial, stages of the line}. The contributors are the non-empty ranges
+// ra .. rb (ra = the descriptor's range); range r's partial of the piece sits
+// in slot (r * H_kv + kvh) * 2, + 1 for range ra when the piece is not ra's
+// first.
+// Every CTA loads all descriptors (at most 8 per SM) and lists the valid ones
+// in shared memory, in item order, so the (piece, R query rows) tasks can be
+// spread over every warp of the grid: cut pieces cluster in few ranges when
+// sequences are long. A task loads the contributors' (m, l) (lane c holds
+// contributor c) and the first CB contributors' output rows (D / 32 values
+// per lane and row) together, branch-free, before it uses any of them - the
+// weights are not needed to fetch the rows - so a piece of at most CB
+// contributors costs one round trip after the descriptors. Pieces of a few
+// contributors (many pieces): CB = 4 and R = 4 (R = 1 below 4 query heads per
+// KV head); long pieces (few pieces, many contributors): R = 1, CB = 32.
+// Contributors go 32 at a time with the rescale identity between chunks; up
+// to 32 it is the same arithmetic, in the same contributor order, as the
+// last-arriver merge of the other balanced kernels.
+template <int D, int R, int CB>
+__global__ void __launch_bounds__(kMergeThreads, 1)
+    decode_piece_merge_kernel(const DecodeArgs a, int64_t ranges) {
+  constexpr int E = D / 32;
+  constexpr int W = kMergeThreads / 32;
+  extern __shared__ __align__(16) unsigned char merge_smem[];
+  __shared__ int warp_cnt[W];
+  const int hkv = a.num_kv_heads;
+  const int nitems = static_cast<int>(ranges * hkv);
+  int4* sdesc = reinterpret_cast<int4*>(merge_smem);       // [nitems] valid descriptors
+  int* sitem = reinterpret_cast<int*>(sdesc + nitems);     // their items
+  // every partial and descriptor of the stream kernel is visible past this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // ---- the valid descriptors, in item order
+  int nvalid = 0;
+  for (int r0 = 0; r0 < nitems; r0 += kMergeThreads * kMergeLoadRounds) {
+    int4 dv[kMergeLoadRounds];
+#pragma unroll
+    for (int k = 0; k < kMergeLoadRounds; ++k) {
+      const int i = r0 + k * kMergeThreads + static_cast<int>(threadIdx.x);
+      dv[k] = i < nitems ? __ldcg(a.piece_desc + i) : make_int4(-1, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kMergeLoadRounds; ++k) {
+      const int i = r0 + k * kMergeThreads + static_cast<int>(threadIdx.x);
+      const unsigned vm = __ballot_sync(0xffffffffu, dv[k].x >= 0);
+      if (lane == 0) warp_cnt[warp] = __popc(vm);
+      __syncthreads();
+      int before = nvalid;
+      int round = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < W; ++w2) {
+        before += w2 < warp ? warp_cnt[w2] : 0;
+        round += warp_cnt[w2];
+      }
+      if (dv[k].x >= 0) {
+        const int pos = before + __popc(vm & ((1u << lane) - 1u));
+        sdesc[pos] = dv[k];
+        sitem[pos] = i;
+      }
+      nvalid += round;
+      __syncthreads();  // warp_cnt is rewritten next round
+    }
+  }
+
+  // ---- tasks (valid piece, R rows), spread over all warps of the grid
+  const int g = a.group;
+  const int rgroups = (g + R - 1) / R;
+  const int ntasks = nvalid * rgroups;
+  for (int t = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x); t < ntasks;
+       t += static_cast<int>(gridDim.x) * W) {
+    const int4 d = sdesc[t / rgroups];
+    const int item = sitem[t / rgroups];
+    const int j0 = (t % rgroups) * R;
+    const int64_t ra = item / hkv;
+    const int kvh = item - static_cast<int>(ra) * hkv;
+    const int64_t stot = d.w;
+    const int span = static_cast<int>(d.y - ra + 1);
+    const int64_t first = (ra * hkv + kvh) * 2 + d.z;  // range ra's partial of the piece
+    float M[R];
+    float L[R];
+    float acc[R][E];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      M[r] = -INFINITY;
+      L[r] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+    }
+    for (int c0 = 0; c0 < span; c0 += 32) {
+      const int64_t rr = ra + c0 + lane;
+      int sid = -1;
+      if (c0 + lane < span && range_start(rr, stot, ranges) < range_start(rr + 1, stot, ranges))
+        sid = static_cast<int>((rr * hkv + kvh) * 2 + (c0 + lane == 0 ? d.z : 0));
+      // Loads are branch-free so that all of them are in flight together: a
+      // contributor or row without a partial reads the first contributor's
+      // row j0 (this task's own data, always written), and its weight 0
+      // selects the value away.
+      float2 ml[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const bool use = sid >= 0 && j0 + r < g;
+        ml[r] = __ldcg(reinterpret_cast<const float2*>(a.part_ml) +
+                       (use ? static_cast<int64_t>(sid) * g + j0 + r : first * g + j0));
+      }
+      const int nch = span - c0 < 32 ? span - c0 : 32;
+      float w[R];
+      for (int b0 = 0; b0 < nch; b0 += CB) {
+        float v[CB][R][E];
+#pragma unroll
+        for (int c = 0; c < CB; ++c) {
+          const int sc = __shfl_sync(0xffffffffu, sid, (b0 + c) & 31);
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const bool use = b0 + c < nch && sc >= 0 && j0 + r < g;
+            ldcg_vec<E>(a.part_o + (use ? static_cast<int64_t>(sc) * g + j0 + r : first * g + j0) * D +
+                            lane * E,
+                        v[c][r]);
+          }
+        }
+        if (b0 == 0) {  // the chunk's weights, while its rows are in flight
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const bool use = sid >= 0 && j0 + r < g;
+            const float m = use ? ml[r].x : -INFINITY;
+            ml[r].y = use ? ml[r].y : 0.f;
+            const float mnew = fmaxf(M[r], warp_max(m));
+            // what earlier chunks summed, rescaled to the new maximum (0 when
+            // nothing came before; a row with no logit yet keeps zeros)
+            const float alpha = M[r] == -INFINITY ? 0.f : exp2f(M[r] - mnew);
+            w[r] = m == -INFINITY ? 0.f : exp2f(m - mnew);
+            L[r] = L[r] * alpha + warp_sum(w[r] * ml[r].y);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[r][e] *= alpha;
+            M[r] = mnew;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < CB; ++c) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float wc = __shfl_sync(0xffffffffu, w[r], (b0 + c) & 31);
+            if (b0 + c < nch) {
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc[r][e] += wc != 0.f ? v[c][r][e] * wc : 0.f;
+            }
+          }
+        }
+      }
+    }
+    const int64_t row0 = static_cast<int64_t>(d.x) * a.num_q_heads + static_cast<int64_t>(kvh) * g + j0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (j0 + r >= g) break;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        store_out(a, (row0 + r) * D + lane * E + e, L[r] > 0.f ? acc[r][e] / L[r] : 0.f);
+    }
+  }
+}
+
+template <int D, int R, int CB>
+cudaError_t launch_merge(const DecodeArgs& a, int64_t ranges, int sms, cudaStream_t st) {
+  const int64_t nitems = ranges * a.num_kv_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms), 1, 1);  // one CTA per SM
+  cfg.blockDim = dim3(kMergeThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(nitems) * (sizeof(int4) + sizeof(int));
+  cfg.stream = st;
+  // a programmatic dependent of the stream kernel: it is scheduled while that
+  // kernel runs and waits for it in griddepcontrol.wait
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  auto kern = decode_piece_merge_kernel<D, R, CB>;
+  if (cfg.dynamicSmemBytes > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(cfg.dynamicSmemBytes));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, a, ranges);
+}
+
+template <int D>
+cudaError_t launch_merge_for(const DecodeArgs& a, int64_t ranges, int sms, cudaStream_t st) {
+  constexpr int E = D / 32;
+  // a piece spans about ranges / N + 1 ranges when the lengths are alike
+  if (ranges >= 4LL * a.num_seqs) return launch_merge<D, 1, (E > 4 ? 16 : 32)>(a, ranges, sms, st);
+  if (a.group < 4) return launch_merge<D, 1, (E > 4 ? 2 : 4)>(a, ranges, sms, st);
+  return launch_merge<D, 4, (E > 4 ? 2 : 4)>(a, ranges, sms, st);
+}
+
 }  // namespace
+
+cudaError_t launch_decode_piece_merge(const DecodeArgs& a, int head_dim, int64_t ranges,
+                                      int sms, cudaStream_t st) {
+  switch (head_dim) {
+    case 64: return launch_merge_for<64>(a, ranges, sms, st);
+    case 128: return launch_merge_for<128>(a, ranges, sms, st);
+    case 256: return launch_merge_for<256>(a, ranges, sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st) {
   const unsigned blocks = static_cast<unsigned>(static_cast<int64_t>(a.num_seqs) * a.num_q_heads);

@@ -78,9 +78,9 @@ def test_decode_kernel_name(lib):
         r = lib.pa_decode_kernel_name(*a)
         return None if r is None else r.decode()
     # balanced: grouped boxes need b >= 8 and 4 | H_kv; otherwise per-warp boxes
-    assert name(32, 32, 128, 16, 2048, -1) == "decode_grouped_kernel"
-    assert name(64, 8, 128, 16, 8192, -1) == "decode_grouped_kernel"
-    assert name(32, 8, 128, 8, 32768, -1) == "decode_grouped_kernel"
+    assert name(32, 32, 128, 16, 2048, -1) == "decode_grouped_kernel+decode_piece_merge_kernel"
+    assert name(64, 8, 128, 16, 8192, -1) == "decode_grouped_kernel+decode_piece_merge_kernel"
+    assert name(32, 8, 128, 8, 32768, -1) == "decode_grouped_kernel+decode_piece_merge_kernel"
     assert name(4, 4, 64, 4, 33, -1) == "decode_balanced_kernel"
     assert name(6, 6, 128, 16, 100, -1) == "decode_balanced_kernel"
     # fixed split: a reduce only when there is more than one partition
