@@ -123,10 +123,9 @@ int64_t decode_parts(int32_t max_seq_len, int32_t partition_tokens) {
 
 // Balanced-mode workspace: arrival counters [N][H_kv] (cleared by every call),
 // then kBalancedSlotsPerSm * SMs partial slots of (m, l) and o for the g query
-// heads of a KV head, then kPieceDescPerSm * SMs cut-piece descriptors of the
-// grouped kernel. Both balanced kernels stay within that many slots.
+// heads of a KV head. Both balanced kernels stay within that many slots.
 struct BalancedLayout {
-  size_t ml_offset, o_offset, desc_offset, total;
+  size_t ml_offset, o_offset, total;
 };
 
 BalancedLayout balanced_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -137,9 +136,7 @@ BalancedLayout balanced_layout(int32_t num_seqs, int32_t num_q_heads, int32_t nu
   const size_t counters = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(unsigned int);
   l.ml_offset = (counters + 255) / 256 * 256;
   l.o_offset = l.ml_offset + static_cast<size_t>(slots * g * 2) * sizeof(float);
-  const size_t o_end = l.o_offset + static_cast<size_t>(slots * g * head_dim) * sizeof(float);
-  l.desc_offset = (o_end + 255) / 256 * 256;
-  l.total = l.desc_offset + static_cast<size_t>(pa::kPieceDescPerSm) * sms * sizeof(int4);
+  l.total = l.o_offset + static_cast<size_t>(slots * g * head_dim) * sizeof(float);
   return l;
 }
 
@@ -826,7 +823,6 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
     a.counters = reinterpret_cast<unsigned int*>(ws);
     a.part_ml = reinterpret_cast<float*>(ws + lay.ml_offset);
     a.part_o = reinterpret_cast<float*>(ws + lay.o_offset);
-    a.piece_desc = reinterpret_cast<int4*>(ws + lay.desc_offset);
     head_group = plan.head_group;
     kernel = plan.kernel;
     grid = dim3(plan.ctas, 1, 1);

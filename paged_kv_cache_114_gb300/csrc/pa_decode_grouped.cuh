@@ -21,11 +21,8 @@
 // but a piece end only stores: no fence, no arrival counter, no merge. While
 // HBM is saturated every global round trip waits behind the stream (several
 // microseconds), so those steps cost a warp that is as fast as the stream
-// time it never makes up. Each (range, KV head) also leaves a descriptor of
-// the cut piece that starts in the range, if any: a piece that runs past its
-// range's end is that range's last piece, so one slot per (range, KV head)
-// describes every cut piece exactly once. decode_piece_merge_kernel, launched
-// right after on the same stream as a programmatic dependent, merges them.
+// time it never makes up. decode_piece_merge_kernel, launched right after on
+// the same stream as a programmatic dependent, merges every cut piece.
 //
 // FP8 caches: a 128-byte line holds 128 head-dim codes, so a box is 128 x 16
 // tokens x HG heads and a stage is half the bytes; the ring has twice the
@@ -156,9 +153,6 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   const int64_t stot = pre[N];
   const int g0 = static_cast<int>(range_start(range, stot, ranges));
   const int g1 = static_cast<int>(range_start(range + 1, stot, ranges));
-  // this range's descriptors say "no cut piece starts here" unless a consumer
-  // warp overwrites its own at its last piece end (after the barrier below)
-  if (threadIdx.x < hg) a.piece_desc[range * hkv + head0 + threadIdx.x] = make_int4(-1, 0, 0, 0);
   if (g0 >= g1) return;
   const int count = g1 - g0;
 
@@ -230,8 +224,10 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
     if (!aborted) {
       sv.k = sm_base + slot * stage_bytes;
       sv.v = sv.k + HALVES * half_bytes;
-      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8>(sv, sm_base, sm, masks[slot], qb, acc, ls,
-                                                  lane);
+      // E4M3: lazy maximum, and a warp vote skips its reduction on the
+      // stages where no logit passes it by more than 8 (most of them)
+      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8, GroupView<HG, TPO>, NoColLimit, FP8, false, FP8>(
+          sv, sm_base, sm, masks[slot], qb, acc, ls, lane);
       static_assert(GroupView<HG, TPO>::half_stride == S::half_bytes(HG), "layout");
       fence_proxy_async_smem();
       __syncwarp();
@@ -246,14 +242,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
     if (aborted) acc.reset();  // contribute nothing, but still take part
     finish_piece<D, NT, FP8, true>(a, acc, cc.s, cc.ps, cc.ps + cc.n, g0, g1, stot, ranges, range,
                                    kvh, lane);
-    const int pe = cc.ps + cc.n;
-    if (it == count - 1 && lane == 0 && cc.ps >= g0 && pe > g1) {
-      // the range's last piece starts here and runs on: describe it for the
-      // merge (its partial sits in slot 0 when it is also the first piece)
-      a.piece_desc[range * hkv + kvh] =
-          make_int4(cc.s, static_cast<int>(stage_owner(pe - 1, stot, ranges)), cc.ps == g0 ? 0 : 1,
-                    static_cast<int>(stot));
-    }
+
     if (it + 1 < count) {
       cursor_next(a, pre, cc);
       load_q<IS_BF16, D, NT, FP8>(a, cc.s, kvh, lane, qb, ls);

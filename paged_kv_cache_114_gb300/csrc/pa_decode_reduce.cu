@@ -43,88 +43,114 @@ __global__ void decode_reduce_kernel(const DecodeArgs a, int head_dim) {
 }
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeLoadRounds = 8;  // descriptor loads in flight per thread
+constexpr int kMergeRangeRuns = 8;  // ranges one thread examines per pass
 
-// Merge of the cut pieces decode_grouped_kernel leaves: it stores their
-// partials and, per (range, KV head), a descriptor of the cut piece that
-// starts in that range - {sequence or -1, last range rb, slot of the first
-// partial, stages of the line}. The contributors are the non-empty ranges
-// ra .. rb (ra = the descriptor's range); range r's partial of the piece sits
-// in slot (r * H_kv + kvh) * 2, + 1 for range ra when the piece is not ra's
-// first.
-// Every CTA loads all descriptors (at most 8 per SM) and lists the valid ones
-// in shared memory, in item order, so the (piece, R query rows) tasks can be
-// spread over every warp of the grid: cut pieces cluster in few ranges when
-// sequences are long. A task loads the contributors' (m, l) (lane c holds
-// contributor c) and the first CB contributors' output rows (D / 32 values
-// per lane and row) together, branch-free, before it uses any of them - the
-// weights are not needed to fetch the rows - so a piece of at most CB
-// contributors costs one round trip after the descriptors. Pieces of a few
-// contributors (many pieces): CB = 4 and R = 4 (R = 1 below 4 query heads per
-// KV head); long pieces (few pieces, many contributors): R = 1, CB = 32.
-// Contributors go 32 at a time with the rescale identity between chunks; up
-// to 32 it is the same arithmetic, in the same contributor order, as the
-// last-arriver merge of the other balanced kernels.
+// Merge of the cut pieces decode_grouped_kernel leaves as partials. The
+// equal-range split of the stage line follows from the lengths alone, so the
+// kernel finds the cut pieces before griddepcontrol.wait, while the stream
+// kernel's last CTAs still run: it builds the stage prefix, and for each
+// range r takes its last piece - the sequence s holding stage g1(r) - 1. That
+// piece is cut and starts in r when pre[s] >= g0(r) and pre[s + 1] > g1(r);
+// every cut piece is the last piece of the range it starts in, so this lists
+// each exactly once (the same for every KV head). Its contributors are the
+// non-empty ranges r .. rb, rb the owner of its last stage; range r'
+// holds its partial in slot (r' * H_kv + kvh) * 2, + 1 for r itself when the
+// piece does not start r (then it is r's last piece, not its first).
+// Past the wait the (piece, KV head, R query rows) tasks are spread over every
+// warp of the grid - cut pieces cluster in few ranges when sequences are
+// long. A task loads the contributors' (m, l) (lane c holds contributor c)
+// and the first CB contributors' output rows (D / 32 values per lane and row)
+// together, branch-free, before it uses any of them - the weights are not
+// needed to fetch the rows - so a piece of at most CB contributors costs one
+// round trip. Pieces of a few contributors (many pieces): CB = 4 and R = 4
+// (R = 1 below 4 query heads per KV head); long pieces (few pieces, many
+// contributors): R = 1, CB = 32. Contributors go 32 at a time with the
+// rescale identity between chunks; up to 32 it is the same arithmetic, in the
+// same contributor order, as the last-arriver merge of the other balanced
+// kernels.
 template <int D, int R, int CB>
 __global__ void __launch_bounds__(kMergeThreads, 1)
     decode_piece_merge_kernel(const DecodeArgs a, int64_t ranges) {
   constexpr int E = D / 32;
   constexpr int W = kMergeThreads / 32;
   extern __shared__ __align__(16) unsigned char merge_smem[];
-  __shared__ int warp_cnt[W];
-  const int hkv = a.num_kv_heads;
-  const int nitems = static_cast<int>(ranges * hkv);
-  int4* sdesc = reinterpret_cast<int4*>(merge_smem);       // [nitems] valid descriptors
-  int* sitem = reinterpret_cast<int*>(sdesc + nitems);     // their items
-  // every partial and descriptor of the stream kernel is visible past this
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
+  __shared__ int warp_tot[16];
+  const int N = a.num_seqs;
+  int32_t* pre = reinterpret_cast<int32_t*>(merge_smem);                    // [N + 1]
+  int4* cut = reinterpret_cast<int4*>(merge_smem + ((N + 1) * 4 + 15) / 16 * 16);  // [ranges]
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // ---- the valid descriptors, in item order
-  int nvalid = 0;
-  for (int r0 = 0; r0 < nitems; r0 += kMergeThreads * kMergeLoadRounds) {
-    int4 dv[kMergeLoadRounds];
+
+  // ---- before the wait: the cut pieces, from the lengths alone
+  build_line_prefix(a, pre, kStageRows, warp_tot, W);
+  const int64_t stot = pre[N];
+  int ncut = 0;
+  for (int64_t r0 = 0; r0 < ranges; r0 += static_cast<int64_t>(kMergeThreads) * kMergeRangeRuns) {
+    const int64_t left = ranges - r0;
+    const int n = left < kMergeThreads * kMergeRangeRuns ? static_cast<int>(left)
+                                                         : kMergeThreads * kMergeRangeRuns;
+    const int run = (n + kMergeThreads - 1) / kMergeThreads;
+    const int64_t i0 = r0 + static_cast<int64_t>(threadIdx.x) * run;
+    int4 cv[kMergeRangeRuns];
+    int mine = 0;
 #pragma unroll
-    for (int k = 0; k < kMergeLoadRounds; ++k) {
-      const int i = r0 + k * kMergeThreads + static_cast<int>(threadIdx.x);
-      dv[k] = i < nitems ? __ldcg(a.piece_desc + i) : make_int4(-1, 0, 0, 0);
+    for (int k = 0; k < kMergeRangeRuns; ++k) {
+      cv[k] = make_int4(-1, 0, 0, 0);
+      const int64_t r = i0 + k;
+      if (k < run && r < r0 + n) {
+        const int64_t g0 = range_start(r, stot, ranges);
+        const int64_t g1 = range_start(r + 1, stot, ranges);
+        if (g0 < g1) {
+          int lo = 0;
+          int hi = N - 1;  // the sequence holding stage g1 - 1
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= g1 - 1) lo = mid; else hi = mid - 1;
+          }
+          if (pre[lo] >= g0 && pre[lo + 1] > g1)
+            cv[k] = make_int4(lo, static_cast<int>(stage_owner(pre[lo + 1] - 1, stot, ranges)),
+                              pre[lo] == g0 ? 0 : 1, static_cast<int>(r));
+        }
+      }
+      mine += cv[k].x >= 0 ? 1 : 0;
+    }
+    int incl = mine;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int pos = ncut + incl - mine;
+    int total = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < W; ++w2) {
+      pos += w2 < warp ? warp_tot[w2] : 0;
+      total += warp_tot[w2];
     }
 #pragma unroll
-    for (int k = 0; k < kMergeLoadRounds; ++k) {
-      const int i = r0 + k * kMergeThreads + static_cast<int>(threadIdx.x);
-      const unsigned vm = __ballot_sync(0xffffffffu, dv[k].x >= 0);
-      if (lane == 0) warp_cnt[warp] = __popc(vm);
-      __syncthreads();
-      int before = nvalid;
-      int round = 0;
-#pragma unroll
-      for (int w2 = 0; w2 < W; ++w2) {
-        before += w2 < warp ? warp_cnt[w2] : 0;
-        round += warp_cnt[w2];
-      }
-      if (dv[k].x >= 0) {
-        const int pos = before + __popc(vm & ((1u << lane) - 1u));
-        sdesc[pos] = dv[k];
-        sitem[pos] = i;
-      }
-      nvalid += round;
-      __syncthreads();  // warp_cnt is rewritten next round
-    }
+    for (int k = 0; k < kMergeRangeRuns; ++k)
+      if (cv[k].x >= 0) cut[pos++] = cv[k];
+    ncut += total;
+    __syncthreads();  // the list is complete; warp_tot is rewritten next pass
   }
 
+  // every partial of the stream kernel is written and visible past this point
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // ---- tasks (valid piece, R rows), spread over all warps of the grid
+  const int hkv = a.num_kv_heads;
   const int g = a.group;
   const int rgroups = (g + R - 1) / R;
-  const int ntasks = nvalid * rgroups;
+  const int ntasks = ncut * hkv * rgroups;
   for (int t = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x); t < ntasks;
        t += static_cast<int>(gridDim.x) * W) {
-    const int4 d = sdesc[t / rgroups];
-    const int item = sitem[t / rgroups];
-    const int j0 = (t % rgroups) * R;
-    const int64_t ra = item / hkv;
-    const int kvh = item - static_cast<int>(ra) * hkv;
-    const int64_t stot = d.w;
+    const int4 d = cut[t / (hkv * rgroups)];  // {sequence, last range, slot bit, first range}
+    const int rest = t - (t / (hkv * rgroups)) * (hkv * rgroups);
+    const int kvh = rest / rgroups;
+    const int j0 = (rest - kvh * rgroups) * R;
+    const int64_t ra = d.w;
     const int span = static_cast<int>(d.y - ra + 1);
     const int64_t first = (ra * hkv + kvh) * 2 + d.z;  // range ra's partial of the piece
     float M[R];
@@ -211,11 +237,11 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
 
 template <int D, int R, int CB>
 cudaError_t launch_merge(const DecodeArgs& a, int64_t ranges, int sms, cudaStream_t st) {
-  const int64_t nitems = ranges * a.num_kv_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms), 1, 1);  // one CTA per SM
   cfg.blockDim = dim3(kMergeThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(nitems) * (sizeof(int4) + sizeof(int));
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.num_seqs + 1 + 3) / 4 * 16 +
+                         static_cast<size_t>(ranges) * sizeof(int4);
   cfg.stream = st;
   // a programmatic dependent of the stream kernel: it is scheduled while that
   // kernel runs and waits for it in griddepcontrol.wait

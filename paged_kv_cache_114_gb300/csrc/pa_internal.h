@@ -18,10 +18,6 @@ struct DecodeArgs {
   float* part_o;                 // [N][Hq][max_parts][D]   (split-K only)
   float* part_ml;                // [N][Hq][max_parts][2]   (max in log2 units, normaliser)
   unsigned int* counters;        // balanced mode: [N][H_kv] arrival counters, cleared by each call
-  // Head-grouped balanced mode: per (range, KV head) the cut piece that starts
-  // in that range, {sequence or -1, last range, slot of the first partial
-  // (0 or 1), stages of the whole line}; decode_piece_merge_kernel reads them.
-  int4* piece_desc;              // [ranges][H_kv]
   const int32_t* block_tables;   // [N][max_blocks]
   const int32_t* seq_lens;       // [N]
   int* err;                      // device error word
@@ -153,14 +149,10 @@ cudaError_t launch_prefill_tc_e4m3(const CUtensorMap& tk, const CUtensorMap& tv,
 // Merges split-K partials into out (pa_decode_reduce.cu).
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);
 // Merges the cut pieces decode_grouped_kernel left as partials (it stores them
-// and their descriptors without a merge); `ranges` is that launch's range
-// count. Launched right after it on the same stream, as a programmatic
-// dependent.
+// without a merge); `ranges` is that launch's range count. Launched right
+// after it on the same stream, as a programmatic dependent.
 cudaError_t launch_decode_piece_merge(const DecodeArgs& a, int head_dim, int64_t ranges, int sms,
                                       cudaStream_t st);
-// Descriptors the grouped kernel may write: ranges x H_kv <= 8 per SM (its
-// CTAs x head group, 8 / HG CTAs of HG heads per SM).
-constexpr int kPieceDescPerSm = 8;
 
 // Cache operations (pa_cache_ops.cu).
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
