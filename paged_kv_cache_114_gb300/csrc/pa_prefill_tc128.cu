@@ -209,18 +209,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  tc_fence_before();
-  __syncthreads();  // barriers initialised, TMEM allocated
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
-  // bound of every wait that depends on a K/V tile arriving (the test hook can shorten it)
-  const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kLimitNs);
-
-  // ---- Q rows into shared memory (K-major, 128-byte swizzle), one row per
-  // softmax thread, while the producer already streams K and V; the MMA warp
-  // waits on q_full before the first scores
+  const int tpo = a.tok_per_op;  // tokens per box: min(block_size, 64), a power of two
+  const int ops = kKeys / tpo;   // boxes per column half of a tile (<= 16)
+  // The first global reads go out before the start-up barrier, so that their
+  // latency overlaps the barrier set-up and the TMEM allocation: each softmax
+  // thread's Q row, and the producer's block ids of tile 0.
+  int id0 = -1;
+  if (warp == kProducerWarp && lane < ops && lane * tpo < L)
+    id0 = __ldg(a.block_tables + table_row + (lane * tpo) / a.block_size);
   if (warp < kSoftmaxWarps) {
+    // Q rows into shared memory (K-major, 128-byte swizzle), one row per
+    // softmax thread; the MMA warp waits on q_full before the first scores
     const int q = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const int R = row0 + q * kRows + r;
@@ -239,15 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(sm + off) = row[c];
     }
     fence_proxy_async_smem();  // the MMAs read Q through the async proxy
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_full);
   }
+
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, TMEM allocated, Q rows stored
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // bound of every wait that depends on a K/V tile arriving (the test hook can shorten it)
+  const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kLimitNs);
+  if (warp < kSoftmaxWarps && lane == 0) mbar_arrive(q_full);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    const int tpo = a.tok_per_op;  // tokens per box: min(block_size, 64), a power of two
     const int tpo_shift = __ffs(tpo) - 1;
-    const int ops = kKeys / tpo;   // boxes per column half of a tile (<= 16)
     const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < ntiles ? a.test_stop_stage : ntiles;
     // lane j < ops reads the block id of piece j of a tile; the ids of tile
     // t + 1 are requested while tile t is issued, so no tile waits on them
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < ops && tok < L) id = __ldg(a.block_tables + table_row + tok / a.block_size);
       return id;
     };
-    int blk_next = stop > 0 ? read_id(0) : -1;
+    int blk_next = stop > 0 ? id0 : -1;  // tile 0's ids, read before the start-up barrier
     int issued = 0;  // ring items (K or V tiles) issued
     bool ok = true;
     for (int t = 0; ok && t < stop; ++t) {
