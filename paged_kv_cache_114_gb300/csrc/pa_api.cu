@@ -870,7 +870,7 @@ int pa_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const pa_cac
   }
   if (grouped) {
     const int64_t ranges = static_cast<int64_t>(grid.x) / (hkv / head_group);
-    e = pa::launch_decode_piece_merge(a, D, ranges, di.sms, st);
+    e = pa::launch_decode_piece_merge(a, D, ranges, pa::grouped_line_tokens(fp8), di.sms, st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

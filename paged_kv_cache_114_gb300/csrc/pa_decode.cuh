@@ -444,12 +444,13 @@ __device__ __forceinline__ WarpView warp_stage_view(uint32_t stage, int halves) 
   return WarpView{stage, stage + halves * WarpView::half_stride};
 }
 
-// Head-grouped stage (box of 64 x TPO tokens x HG heads per column half):
-// per token group, HG heads of TPO lines each; this head's lines at head_off.
-template <int HG, int TPO>
+// Head-grouped stage of ST token rows (box of 64 x TPO tokens x HG heads per
+// column half): per token group, HG heads of TPO lines each; this head's lines
+// at head_off.
+template <int HG, int TPO, int ST = kStageRows>
 struct GroupView {
   uint32_t k, v, head_off;
-  static constexpr uint32_t half_stride = HG * kStageRows * 128u;
+  static constexpr uint32_t half_stride = HG * ST * 128u;
   static constexpr uint32_t op_stride = HG * TPO * 128u;
   __device__ __forceinline__ uint32_t row(int r) const {
     return static_cast<uint32_t>(r / TPO) * op_stride + head_off + static_cast<uint32_t>(r % TPO) * 128u;

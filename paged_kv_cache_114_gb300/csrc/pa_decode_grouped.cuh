@@ -33,11 +33,12 @@
 
 namespace pa {
 
-// Shared-memory plan of the grouped kernel for head group HG (runtime).
-template <int D, int NS, bool FP8>
+// Shared-memory plan of the grouped kernel for head group HG (runtime) and
+// stages of ST token rows.
+template <int D, int NS, bool FP8, int ST = kStageRows>
 struct GroupedSmem {
   static constexpr int kHalves = D / KvLayout<FP8>::kPieceElems;
-  __host__ __device__ static constexpr uint32_t half_bytes(int hg) { return hg * kStageRows * 128u; }
+  __host__ __device__ static constexpr uint32_t half_bytes(int hg) { return hg * ST * 128u; }
   __host__ __device__ static constexpr uint32_t stage_bytes(int hg) { return 2u * kHalves * half_bytes(hg); }
   __host__ __device__ static constexpr uint32_t bar_offset(int hg) { return NS * stage_bytes(hg); }
   __host__ __device__ static constexpr uint32_t mask_offset(int hg) { return bar_offset(hg) + 2u * NS * 8u; }
@@ -48,11 +49,11 @@ struct GroupedSmem {
   }
 };
 
-// The producer's issue of one stage (tokens [t0, t0 + 16) of the sequence at
+// The producer's issue of one stage (tokens [t0, t0 + ST) of the sequence at
 // table_row, clipped at tok_end) for KV heads [head0, head0 + hg): one box per
 // block piece and column half, for K and for V, all completing on `bar`.
 // Lane j handles the j-th block piece. Stores the valid-row mask to *mask.
-template <int D, bool FP8>
+template <int D, bool FP8, int ST = kStageRows>
 __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUtensorMap* tmk,
                                                   const CUtensorMap* tmv, int64_t table_row,
                                                   int head0, int hg, int t0, int tok_end,
@@ -64,7 +65,7 @@ __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUt
   int blk = 0;
   int off = 0;
   bool ok = false;
-  if (lane < a.ops_per_stage) {
+  if (lane < ST / tpo) {
     const int t = t0 + lane * tpo;
     if (t < tok_end) {
       const int j = t / a.block_size;
@@ -76,12 +77,13 @@ __device__ __forceinline__ void issue_group_stage(const DecodeArgs& a, const CUt
   }
   const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
   bool rv = false;
-  if (lane < kStageRows) {
+  if (lane < ST) {
     const int jr = lane / tpo;
     const int tok = t0 + lane;
     rv = tok < tok_end && ((okmask >> jr) & 1u);
   }
-  const uint32_t rowmask = __ballot_sync(0xffffffffu, rv) & ((1u << kStageRows) - 1u);
+  static_assert(ST == 16 || ST == 32, "stage rows");
+  const uint32_t rowmask = __ballot_sync(0xffffffffu, rv) & (ST == 32 ? 0xffffffffu : (1u << ST) - 1u);
   if (lane == 0) {
     *mask = rowmask;
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(okmask)) * tpo * hg * D * 2u *
@@ -106,11 +108,11 @@ __host__ __device__ constexpr int max_head_group(int d, int nt) { return (d > 12
 
 // Grid: ranges x (H_kv / HG) CTAs of HG + 1 warps; CTA c takes range c / nhg
 // and head group c % nhg, so the head groups of one range run side by side.
-template <bool IS_BF16, int D, int NT, int NS, int HG, int TPO, bool SPLIT_P, bool FP8>
+template <bool IS_BF16, int D, int NT, int NS, int HG, int TPO, bool SPLIT_P, bool FP8, int ST>
 __global__ void __launch_bounds__((HG + 1) * 32, 1)
     decode_grouped_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
-  using S = GroupedSmem<D, NS, FP8>;
+  using S = GroupedSmem<D, NS, FP8, ST>;
   constexpr int KD = D / 16;
   constexpr int HALVES = S::kHalves;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   const int lane = threadIdx.x & 31;
   const int N = a.num_seqs;
   const int hkv = a.num_kv_heads;
-  const int tt = kStageRows;
+  const int tt = ST;  // tokens per stage of the line
   const uint32_t half_bytes = S::half_bytes(hg);
   const uint32_t stage_bytes = S::stage_bytes(hg);
 
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
           break;
         }
       }
-      issue_group_stage<D, FP8>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, head0,
+      issue_group_stage<D, FP8, ST>(a, &tmk, &tmv, static_cast<int64_t>(ic.s) * a.max_blocks, head0,
                                 hg, ic.j * tt, ic.len, sm_base + slot * stage_bytes, half_bytes,
                                 full0 + 8 * slot, masks + slot, lane);
       cursor_next(a, pre, ic);
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
 
   // -------------------------------------------------------------- consumers
   const int kvh = head0 + warp;
-  GroupView<HG, TPO> sv;
+  GroupView<HG, TPO, ST> sv;
   sv.head_off = static_cast<uint32_t>(warp * TPO * 128);
 
   Cursor cc = cursor_at(a, pre, g0);
@@ -222,13 +224,20 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
       }
     }
     if (!aborted) {
-      sv.k = sm_base + slot * stage_bytes;
-      sv.v = sv.k + HALVES * half_bytes;
-      // E4M3: lazy maximum, and a warp vote skips its reduction on the
-      // stages where no logit passes it by more than 8 (most of them)
-      compute_stage<IS_BF16, D, NT, SPLIT_P, FP8, GroupView<HG, TPO>, NoColLimit, FP8, false, FP8>(
-          sv, sm_base, sm, masks[slot], qb, acc, ls, lane);
-      static_assert(GroupView<HG, TPO>::half_stride == S::half_bytes(HG), "layout");
+      // a stage holds ST / 16 tiles of 16 token rows; each goes through the
+      // 16-row step (rows 16h .. 16h + 15 start (16h / TPO) boxes in)
+#pragma unroll
+      for (int h = 0; h < ST / kStageRows; ++h) {
+        const uint32_t rm = (masks[slot] >> (kStageRows * h)) & ((1u << kStageRows) - 1u);
+        if (h > 0 && rm == 0u) break;  // the rest of the stage lies past the sequence
+        sv.k = sm_base + slot * stage_bytes + h * (kStageRows / TPO) * GroupView<HG, TPO, ST>::op_stride;
+        sv.v = sv.k + HALVES * half_bytes;
+        // E4M3: lazy maximum, and a warp vote skips its reduction on the
+        // stages where no logit passes it by more than 8 (most of them)
+        compute_stage<IS_BF16, D, NT, SPLIT_P, FP8, GroupView<HG, TPO, ST>, NoColLimit, FP8, false, FP8>(
+            sv, sm_base, sm, rm, qb, acc, ls, lane);
+      }
+      static_assert(GroupView<HG, TPO, ST>::half_stride == S::half_bytes(HG), "layout");
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
@@ -252,19 +261,23 @@ __global__ void __launch_bounds__((HG + 1) * 32, 1)
   }
 }
 
-// Stages in the shared ring: 64 KB stages for HG = 8 at D = 128 (HG = 4 at
-// D = 256), three of them; six of the 32 KB FP8 stages.
+// Stages in the shared ring: 16-token stages of 64 KB for HG = 8 at D = 128
+// (HG = 4 at D = 256), three of them. E4M3 stages hold 32 tokens, so they
+// carry the same bytes and each stage's fixed costs (the producer's block-id
+// read and issue, the consumers' wait and release) are paid once per 64 KB.
 template <int D, bool FP8>
 constexpr int grouped_stages() {
-  return FP8 ? 6 : 3;
+  return 3;
 }
+
 
 template <bool IS_BF16, int D, int NT, int HG, int TPO, bool FP8>
 cudaError_t launch_grouped(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                            dim3 grid, cudaStream_t st) {
   constexpr int NS = grouped_stages<D, FP8>();
-  using S = GroupedSmem<D, NS, FP8>;
-  auto kern = decode_grouped_kernel<IS_BF16, D, NT, NS, HG, TPO, true, FP8>;
+  constexpr int ST = grouped_line_tokens(FP8);
+  using S = GroupedSmem<D, NS, FP8, ST>;
+  auto kern = decode_grouped_kernel<IS_BF16, D, NT, NS, HG, TPO, true, FP8, ST>;
   const int smem = static_cast<int>(S::total(HG, a.num_seqs));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -46,7 +46,8 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeRangeRuns = 8;  // ranges one thread examines per pass
 
 // Merge of the cut pieces decode_grouped_kernel leaves as partials. The
-// equal-range split of the stage line follows from the lengths alone, so the
+// equal-range split of the stage line (stage_tokens tokens a stage, as the
+// stream kernel cut it) follows from the lengths alone, so the
 // kernel finds the cut pieces before griddepcontrol.wait, while the stream
 // kernel's last CTAs still run: it builds the stage prefix, and for each
 // range r takes its last piece - the sequence s holding stage g1(r) - 1. That
@@ -70,7 +71,7 @@ constexpr int kMergeRangeRuns = 8;  // ranges one thread examines per pass
 // kernels.
 template <int D, int R, int CB>
 __global__ void __launch_bounds__(kMergeThreads, 1)
-    decode_piece_merge_kernel(const DecodeArgs a, int64_t ranges) {
+    decode_piece_merge_kernel(const DecodeArgs a, int64_t ranges, int stage_tokens) {
   constexpr int E = D / 32;
   constexpr int W = kMergeThreads / 32;
   extern __shared__ __align__(16) unsigned char merge_smem[];
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- before the wait: the cut pieces, from the lengths alone
-  build_line_prefix(a, pre, kStageRows, warp_tot, W);
+  build_line_prefix(a, pre, stage_tokens, warp_tot, W);
   const int64_t stot = pre[N];
   int ncut = 0;
   for (int64_t r0 = 0; r0 < ranges; r0 += static_cast<int64_t>(kMergeThreads) * kMergeRangeRuns) {
@@ -236,7 +237,8 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
 }
 
 template <int D, int R, int CB>
-cudaError_t launch_merge(const DecodeArgs& a, int64_t ranges, int sms, cudaStream_t st) {
+cudaError_t launch_merge(const DecodeArgs& a, int64_t ranges, int stage_tokens, int sms,
+                         cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms), 1, 1);  // one CTA per SM
   cfg.blockDim = dim3(kMergeThreads, 1, 1);
@@ -256,26 +258,28 @@ cudaError_t launch_merge(const DecodeArgs& a, int64_t ranges, int sms, cudaStrea
                                                static_cast<int>(cfg.dynamicSmemBytes));
     if (e != cudaSuccess) return e;
   }
-  return cudaLaunchKernelEx(&cfg, kern, a, ranges);
+  return cudaLaunchKernelEx(&cfg, kern, a, ranges, stage_tokens);
 }
 
 template <int D>
-cudaError_t launch_merge_for(const DecodeArgs& a, int64_t ranges, int sms, cudaStream_t st) {
+cudaError_t launch_merge_for(const DecodeArgs& a, int64_t ranges, int stage_tokens, int sms,
+                             cudaStream_t st) {
   constexpr int E = D / 32;
   // a piece spans about ranges / N + 1 ranges when the lengths are alike
-  if (ranges >= 4LL * a.num_seqs) return launch_merge<D, 1, (E > 4 ? 16 : 32)>(a, ranges, sms, st);
-  if (a.group < 4) return launch_merge<D, 1, (E > 4 ? 2 : 4)>(a, ranges, sms, st);
-  return launch_merge<D, 4, (E > 4 ? 2 : 4)>(a, ranges, sms, st);
+  if (ranges >= 4LL * a.num_seqs)
+    return launch_merge<D, 1, (E > 4 ? 16 : 32)>(a, ranges, stage_tokens, sms, st);
+  if (a.group < 4) return launch_merge<D, 1, (E > 4 ? 2 : 4)>(a, ranges, stage_tokens, sms, st);
+  return launch_merge<D, 4, (E > 4 ? 2 : 4)>(a, ranges, stage_tokens, sms, st);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_piece_merge(const DecodeArgs& a, int head_dim, int64_t ranges,
-                                      int sms, cudaStream_t st) {
+                                      int stage_tokens, int sms, cudaStream_t st) {
   switch (head_dim) {
-    case 64: return launch_merge_for<64>(a, ranges, sms, st);
-    case 128: return launch_merge_for<128>(a, ranges, sms, st);
-    case 256: return launch_merge_for<256>(a, ranges, sms, st);
+    case 64: return launch_merge_for<64>(a, ranges, stage_tokens, sms, st);
+    case 128: return launch_merge_for<128>(a, ranges, stage_tokens, sms, st);
+    case 256: return launch_merge_for<256>(a, ranges, stage_tokens, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

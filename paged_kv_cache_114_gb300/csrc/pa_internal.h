@@ -149,10 +149,14 @@ cudaError_t launch_prefill_tc_e4m3(const CUtensorMap& tk, const CUtensorMap& tv,
 // Merges split-K partials into out (pa_decode_reduce.cu).
 cudaError_t launch_decode_reduce(const DecodeArgs& a, int head_dim, cudaStream_t st);
 // Merges the cut pieces decode_grouped_kernel left as partials (it stores them
-// without a merge); `ranges` is that launch's range count. Launched right
-// after it on the same stream, as a programmatic dependent.
-cudaError_t launch_decode_piece_merge(const DecodeArgs& a, int head_dim, int64_t ranges, int sms,
-                                      cudaStream_t st);
+// without a merge); `ranges` and `stage_tokens` are that launch's range count
+// and tokens per stage of the line. Launched right after it on the same
+// stream, as a programmatic dependent.
+cudaError_t launch_decode_piece_merge(const DecodeArgs& a, int head_dim, int64_t ranges,
+                                      int stage_tokens, int sms, cudaStream_t st);
+// Tokens per stage of the head-grouped decode kernel's line: 32 for E4M3
+// caches (64 KB stages at 8 heads), 16 otherwise.
+constexpr int grouped_line_tokens(bool fp8) { return fp8 ? 32 : kStageRows; }
 
 // Cache operations (pa_cache_ops.cu).
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
