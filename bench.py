@@ -529,6 +529,8 @@ def run_prefill(args):
     hbm_bound = args.prefill.startswith("verify")
     kernel = pa.prefill_kernel_name(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                     w.block_size, max_q, ws is not None)
+    if w.kv_dtype == "e4m3" and kernel == "prefill_tc_kernel":
+        kernel = "prefill_tc_e4m3_kernel"  # the same routing, the E4M3 instantiation
     roofline = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                  "frac": round(gbs / hbm, 4)} if hbm_bound else
                 {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_peak, "unit": "TFLOP/s",

@@ -247,12 +247,16 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
       *reinterpret_cast<uint4*>(sm + off) = row[c];
     }
   }
+  // the producer's first block-id read goes out before the start-up barrier
+  const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
+  int id_next = -1;
+  if (warp == kProducerWarp && lane < a.ops_per_stage && lane * a.tok_per_op < L)
+    id_next = __ldg(a.block_tables + table_row + (lane * a.tok_per_op) / a.block_size);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int64_t table_row = static_cast<int64_t>(s) * a.max_blocks;
   // bound of every wait that depends on a K/V tile arriving (the test hook can shorten it)
   const uint64_t wait_ns = PA_STAGE_WAIT_NS(a, kLimitTcNs);
 
@@ -260,9 +264,20 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
     // ------------------------------------------------------------ TMA producer
     const int tpo = a.tok_per_op;
     const int stop = a.test_stop_stage >= 0 && a.test_stop_stage < ntiles ? a.test_stop_stage : ntiles;
+    // lane j < ops_per_stage reads the block id of piece j of a tile; the ids
+    // of tile t + 1 are requested before tile t is issued, so no tile waits
+    // on its table read
+    auto read_id = [&](int t) {
+      int id = -1;
+      const int tok = t * kBn + lane * tpo;
+      if (lane < a.ops_per_stage && tok < L) id = __ldg(a.block_tables + table_row + tok / a.block_size);
+      return id;
+    };
     int issued = 0;
     for (; issued < stop; ++issued) {
       const int slot = issued % LS;
+      const int id_cur = id_next;
+      if (issued + 1 < stop) id_next = read_id(issued + 1);
       if (issued >= LS &&
           !wait_or_abort(kv_empty(slot), ((issued / LS) - 1) & 1, abort, wait_ns)) {
         if (lane == 0) { atomicOr(a.err, PA_DEVERR_TIMEOUT); *abort = 1u; }
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(tc_threads<FP8>(), 1)
         if (t < L) {
           const int j = t / a.block_size;
           off = t - j * a.block_size;
-          blk = __ldg(a.block_tables + table_row + j);
+          blk = id_cur;
           ok = blk >= 0 && blk < a.num_blocks;
           if (!ok) atomicOr(a.err, PA_DEVERR_BLOCK_ID);
         }
