@@ -9,8 +9,8 @@
 // A CTA = one producer warp + HG consumer warps (one per KV head of its group)
 // and owns one range of the stage line (the same equal-range split as the
 // balanced kernel, now per range x head group). The producer fills a shared
-// ring of NS stages: per stage and 64-element column half, one TMA box of
-// 64 x 16 tokens x HG heads for K and one for V. Its tensor map lists the
+// ring of NS stages: per stage, block piece and 64-element column half, one
+// TMA box of 64 x 16 tokens x HG heads for K and one for V. Its tensor map lists the
 // cache as (head_dim, token, head, block) - token before head - so the box
 // lands head-major in shared memory, [head][token][64]: each consumer's rows
 // are 16 contiguous 128-byte lines, read with the same conflict-free swizzled
@@ -25,8 +25,9 @@
 // the same stream as a programmatic dependent, merges every cut piece.
 //
 // FP8 caches: a 128-byte line holds 128 head-dim codes, so a box is 128 x 16
-// tokens x HG heads and a stage is half the bytes; the ring has twice the
-// stages to keep the same bytes in flight.
+// tokens x HG heads; a stage holds 32 tokens (ST = 32, two boxes per 16-token
+// half) to carry the same bytes as a 16-bit stage, and consumers run their
+// 16-row step twice per stage.
 #pragma once
 
 #include "pa_decode.cuh"
