@@ -62,12 +62,15 @@ DECODE = [
     (256, dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16")),
     (-1, dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, dtype="f16")),
     (-1, dict(num_q_heads=12, num_kv_heads=4, head_dim=128, block_size=4, dtype="f16")),
+    # E4M3 pool: the grouped kernel with two consumer warps per KV head
+    (-1, dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16",
+              kv_dtype="e4m3")),
 ]
 
 
 @pytest.mark.parametrize("stop", [0, 2])
 @pytest.mark.parametrize("partition,shape", DECODE,
-                         ids=["single", "split256", "grouped", "per_warp"])
+                         ids=["single", "split256", "grouped", "per_warp", "grouped_e4m3"])
 def test_decode_timeout_then_exact(dev, partition, shape, stop):
     import paged_kv_cache_114_gb300 as pa
     w = make_random_case(900 + stop, num_seqs=6, seq_lens=[6000, 3000, 300, 77, 16, 8000], **shape)
